@@ -1,0 +1,246 @@
+/*
+ * lossk.h -- C ABI of liblossk.so, a fused LM-head loss for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The loss takes hidden[n_tok][d_model] and weight[vocab][d_model] and never
+ * builds the [n_tok][vocab] logit tensor: the projection runs tile by tile on
+ * the tensor cores and each tile is reduced on chip to the per-token
+ * log-sum-exp and target logit ("Loss functions and resident-context
+ * kernels", section "lossk: the loss is where the memory goes", entries
+ * fused_linear_ce_flat and fused_linear_ce_bwd_flat).  A z-loss term lse^2
+ * and a distillation variant against a full teacher distribution follow
+ * "Fuse distillation + z-loss in the triton monolithic path (#507)", section
+ * "What it does".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Return value: a status code in 580..599 (enum lossk_status).  580 means
+ *    the work was enqueued (or the check passed).  Any other code means the
+ *    call was refused before any output was written, except 589/590, which
+ *    report a device failure.
+ *  - Buffers: every tensor argument is a caller-owned DEVICE pointer to a
+ *    contiguous row-major array; the library never allocates device memory.
+ *    Each tensor comes with its element count (`*_len`); a count shorter than
+ *    the shape needs, or a NULL required pointer, gives 582.
+ *  - dtype: LOSSK_BF16 (uint16 bf16 bits) or LOSSK_F32 (float) for hidden,
+ *    weight, logits and teacher logits.  bf16 inputs are multiplied on the
+ *    tcgen05 tensor cores with fp32 accumulation; fp32 inputs use an FFMA
+ *    path.  Per-token outputs are float, gradients are float, the three
+ *    reduced scalars are double.  The bf16 tensor path loads operands with
+ *    TMA, which needs 16-byte row pitches: d_model % 8 == 0 (and, for the
+ *    teacher logits, vocab % 8 == 0), else 591.  Every device pointer must be
+ *    16-byte aligned, else 591.
+ *  - Scratch: `workspace` is device memory of at least
+ *    lossk_workspace_bytes(...) bytes, 256-byte aligned; shorter gives 582.
+ *    Calls that share a workspace must not overlap in time.
+ *  - Streams: all device work is enqueued on `stream` (NULL = legacy default
+ *    stream).  Each compute call synchronises `stream` once, after a small
+ *    validation kernel, to read back the target-range flag and the number of
+ *    counted tokens: the call refuses bad targets (586) before the main
+ *    kernels run, the way the pages' functions validate first.  After that
+ *    point the call returns without waiting for the GPU.
+ *  - Check order (the first failing check wins): 581 empty dimension, 583
+ *    dimension over 2^24, 584 n_tok*d_model*vocab over 2^46, 587 chunk*vocab
+ *    over 2^27, 582 length / NULL pointer / short workspace, 591 alignment,
+ *    585 non-finite scalar, 588 unknown objective, 586 target out of range.
+ *  - Mask: `loss_mask` is an optional uint8[n_tok] (NULL = every token
+ *    counts; nonzero = counts).  Reductions are means over the N_valid
+ *    counted tokens; with N_valid == 0 every reduced value and gradient is 0.
+ *    A masked token's target must still lie in [0, vocab).  Per-token
+ *    outputs of a masked token: ce/loss 0, lse still written.
+ *  - Chunk: `chunk` is the pages' peak-memory knob.  It is validated
+ *    (chunk*vocab <= 2^27, else 587) but the GPU never holds a chunk of
+ *    logits: tiles live in tensor memory, and the tile schedule depends only
+ *    on the shape, so every output is bit-identical for every valid chunk.
+ *  - Determinism: no atomics on any output; the same inputs give the same
+ *    bits on every run.  The token mean is a fixed-shape double-precision
+ *    tree.
+ *  - Device waits are bounded: a kernel that waits too long sets an error
+ *    word in the workspace and exits; lossk_device_status() (and the next
+ *    call that uses the same workspace) reports it as 590.
+ */
+#ifndef LOSSK_H
+#define LOSSK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t, without pulling in the CUDA headers. */
+typedef struct CUstream_st *lossk_stream_t;
+
+/* Status vocabulary 580-599 ("Loss functions and resident-context kernels",
+ * section "Status codes").  589-591 are this library's own additions inside
+ * the same range; 592-599 are unassigned. */
+enum lossk_status {
+    LOSSK_OK = 580,
+    LOSSK_EMPTY_DIMENSION = 581,
+    LOSSK_LENGTH_MISMATCH = 582,
+    LOSSK_DIMENSION_TOO_LARGE = 583,
+    LOSSK_WORK_BUDGET_EXCEEDED = 584,
+    LOSSK_NON_FINITE_SCALAR = 585,
+    LOSSK_TARGET_OUT_OF_RANGE = 586,
+    LOSSK_CHUNK_EXCEEDS_LOGIT_BUDGET = 587,
+    LOSSK_UNKNOWN_OBJECTIVE = 588,
+    LOSSK_DEVICE_ERROR = 589,   /* a CUDA call or launch failed */
+    LOSSK_DEVICE_TIMEOUT = 590, /* a device-side wait hit its time limit */
+    LOSSK_UNALIGNED = 591       /* pointer or row pitch not 16-byte aligned */
+};
+
+enum lossk_dtype { LOSSK_F32 = 0, LOSSK_BF16 = 1 };
+
+/* Distillation objective ("Fuse distillation + z-loss ...", "What it
+ * does": cross-entropy, forward-KL, reverse-KL).  Any other value -> 588. */
+enum lossk_direction { LOSSK_DISTILL_CE = 0, LOSSK_DISTILL_FWD_KL = 1, LOSSK_DISTILL_REV_KL = 2 };
+
+/* Which call a workspace is sized for. */
+enum lossk_kind {
+    LOSSK_KIND_CE_FWD = 0,
+    LOSSK_KIND_CE_BWD = 1,
+    LOSSK_KIND_CE_FWD_BWD = 2,
+    LOSSK_KIND_FROM_LOGITS = 3,
+    LOSSK_KIND_DISTILL = 4
+};
+
+/* ---- contract: host arithmetic, no device ------------------------------- */
+
+/* Name of a status code: "ok", "empty_dimension", ... for 580-588,
+ * "device_error", "device_timeout", "unaligned" for 589-591, and
+ * "unknown_status" for anything else (never a neighbour's name).
+ * loss_status_name in the pages' function table.  Returns a static string. */
+const char *lossk_status_name(int32_t code);
+
+/* loss_dims_check: every dimension >= 1 (581) and <= 2^24 (583), and
+ * n_tok*d_model*vocab <= 2^46 (584).  The 2^24 per-dimension ceiling is this
+ * library's reading: the pages name a ceiling without printing it. */
+int32_t lossk_dims_check(int64_t n_tok, int64_t d_model, int64_t vocab);
+
+/* loss_chunk_check: chunk, vocab >= 1 (581); chunk*vocab <= 2^27 (587,
+ * refused, never clamped). */
+int32_t lossk_chunk_check(int64_t chunk, int64_t vocab);
+
+/* loss_logit_cells: chunk*vocab as a double; -1.0 if either is < 1. */
+double lossk_logit_cells(int64_t chunk, int64_t vocab);
+
+/* loss_work_fits: 1 when n_tok*d_model*vocab <= ceiling, decided by
+ * successive division (no overflow); 0 otherwise or for any argument < 1. */
+int32_t lossk_work_fits(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t ceiling);
+
+/* ce_peak_logit_cells ("Loss functions and resident-context kernels",
+ * opening example): what a chunked call holds against the materialised
+ * form.  chunked_cells = min(chunk, n_tok)*vocab, materialized_cells =
+ * n_tok*vocab, ratio = materialized/chunked, n_chunks = ceil(n_tok/chunk),
+ * status = lossk_chunk_check(chunk, vocab) (the numbers are filled in even
+ * when it is 587).  Any argument < 1: cells -1, ratio 0, n_chunks 0, 581.
+ * `out` is a host pointer; NULL gives 582.  Returns out->status. */
+typedef struct {
+    double chunked_cells;
+    double materialized_cells;
+    double ratio;
+    int64_t n_chunks;
+    int32_t status;
+} lossk_peak_cells;
+int32_t lossk_peak_logit_cells(int64_t n_tok, int64_t vocab, int64_t chunk, lossk_peak_cells *out);
+
+/* Bytes of device workspace a call of `kind` needs at this shape and dtype
+ * (a multiple of 256).  Returns -1 for a shape that lossk_dims_check
+ * refuses. */
+int64_t lossk_workspace_bytes(int32_t kind, int64_t n_tok, int64_t d_model, int64_t vocab,
+                              int32_t dtype);
+
+/* ---- device calls --------------------------------------------------------- */
+
+/* loss_targets_in_range on device data: 580 when every one of targets[0..n)
+ * lies in [0, vocab), 586 otherwise.  Synchronises `stream`. */
+int32_t lossk_targets_check(int64_t n_tok, int64_t vocab, const int64_t *targets,
+                            int64_t targets_len, void *workspace, int64_t workspace_bytes,
+                            lossk_stream_t stream);
+
+/* Fused projection + cross-entropy forward (fused_linear_ce_flat).
+ *   hidden   [n_tok][d_model]  (dtype)       weight [vocab][d_model] (dtype)
+ *   targets  int64[n_tok] in [0, vocab)      loss_mask uint8[n_tok] or NULL
+ *   z_weight >= 0: adds z_weight * lse^2 per token ("Fuse distillation +
+ *            z-loss ...": forward scalar log_sum_exp^2)
+ * Outputs (device):
+ *   lse_out     float[n_tok], required: log-sum-exp of each token's logits
+ *               (the backward takes it back)
+ *   ce_out      float[n_tok] or NULL: lse - target logit (0 if masked)
+ *   scalars_out double[3], required: {total, ce_mean, z_mean} with
+ *               total = sum_t m_t (ce_t + z_weight lse_t^2) / N_valid. */
+int32_t lossk_ce_fwd(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk, int32_t dtype,
+                     const void *hidden, int64_t hidden_len, const void *weight, int64_t weight_len,
+                     const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                     double z_weight, float *lse_out, float *ce_out, double *scalars_out,
+                     void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
+/* Backward of grad_scale * total (fused_linear_ce_bwd_flat; not chunked).
+ * Takes lse from lossk_ce_fwd on the same inputs.  Recomputes the logit
+ * tiles, forms grad_logits = a_t((1 + 2 z_weight lse_t) softmax - onehot),
+ * a_t = grad_scale m_t / N_valid, in registers, and folds it into
+ *   d_hidden float[n_tok][d_model] = G W      (NULL to skip)
+ *   d_weight float[vocab][d_model] = G^T H    (NULL to skip)
+ * Both are overwritten (not accumulated). */
+int32_t lossk_ce_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int32_t dtype,
+                     const void *hidden, int64_t hidden_len, const void *weight, int64_t weight_len,
+                     const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                     double z_weight, double grad_scale, const float *lse, int64_t lse_len,
+                     float *d_hidden, float *d_weight, void *workspace, int64_t workspace_bytes,
+                     lossk_stream_t stream);
+
+/* lossk_ce_fwd followed by lossk_ce_bwd on the same inputs, with one
+ * validation sync instead of two: the training-step call.  lse_out is
+ * required (it is also the backward's input). */
+int32_t lossk_ce_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
+                         int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight,
+                         int64_t weight_len, const int64_t *targets, int64_t targets_len,
+                         const uint8_t *loss_mask, double z_weight, double grad_scale,
+                         float *lse_out, float *ce_out, double *scalars_out, float *d_hidden,
+                         float *d_weight, void *workspace, int64_t workspace_bytes,
+                         lossk_stream_t stream);
+
+/* Cross-entropy from materialised logits [n_tok][vocab] (ce_from_logits_flat).
+ * Same outputs as lossk_ce_fwd; grad_logits (same dtype as logits, or NULL)
+ * receives grad_scale * d total / d logits. */
+int32_t lossk_ce_from_logits(int64_t n_tok, int64_t vocab, int32_t dtype, const void *logits,
+                             int64_t logits_len, const int64_t *targets, int64_t targets_len,
+                             const uint8_t *loss_mask, double z_weight, double grad_scale,
+                             float *lse_out, float *ce_out, double *scalars_out, void *grad_logits,
+                             int64_t grad_len, void *workspace, int64_t workspace_bytes,
+                             lossk_stream_t stream);
+
+/* Distillation against a full teacher distribution, forward and backward in
+ * one call ("Fuse distillation + z-loss ...", "What it does").  With
+ * a = logits/T, b = teacher/T, q = softmax(a), p = softmax(b):
+ *   LOSSK_DISTILL_CE:     L_t = -sum p log q
+ *   LOSSK_DISTILL_FWD_KL: L_t = sum p (log p - log q)
+ *   LOSSK_DISTILL_REV_KL: L_t = sum q (log q - log p)
+ *   z_t = lse(a)^2 over the same student softmax
+ *   total = sum_t m_t (L_t + z_weight z_t) / N_valid
+ * Gradients of grad_scale * total: d/dlogits = (q - p)/T (CE, fKL) or
+ * q (log q - log p - L_t)/T (rKL), plus 2 z_weight lse(a) q / T; no T^2
+ * factor.  temperature must be finite and > 0 (585).
+ *   teacher_logits [n_tok][vocab] (dtype)
+ *   scalars_out double[3] {total, distill_mean, z_mean}, required
+ *   per_token_out float[n_tok] or NULL: L_t (0 if masked)
+ *   lse_out float[n_tok] or NULL: lse(a)
+ *   d_hidden, d_weight: float gradients or NULL to skip. */
+int32_t lossk_distill_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
+                              int32_t dtype, const void *hidden, int64_t hidden_len,
+                              const void *weight, int64_t weight_len, const void *teacher_logits,
+                              int64_t teacher_len, const uint8_t *loss_mask, int32_t direction,
+                              double temperature, double z_weight, double grad_scale,
+                              double *scalars_out, float *per_token_out, float *lse_out,
+                              float *d_hidden, float *d_weight, void *workspace,
+                              int64_t workspace_bytes, lossk_stream_t stream);
+
+/* Synchronises `stream`, then reports and clears the workspace's device
+ * error word: 580 (none), 590 (a bounded device wait timed out) or 589. */
+int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOSSK_H */

@@ -1,0 +1,636 @@
+// k_simt.cu -- the CUDA-core kernels of the fused LM-head loss:
+//   validate       target-range guard and counted-token count
+//                  ("Loss functions and resident-context kernels", lossk
+//                  function table: loss_targets_in_range)
+//   merge_ce       per token: combine the per-tile (max, sum-exp) partials in
+//                  tile order into lse, then ce = lse - target logit and
+//                  z = lse^2 ("Fuse distillation + z-loss ...", "What it does")
+//   merge_distill  the same for the student/teacher pair and the three
+//                  distillation objectives, plus the backward parameters
+//   reduce         fixed-shape double-precision tree over tokens -> the means
+//   tokp_ce        per-token backward parameters of the label loss
+//   sum_splits     d_hidden partials of the vocabulary splits, in split order
+//   from_logits    cross-entropy from materialised logits (ce_from_logits_flat):
+//                  a row-streaming, HBM-bound kernel with an optional
+//                  grad_logits write
+//   fp_kernel      the fp32 inputs path: the same three passes as the tensor
+//                  core kernel (statistics, d_hidden, d_weight) on FFMA tiles.
+#include "lossk_internal.h"
+#include "ptx.cuh"
+
+#include <cfloat>
+
+namespace lossk {
+
+// ---------------------------------------------------------------------------
+__global__ void validate_kernel(const int64_t *__restrict__ targets, const uint8_t *__restrict__ mask,
+                                int64_t n, int64_t V, WsHeader *hdr)
+{
+    int bad = 0, valid = 0;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < n;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (targets) {
+            const int64_t y = targets[t];
+            bad += (y < 0 || y >= V) ? 1 : 0;
+        }
+        valid += mask ? (mask[t] != 0) : 1;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        valid += __shfl_xor_sync(0xffffffffu, valid, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (bad) atomicAdd(&hdr->bad_targets, bad);
+        if (valid) atomicAdd(&hdr->n_valid, valid);
+    }
+}
+
+cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
+                            WsHeader *hdr, cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 2 * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    int grid = static_cast<int>((n + 255) / 256);
+    if (grid > 1024) grid = 1024;
+    validate_kernel<<<grid, 256, 0, st>>>(targets, mask, n, V, hdr);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+__global__ void merge_ce_kernel(const float *__restrict__ part, const float *__restrict__ tgt,
+                                const int64_t *__restrict__ targets, const uint8_t *__restrict__ mask,
+                                int64_t n, int64_t n_ct, int64_t n_pad, double wz,
+                                float *__restrict__ lse_out, float *__restrict__ ce_out,
+                                double *__restrict__ tokacc)
+{
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= n) return;
+    const float *m2 = part;
+    const float *z = part + n_ct * n_pad;
+    float M = -INFINITY;
+    for (int64_t c = 0; c < n_ct; ++c) M = fmaxf(M, m2[c * n_pad + t]);
+    double Z = 0.0;
+    for (int64_t c = 0; c < n_ct; ++c)
+        Z += static_cast<double>(z[c * n_pad + t]) * exp2(static_cast<double>(m2[c * n_pad + t]) - M);
+    const double lse = (static_cast<double>(M) + log2(Z)) * LN2;
+    const bool on = mask ? (mask[t] != 0) : true;
+    const double ce = on ? lse - static_cast<double>(tgt[t]) : 0.0;
+    const double zz = on ? lse * lse : 0.0;
+    lse_out[t] = static_cast<float>(lse);
+    if (ce_out) ce_out[t] = static_cast<float>(ce);
+    tokacc[t] = ce + wz * zz;
+    tokacc[n_pad + t] = ce;
+    tokacc[2 * n_pad + t] = zz;
+    (void)targets;
+}
+
+cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
+                            const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
+                            double wz, float *lse_out, float *ce_out, double *tokacc,
+                            cudaStream_t st)
+{
+    merge_ce_kernel<<<static_cast<int>((n + 127) / 128), 128, 0, st>>>(
+        part, tgt, targets, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+__global__ void merge_distill_kernel(const float *__restrict__ part, const uint8_t *__restrict__ mask,
+                                     int64_t n, int64_t n_ct, int64_t n_pad, int direction,
+                                     double wz, float *__restrict__ lse_out,
+                                     float *__restrict__ per_token, double *__restrict__ tokacc,
+                                     float4 *__restrict__ tokp, double alpha, double temperature)
+{
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= n_pad) return;
+    if (t >= n) {
+        tokp[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int64_t pl = n_ct * n_pad;
+    const float *ms = part, *zs = part + pl, *mt = part + 2 * pl, *zt = part + 3 * pl,
+                *xx = part + 4 * pl;
+    float Ms = -INFINITY, Mt = -INFINITY;
+    for (int64_t c = 0; c < n_ct; ++c) {
+        Ms = fmaxf(Ms, ms[c * n_pad + t]);
+        Mt = fmaxf(Mt, mt[c * n_pad + t]);
+    }
+    double Zs = 0.0, Zt = 0.0, X = 0.0;
+    for (int64_t c = 0; c < n_ct; ++c) {
+        const int64_t o = c * n_pad + t;
+        const double fs = exp2(static_cast<double>(ms[o]) - Ms);
+        const double ft = exp2(static_cast<double>(mt[o]) - Mt);
+        Zs += zs[o] * fs;
+        Zt += zt[o] * ft;
+        X += xx[o] * (direction == DIR_RKL ? fs : ft);
+    }
+    const double lse_s = (static_cast<double>(Ms) + log2(Zs)) * LN2;
+    const double lse_t = (static_cast<double>(Mt) + log2(Zt)) * LN2;
+    const double E = LN2 * X / (direction == DIR_RKL ? Zs : Zt);
+    double L;
+    if (direction == DIR_CE) L = lse_s - E;
+    else if (direction == DIR_FKL) L = E + lse_s - lse_t;
+    else L = E - lse_s + lse_t;
+    const bool on = mask ? (mask[t] != 0) : true;
+    const double Lm = on ? L : 0.0;
+    const double zz = on ? lse_s * lse_s : 0.0;
+    if (lse_out) lse_out[t] = static_cast<float>(lse_s);
+    if (per_token) per_token[t] = static_cast<float>(Lm);
+    tokacc[t] = Lm + wz * zz;
+    tokacc[n_pad + t] = Lm;
+    tokacc[2 * n_pad + t] = zz;
+    const double at = on ? alpha / temperature : 0.0;
+    float4 P;
+    P.x = static_cast<float>(lse_s * LOG2E);
+    P.y = static_cast<float>(lse_t * LOG2E);
+    if (direction == DIR_RKL) {
+        P.z = static_cast<float>(at);
+        P.w = static_cast<float>(lse_t - lse_s - L + 2.0 * wz * lse_s);
+    } else {
+        P.z = static_cast<float>(at * (1.0 + 2.0 * wz * lse_s));
+        P.w = static_cast<float>(at);
+    }
+    tokp[t] = P;
+}
+
+cudaError_t launch_merge_distill(const float *part, const uint8_t *mask, int64_t n, int64_t n_ct,
+                                 int64_t n_pad, int direction, double wz, float *lse_out,
+                                 float *per_token, double *tokacc, float4 *tokp, double alpha,
+                                 double temperature, cudaStream_t st)
+{
+    merge_distill_kernel<<<static_cast<int>((n_pad + 127) / 128), 128, 0, st>>>(
+        part, mask, n, n_ct, n_pad, direction, wz, lse_out, per_token, tokacc, tokp, alpha,
+        temperature);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-shape tree: thread i sums tokens i, i+1024, i+2048, ... in that
+// order, then the 1024 partials are added pairwise (i += i + stride, stride
+// halving).  The shape depends on n only, so the result is the same bits for
+// every chunk, grid and run.
+__global__ void __launch_bounds__(1024) reduce_kernel(const double *__restrict__ tokacc, int64_t n,
+                                                      int64_t n_pad, const WsHeader *hdr,
+                                                      double *__restrict__ out)
+{
+    __shared__ double sh[3][1024];
+    const int i = threadIdx.x;
+    for (int s = 0; s < 3; ++s) {
+        double acc = 0.0;
+        for (int64_t t = i; t < n; t += 1024) acc += tokacc[s * n_pad + t];
+        sh[s][i] = acc;
+    }
+    __syncthreads();
+    for (int stride = 512; stride > 0; stride >>= 1) {
+        if (i < stride)
+            for (int s = 0; s < 3; ++s) sh[s][i] += sh[s][i + stride];
+        __syncthreads();
+    }
+    if (i == 0) {
+        const int nv = hdr->n_valid;
+        for (int s = 0; s < 3; ++s) out[s] = nv > 0 ? sh[s][0] / nv : 0.0;
+    }
+}
+
+cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
+                          double wz, double *scalars_out, cudaStream_t st)
+{
+    (void)wz;
+    reduce_kernel<<<1, 1024, 0, st>>>(tokacc, n, n_pad, hdr, scalars_out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+__global__ void tokp_ce_kernel(const float *__restrict__ lse, const int64_t *__restrict__ targets,
+                               const uint8_t *__restrict__ mask, int64_t n, int64_t n_pad,
+                               double alpha, double wz, float4 *__restrict__ tokp)
+{
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= n_pad) return;
+    if (t >= n) {
+        tokp[t] = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+        return;
+    }
+    const double l = lse[t];
+    const double at = (mask ? (mask[t] != 0) : true) ? alpha : 0.0;
+    tokp[t] = make_float4(static_cast<float>(l * LOG2E), static_cast<float>(at * (1.0 + 2.0 * wz * l)),
+                          static_cast<float>(at), __int_as_float(static_cast<int>(targets[t])));
+}
+
+cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,
+                           int64_t n, int64_t n_pad, double alpha, double wz, float4 *tokp,
+                           cudaStream_t st)
+{
+    tokp_ce_kernel<<<static_cast<int>((n_pad + 127) / 128), 128, 0, st>>>(lse, targets, mask, n,
+                                                                          n_pad, alpha, wz, tokp);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+__global__ void sum_splits_kernel(const float4 *__restrict__ part, int64_t nsplit, int64_t count4,
+                                  float4 *__restrict__ out)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 acc = part[i];
+        for (int64_t s = 1; s < nsplit; ++s) {
+            const float4 v = part[s * count4 + i];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        out[i] = acc;
+    }
+}
+
+cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
+                              cudaStream_t st)
+{
+    const int64_t c4 = count / 4;  // count is a multiple of 4 (d_model % 8 == 0)
+    int64_t grid = (c4 + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    sum_splits_kernel<<<static_cast<int>(grid), 256, 0, st>>>(
+        reinterpret_cast<const float4 *>(part), nsplit, c4, reinterpret_cast<float4 *>(out));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Cross-entropy from materialised logits.  One 512-thread block per row:
+// pass 1 streams the row with 16-byte loads and keeps an online (max, sum)
+// per thread, merged by a fixed tree; pass 2 (optional) writes grad_logits.
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<uint16_t> { static constexpr int N = 8; };
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T *p, float *f);
+template <>
+__device__ __forceinline__ void load_vec<float>(const float *p, float *f)
+{
+    const float4 v = __ldcs(reinterpret_cast<const float4 *>(p));
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *p, float *f)
+{
+    const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void online_add(float &m, float &z, float x2)
+{
+    if (x2 > m) {
+        z = z * ex2_approx(m - x2) + 1.f;
+        m = x2;
+    } else {
+        z += ex2_approx(x2 - m);
+    }
+}
+
+__device__ __forceinline__ void online_merge(float &m, float &z, float m_o, float z_o)
+{
+    const float M = fmaxf(m, m_o);
+    if (M == -INFINITY) return;
+    z = z * ex2_approx(m - M) + z_o * ex2_approx(m_o - M);
+    m = M;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) from_logits_kernel(const T *__restrict__ logits,
+                                                          const int64_t *__restrict__ targets,
+                                                          const uint8_t *__restrict__ mask, int64_t V,
+                                                          double wz, double alpha,
+                                                          float *__restrict__ lse_out,
+                                                          float *__restrict__ ce_out,
+                                                          double *__restrict__ tokacc, int64_t n_pad,
+                                                          T *__restrict__ grad)
+{
+    constexpr int NV = Vec<T>::N;
+    const int64_t t = blockIdx.x;
+    const T *x = logits + t * V;
+    const float L2E = static_cast<float>(LOG2E);
+    const bool vec_ok = ((V * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    float m = -INFINITY, z = 0.f;
+    if (vec_ok) {
+        const int64_t nvec = V / NV;
+        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float f[NV];
+            load_vec<T>(x + i * NV, f);
+#pragma unroll
+            for (int u = 0; u < NV; ++u) online_add(m, z, f[u] * L2E);
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < V; i += blockDim.x) online_add(m, z, to_f(x[i]) * L2E);
+    }
+    // fixed-shape merge: warp butterfly, then warp 0 over the 16 warp results
+    for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+        const float zo = __shfl_xor_sync(0xffffffffu, z, o);
+        online_merge(m, z, mo, zo);
+    }
+    __shared__ float sm[16], sz[16];
+    __shared__ float s_lse2;
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { sm[w] = m; sz[w] = z; }
+    __syncthreads();
+    if (w == 0) {
+        m = l < 16 ? sm[l] : -INFINITY;
+        z = l < 16 ? sz[l] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+            const float zo = __shfl_xor_sync(0xffffffffu, z, o);
+            online_merge(m, z, mo, zo);
+        }
+        if (l == 0) {
+            const double lse = (static_cast<double>(m) + log2(static_cast<double>(z))) * LN2;
+            const bool on = mask ? (mask[t] != 0) : true;
+            const double ce = on ? lse - static_cast<double>(to_f(x[targets[t]])) : 0.0;
+            const double zz = on ? lse * lse : 0.0;
+            lse_out[t] = static_cast<float>(lse);
+            if (ce_out) ce_out[t] = static_cast<float>(ce);
+            tokacc[t] = ce + wz * zz;
+            tokacc[n_pad + t] = ce;
+            tokacc[2 * n_pad + t] = zz;
+            s_lse2 = static_cast<float>(lse * LOG2E);
+        }
+    }
+    if (!grad) return;
+    __syncthreads();
+    const float lse2 = s_lse2;
+    const bool on = mask ? (mask[t] != 0) : true;
+    const float at = on ? static_cast<float>(alpha) : 0.f;
+    const float c = on ? static_cast<float>(alpha * (1.0 + 2.0 * wz * lse2 * LN2)) : 0.f;
+    const int64_t y = targets[t];
+    T *g = grad + t * V;
+    for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
+        float gv = c * ex2_approx(fmaf(to_f(x[i]), L2E, -lse2));
+        if (i == y) gv -= at;
+        if constexpr (sizeof(T) == 4) {
+            g[i] = gv;
+        } else {
+            g[i] = static_cast<uint16_t>(pack_bf16x2(gv, 0.f) & 0xFFFFu);
+        }
+    }
+}
+
+cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *targets,
+                               const uint8_t *mask, int64_t n, int64_t V, double wz,
+                               double alpha, float *lse_out, float *ce_out, double *tokacc,
+                               void *grad, cudaStream_t st)
+{
+    const int64_t n_pad = (n + TC_BM - 1) / TC_BM * TC_BM;
+    if (dtype == 1)
+        from_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const uint16_t *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
+            tokacc, n_pad, static_cast<uint16_t *>(grad));
+    else
+        from_logits_kernel<float><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const float *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
+            tokacc, n_pad, static_cast<float *>(grad));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// fp32 FFMA path.  256 threads (16 x 16), 64 x 64 logit tiles, 4 x 4 per
+// thread; the contraction over d_model is staged through shared memory in
+// steps of 16 and summed in ascending k.  Modes mirror the tensor-core
+// kernel: STATS writes per-tile partial statistics, ROWS/COLS rebuild the
+// gradient tile in shared memory (fp32, never rounded) and accumulate
+// G . Y[:, slice] over the loop of Y tiles.
+template <int MODE, bool DISTILL>
+__global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
+                                                 const float *__restrict__ Y,
+                                                 const float *__restrict__ teach, int n_x, int n_y,
+                                                 int d, int n_tok, int vocab, int n_split,
+                                                 int direction, float inv_t,
+                                                 const int64_t *__restrict__ targets,
+                                                 const float4 *__restrict__ tokp,
+                                                 float *__restrict__ part, float *__restrict__ tgt,
+                                                 int64_t part_stride, int64_t part_plane,
+                                                 float *__restrict__ out, int64_t out_split_stride)
+{
+    __shared__ float xs[FP_BK][FP_BM + 4];
+    __shared__ float ys[FP_BK][FP_BN + 4];
+    __shared__ float gs[FP_BM][FP_BN + 1];
+    __shared__ float yv[FP_BN][FP_SLICE + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const float L2E = static_cast<float>(LOG2E);
+    const int n_xt = (n_x + FP_BM - 1) / FP_BM, n_yt = (n_y + FP_BN - 1) / FP_BN;
+
+    int xt, yt_begin, yt_end, slice = 0, split = 0;
+    if (MODE == TC_STATS) {
+        xt = blockIdx.x % n_xt;
+        yt_begin = blockIdx.x / n_xt;
+        yt_end = yt_begin + 1;
+    } else {
+        const int n_sl = (d + FP_SLICE - 1) / FP_SLICE;
+        int b = blockIdx.x;
+        slice = b % n_sl;
+        b /= n_sl;
+        xt = b % n_xt;
+        split = b / n_xt;
+        yt_begin = static_cast<int>((static_cast<int64_t>(split) * n_yt) / n_split);
+        yt_end = static_cast<int>((static_cast<int64_t>(split + 1) * n_yt) / n_split);
+    }
+    const int xrow0 = xt * FP_BM;
+    float acc[4][4] = {};
+
+    for (int yt = yt_begin; yt < yt_end; ++yt) {
+        const int ycol0 = yt * FP_BN;
+        float s[4][4] = {};
+        for (int k0 = 0; k0 < d; k0 += FP_BK) {
+            for (int e = threadIdx.x; e < FP_BM * FP_BK; e += 256) {
+                const int rr = e / FP_BK, kk = e % FP_BK;
+                const int gx = xrow0 + rr, gy = ycol0 + rr, gk = k0 + kk;
+                xs[kk][rr] = (gx < n_x && gk < d) ? X[static_cast<int64_t>(gx) * d + gk] : 0.f;
+                ys[kk][rr] = (gy < n_y && gk < d) ? Y[static_cast<int64_t>(gy) * d + gk] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < FP_BK; ++kk) {
+                float xa[4], yb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xa[i] = xs[kk][ty * 4 + i];
+                    yb[i] = ys[kk][tx * 4 + i];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) s[i][jx] = fmaf(xa[i], yb[jx], s[i][jx]);
+            }
+            __syncthreads();
+        }
+        if (MODE == TC_STATS) {
+            // rows ty*4+i, columns tx*4+jx; a row's 64 columns live in 16
+            // lanes of one half-warp
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = xrow0 + ty * 4 + i;
+                float vs[4], vt[4];
+#pragma unroll
+                for (int jx = 0; jx < 4; ++jx) {
+                    const int v = ycol0 + tx * 4 + jx;
+                    const bool in = v < vocab && t < n_tok;
+                    vs[jx] = in ? s[i][jx] : -INFINITY;
+                    vt[jx] = (DISTILL && in) ? teach[static_cast<int64_t>(t) * vocab + v] : -INFINITY;
+                }
+                if (!DISTILL) {
+                    float m = -INFINITY, z = 0.f;
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) m = fmaxf(m, vs[jx] * L2E);
+                    for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) z += exp2f(vs[jx] * L2E - m);
+                    for (int o = 1; o < 16; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                    if (t < n_tok) {
+                        if (tx == 0) {
+                            const int64_t o = static_cast<int64_t>(yt) * part_stride + t;
+                            part[o] = m;
+                            part[part_plane + o] = z;
+                        }
+                        const int64_t rel = targets[t] - ycol0 - tx * 4;
+#pragma unroll
+                        for (int jx = 0; jx < 4; ++jx)
+                            if (rel == jx) tgt[t] = s[i][jx];
+                    }
+                } else {
+                    float a2[4], b2[4], ms = -INFINITY, mt = -INFINITY;
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) {
+                        a2[jx] = vs[jx] * inv_t * L2E;
+                        b2[jx] = vt[jx] * inv_t * L2E;
+                        ms = fmaxf(ms, a2[jx]);
+                        mt = fmaxf(mt, b2[jx]);
+                    }
+                    for (int o = 1; o < 16; o <<= 1) {
+                        ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+                        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    }
+                    float zs = 0.f, zt = 0.f, xx = 0.f;
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) {
+                        if (vs[jx] == -INFINITY) continue;
+                        const float es = exp2f(a2[jx] - ms), et = exp2f(b2[jx] - mt);
+                        zs += es;
+                        zt += et;
+                        if (direction == DIR_CE) xx = fmaf(et, a2[jx], xx);
+                        else if (direction == DIR_FKL) xx = fmaf(et, b2[jx] - a2[jx], xx);
+                        else xx = fmaf(es, a2[jx] - b2[jx], xx);
+                    }
+                    for (int o = 1; o < 16; o <<= 1) {
+                        zs += __shfl_xor_sync(0xffffffffu, zs, o);
+                        zt += __shfl_xor_sync(0xffffffffu, zt, o);
+                        xx += __shfl_xor_sync(0xffffffffu, xx, o);
+                    }
+                    if (t < n_tok && tx == 0) {
+                        const int64_t o = static_cast<int64_t>(yt) * part_stride + t;
+                        part[o] = ms;
+                        part[part_plane + o] = zs;
+                        part[2 * part_plane + o] = mt;
+                        part[3 * part_plane + o] = zt;
+                        part[4 * part_plane + o] = xx;
+                    }
+                }
+            }
+        } else {
+            // gradient tile (rows of X by columns of Y) into shared memory
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int jx = 0; jx < 4; ++jx) {
+                    const int xr = xrow0 + ty * 4 + i, yc = ycol0 + tx * 4 + jx;
+                    const int tok = (MODE == TC_ROWS) ? xr : yc;
+                    const int voc = (MODE == TC_ROWS) ? yc : xr;
+                    float g = 0.f;
+                    if (tok < n_tok && voc < vocab) {
+                        const float4 P = tokp[tok];
+                        const float sv = s[i][jx];
+                        if (!DISTILL) {
+                            g = P.y * exp2f(fmaf(sv, L2E, -P.x));
+                            if (__float_as_int(P.w) == voc) g -= P.z;
+                        } else {
+                            const float a2v = sv * inv_t * L2E;
+                            const float b2v = teach[static_cast<int64_t>(tok) * vocab + voc] * inv_t * L2E;
+                            const float qv = exp2f(a2v - P.x);
+                            if (direction == DIR_RKL)
+                                g = P.z * qv * fmaf(a2v - b2v, static_cast<float>(LN2), P.w);
+                            else
+                                g = P.z * qv - P.w * exp2f(b2v - P.y);
+                        }
+                    }
+                    gs[ty * 4 + i][tx * 4 + jx] = g;
+                }
+            }
+            // Y[ycol0 .. +64][slice cols]
+            for (int e = threadIdx.x; e < FP_BN * FP_SLICE; e += 256) {
+                const int rr = e / FP_SLICE, cc = e % FP_SLICE;
+                const int gy = ycol0 + rr, gc = slice * FP_SLICE + cc;
+                yv[rr][cc] = (gy < n_y && gc < d) ? Y[static_cast<int64_t>(gy) * d + gc] : 0.f;
+            }
+            __syncthreads();
+            for (int kk = 0; kk < FP_BN; ++kk) {
+                float ga[4], yb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ga[i] = gs[ty * 4 + i][kk];
+                    yb[i] = yv[kk][tx * 4 + i];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) acc[i][jx] = fmaf(ga[i], yb[jx], acc[i][jx]);
+            }
+            __syncthreads();
+        }
+    }
+    if (MODE != TC_STATS) {
+        float *o = out + static_cast<int64_t>(split) * out_split_stride;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int xr = xrow0 + ty * 4 + i;
+            if (xr >= n_x) continue;
+#pragma unroll
+            for (int jx = 0; jx < 4; ++jx) {
+                const int c = slice * FP_SLICE + tx * 4 + jx;
+                if (c < d) o[static_cast<int64_t>(xr) * d + c] = acc[i][jx];
+            }
+        }
+    }
+}
+
+cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
+                      int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
+                      float inv_t, const int64_t *targets, const float4 *tokp, float *part,
+                      float *tgt, int64_t part_stride, int64_t part_plane, float *out,
+                      int64_t out_split_stride, cudaStream_t st)
+{
+    const int n_xt = (n_x + FP_BM - 1) / FP_BM, n_yt = (n_y + FP_BN - 1) / FP_BN;
+    const int n_sl = (d + FP_SLICE - 1) / FP_SLICE;
+    const int64_t grid64 = mode == TC_STATS ? static_cast<int64_t>(n_xt) * n_yt
+                                            : static_cast<int64_t>(n_xt) * n_sl * n_split;
+    const unsigned grid = static_cast<unsigned>(grid64);
+    const float *x = static_cast<const float *>(X), *y = static_cast<const float *>(Y);
+#define LOSSK_FP(M, D)                                                                             \
+    fp_kernel<M, D><<<grid, 256, 0, st>>>(x, y, teach, n_x, n_y, d, n_tok, vocab, n_split,       \
+                                          direction, inv_t, targets, tokp, part, tgt, part_stride, \
+                                          part_plane, out, out_split_stride)
+    if (mode == TC_STATS) {
+        if (distill) LOSSK_FP(TC_STATS, true); else LOSSK_FP(TC_STATS, false);
+    } else if (mode == TC_ROWS) {
+        if (distill) LOSSK_FP(TC_ROWS, true); else LOSSK_FP(TC_ROWS, false);
+    } else {
+        if (distill) LOSSK_FP(TC_COLS, true); else LOSSK_FP(TC_COLS, false);
+    }
+#undef LOSSK_FP
+    return cudaGetLastError();
+}
+
+} // namespace lossk

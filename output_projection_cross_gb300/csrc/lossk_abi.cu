@@ -1,0 +1,559 @@
+// lossk_abi.cu -- the extern "C" entry points of liblossk.so (declared in
+// include/lossk.h): the host contract arithmetic, argument checks in the
+// documented order, workspace layout, tensor-map encoding and the launch
+// sequence of each call.  No device memory is allocated here.
+#include "../../include/lossk.h"
+#include "lossk_internal.h"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+using namespace lossk;
+
+namespace {
+
+// Ceilings: 2^46 work cells and 2^27 logit cells are the pages' constants
+// ("Loss functions and resident-context kernels", lossk function table); the
+// per-dimension ceiling 2^24 is this library's reading of the unprinted one.
+constexpr int64_t MAX_WORK_CELLS = int64_t(1) << 46;
+constexpr int64_t MAX_LOGIT_CELLS = int64_t(1) << 27;
+constexpr int64_t MAX_DIM = int64_t(1) << 24;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A 2-D bf16 tensor [outer][inner] (row pitch inner*2 bytes) read in boxes of
+// {box_inner, box_outer} with the 128-byte swizzle; out-of-range elements
+// read as zero.
+bool make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, uint32_t box_inner,
+              uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Hdr {
+    int err, bad, n_valid;
+};
+
+int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DEVICE_ERROR; }
+
+// Run the validation kernel and read its result back (the one sync of a call).
+int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V, WsHeader *hdr,
+                 cudaStream_t st, Hdr *h)
+{
+    if (launch_validate(targets, mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    int buf[3] = {0, 0, 0};
+    if (cudaMemcpyAsync(buf, hdr, sizeof(buf), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    h->err = buf[0];
+    h->bad = buf[1];
+    h->n_valid = buf[2];
+    if (h->err) return LOSSK_DEVICE_TIMEOUT;
+    if (h->bad) return LOSSK_TARGET_OUT_OF_RANGE;
+    return LOSSK_OK;
+}
+
+bool is_finite(double x) { return std::isfinite(x); }
+
+struct Ws {
+    WsLayout L;
+    uint8_t *base;
+    WsHeader *hdr() const { return reinterpret_cast<WsHeader *>(base); }
+    float4 *tokp() const { return reinterpret_cast<float4 *>(base + L.off_tokp); }
+    float *tgt() const { return reinterpret_cast<float *>(base + L.off_tgt); }
+    double *tokacc() const { return reinterpret_cast<double *>(base + L.off_tokacc); }
+    float *part() const { return reinterpret_cast<float *>(base + L.off_part); }
+    float *dhpart() const { return reinterpret_cast<float *>(base + L.off_dhpart); }
+};
+
+// ---- the forward statistics pass + merge + reduction (label CE) ------------
+int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
+                   const void *W, const int64_t *targets, const uint8_t *mask, double wz,
+                   float *lse_out, float *ce_out, double *scalars, cudaStream_t st)
+{
+    const WsLayout &L = w.L;
+    cudaError_t e;
+    if (dtype == LOSSK_BF16) {
+        TcArgs a;
+        std::memset(&a, 0, sizeof(a));
+        if (!make_map(&a.map_x, H, d, n, 64, TC_BM) || !make_map(&a.map_y, W, d, V, 64, TC_BN_FWD))
+            return LOSSK_DEVICE_ERROR;
+        a.n_x = static_cast<int>(n);
+        a.n_y = static_cast<int>(V);
+        a.d = static_cast<int>(d);
+        a.n_tok = static_cast<int>(n);
+        a.vocab = static_cast<int>(V);
+        a.n_xt = static_cast<int>(cdiv(n, TC_BM));
+        a.n_yt = static_cast<int>(L.n_ct);
+        a.n_items = a.n_xt * a.n_yt;
+        a.targets = targets;
+        a.part = w.part();
+        a.tgt = w.tgt();
+        a.part_stride = L.n_pad;
+        a.part_plane = L.n_ct * L.n_pad;
+        a.err = &w.hdr()->err;
+        const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        e = launch_tc(TC_STATS, false, a, grid, st);
+    } else {
+        e = launch_fp(TC_STATS, false, H, W, nullptr, static_cast<int>(n), static_cast<int>(V),
+                      static_cast<int>(d), static_cast<int>(n), static_cast<int>(V), 1, 0, 1.f,
+                      targets, nullptr, w.part(), w.tgt(), L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    e = launch_merge_ce(w.part(), w.tgt(), targets, mask, n, L.n_ct, L.n_pad, wz, lse_out, ce_out,
+                        w.tokacc(), st);
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    return status_of(launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st));
+}
+
+// ---- the two accumulate passes (d_hidden, d_weight), label CE or distill ----
+int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
+                const void *W, const void *teacher, bool distill, int direction, double temperature,
+                float *d_hidden, float *d_weight, cudaStream_t st)
+{
+    const WsLayout &L = w.L;
+    cudaError_t e = cudaSuccess;
+    const float inv_t = static_cast<float>(1.0 / temperature);
+    if (dtype == LOSSK_BF16) {
+        for (int pass = 0; pass < 2; ++pass) {
+            float *dst = pass == 0 ? d_hidden : d_weight;
+            if (!dst) continue;
+            const bool rows = pass == 0;
+            TcArgs a;
+            std::memset(&a, 0, sizeof(a));
+            const void *X = rows ? H : W, *Y = rows ? W : H;
+            const int64_t nx = rows ? n : V, ny = rows ? V : n;
+            if (!make_map(&a.map_x, X, d, nx, 64, TC_BM) || !make_map(&a.map_y, Y, d, ny, 64, TC_BN_ACC) ||
+                !make_map(&a.map_ys, Y, d, ny, 64, 64))
+                return LOSSK_DEVICE_ERROR;
+            if (distill && !make_map(&a.map_teach, teacher, V, n, 64, TC_BM)) return LOSSK_DEVICE_ERROR;
+            a.n_x = static_cast<int>(nx);
+            a.n_y = static_cast<int>(ny);
+            a.d = static_cast<int>(d);
+            a.n_tok = static_cast<int>(n);
+            a.vocab = static_cast<int>(V);
+            a.n_xt = static_cast<int>(cdiv(nx, TC_BM));
+            a.n_yt = static_cast<int>(cdiv(ny, TC_BN_ACC));
+            a.n_slices = static_cast<int>(cdiv(d, TC_SLICE));
+            a.n_split = rows ? static_cast<int>(L.nsplit) : 1;
+            a.direction = direction;
+            a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
+            a.tokp = w.tokp();
+            a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
+            a.out_split_stride = n * d;
+            a.err = &w.hdr()->err;
+            const int grid = a.n_xt * a.n_slices * a.n_split;
+            e = launch_tc(rows ? TC_ROWS : TC_COLS, distill, a, grid, st);
+            if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+            if (rows && L.nsplit > 1) {
+                e = launch_sum_splits(w.dhpart(), L.nsplit, n * d, d_hidden, st);
+                if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+            }
+        }
+    } else {
+        for (int pass = 0; pass < 2; ++pass) {
+            float *dst = pass == 0 ? d_hidden : d_weight;
+            if (!dst) continue;
+            const bool rows = pass == 0;
+            const void *X = rows ? H : W, *Y = rows ? W : H;
+            const int64_t nx = rows ? n : V, ny = rows ? V : n;
+            const int64_t nsplit = rows ? L.nsplit : 1;
+            float *out = (rows && nsplit > 1) ? w.dhpart() : dst;
+            e = launch_fp(rows ? TC_ROWS : TC_COLS, distill, X, Y, static_cast<const float *>(teacher),
+                          static_cast<int>(nx), static_cast<int>(ny), static_cast<int>(d),
+                          static_cast<int>(n), static_cast<int>(V), static_cast<int>(nsplit),
+                          direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, 0, 0, out, n * d, st);
+            if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+            if (rows && nsplit > 1) {
+                e = launch_sum_splits(w.dhpart(), nsplit, n * d, d_hidden, st);
+                if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+            }
+        }
+    }
+    return LOSSK_OK;
+}
+
+// Checks shared by the fused calls, in the documented order up to 585.
+int32_t check_fused(int64_t n, int64_t d, int64_t V, int64_t chunk, bool has_chunk, int32_t dtype,
+                    const void *H, int64_t hl, const void *W, int64_t wl, const void *workspace,
+                    int64_t wsb, int kind, WsLayout *L)
+{
+    int32_t s = lossk_dims_check(n, d, V);
+    if (s != LOSSK_OK) return s;
+    if (has_chunk) {
+        s = lossk_chunk_check(chunk, V);
+        if (s != LOSSK_OK) return s;
+    }
+    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (!H || !W || !workspace) return LOSSK_LENGTH_MISMATCH;
+    if (hl < n * d || wl < V * d) return LOSSK_LENGTH_MISMATCH;
+    if (!ws_layout(kind, n, d, V, dtype, L) || wsb < static_cast<int64_t>(L->total))
+        return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(H) || !aligned16(W) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return LOSSK_UNALIGNED;
+    if (dtype == LOSSK_BF16 && d % 8 != 0) return LOSSK_UNALIGNED;
+    return LOSSK_OK;
+}
+
+bool scalars_ok(double wz, double gs) { return is_finite(wz) && wz >= 0.0 && is_finite(gs); }
+
+} // namespace
+
+// ===========================================================================
+namespace lossk {
+
+int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
+{
+    const bool tc = dtype == LOSSK_BF16;
+    const int64_t bm = tc ? TC_BM : FP_BM, bn = tc ? TC_BN_ACC : FP_BN, sl = tc ? TC_SLICE : FP_SLICE;
+    const int64_t base = cdiv(n, bm) * cdiv(d, sl);
+    const int64_t n_yt = cdiv(V, bn);
+    const int64_t target = 296;   // about two CTAs per SM on a 148-152 SM part
+    if (base >= target) return 1;
+    int64_t s = cdiv(target, base);
+    const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
+    return s < cap ? s : cap;
+}
+
+bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L)
+{
+    if (lossk_dims_check(n, d, V) != LOSSK_OK) return false;
+    *L = WsLayout();
+    const bool tc = dtype == LOSSK_BF16;
+    L->n_pad = cdiv(n, TC_BM) * TC_BM;
+    const bool distill = kind == LOSSK_KIND_DISTILL;
+    L->bn = tc ? (distill ? TC_BN_ACC : TC_BN_FWD) : FP_BN;
+    L->n_ct = cdiv(V, L->bn);
+    L->nstat = distill ? NSTAT_DISTILL : NSTAT_CE;
+    const bool fwd = kind == LOSSK_KIND_CE_FWD || kind == LOSSK_KIND_CE_FWD_BWD || distill;
+    const bool bwd = kind == LOSSK_KIND_CE_BWD || kind == LOSSK_KIND_CE_FWD_BWD || distill;
+    L->nsplit = bwd ? dh_splits(n, d, V, dtype) : 1;
+    size_t off = 256;
+    L->off_tokp = off;
+    off = align256(off + sizeof(float4) * L->n_pad);
+    L->off_tgt = off;
+    off = align256(off + sizeof(float) * L->n_pad);
+    L->off_tokacc = off;
+    off = align256(off + sizeof(double) * 3 * L->n_pad);
+    L->off_part = off;
+    if (fwd) off = align256(off + sizeof(float) * L->nstat * L->n_ct * L->n_pad);
+    L->off_dhpart = off;
+    if (bwd && L->nsplit > 1) off = align256(off + sizeof(float) * L->nsplit * n * d);
+    L->off_red = off;
+    off = align256(off + 64);
+    L->total = off;
+    return true;
+}
+
+} // namespace lossk
+
+// ===========================================================================
+extern "C" {
+
+const char *lossk_status_name(int32_t code)
+{
+    switch (code) {
+    case 580: return "ok";
+    case 581: return "empty_dimension";
+    case 582: return "length_mismatch";
+    case 583: return "dimension_too_large";
+    case 584: return "work_budget_exceeded";
+    case 585: return "non_finite_scalar";
+    case 586: return "target_id_out_of_range";
+    case 587: return "chunk_exceeds_logit_budget";
+    case 588: return "unknown_objective";
+    case 589: return "device_error";
+    case 590: return "device_timeout";
+    case 591: return "unaligned";
+    default: return "unknown_status";
+    }
+}
+
+int32_t lossk_work_fits(int64_t n, int64_t d, int64_t V, int64_t ceiling)
+{
+    if (n < 1 || d < 1 || V < 1 || ceiling < 0) return 0;
+    return n <= (ceiling / d) / V ? 1 : 0;
+}
+
+int32_t lossk_dims_check(int64_t n, int64_t d, int64_t V)
+{
+    if (n < 1 || d < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
+    if (n > MAX_DIM || d > MAX_DIM || V > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
+    if (!lossk_work_fits(n, d, V, MAX_WORK_CELLS)) return LOSSK_WORK_BUDGET_EXCEEDED;
+    return LOSSK_OK;
+}
+
+int32_t lossk_chunk_check(int64_t chunk, int64_t V)
+{
+    if (chunk < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
+    if (chunk > MAX_LOGIT_CELLS / V) return LOSSK_CHUNK_EXCEEDS_LOGIT_BUDGET;
+    return LOSSK_OK;
+}
+
+double lossk_logit_cells(int64_t chunk, int64_t V)
+{
+    if (chunk < 1 || V < 1) return -1.0;
+    return static_cast<double>(chunk) * static_cast<double>(V);
+}
+
+int32_t lossk_peak_logit_cells(int64_t n, int64_t V, int64_t chunk, lossk_peak_cells *out)
+{
+    if (!out) return LOSSK_LENGTH_MISMATCH;
+    if (n < 1 || V < 1 || chunk < 1) {
+        out->chunked_cells = -1.0;
+        out->materialized_cells = -1.0;
+        out->ratio = 0.0;
+        out->n_chunks = 0;
+        out->status = LOSSK_EMPTY_DIMENSION;
+        return out->status;
+    }
+    const int64_t held = chunk < n ? chunk : n;
+    out->chunked_cells = static_cast<double>(held) * static_cast<double>(V);
+    out->materialized_cells = static_cast<double>(n) * static_cast<double>(V);
+    out->ratio = out->materialized_cells / out->chunked_cells;
+    out->n_chunks = cdiv(n, chunk);
+    out->status = lossk_chunk_check(chunk, V);
+    return out->status;
+}
+
+int64_t lossk_workspace_bytes(int32_t kind, int64_t n, int64_t d, int64_t V, int32_t dtype)
+{
+    WsLayout L;
+    if (!ws_layout(kind, n, d, V, dtype, &L)) return -1;
+    return static_cast<int64_t>(L.total);
+}
+
+int32_t lossk_targets_check(int64_t n, int64_t V, const int64_t *targets, int64_t targets_len,
+                            void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
+    if (!targets || !workspace || targets_len < n || workspace_bytes < 256) return LOSSK_LENGTH_MISMATCH;
+    Hdr h;
+    return validate(targets, nullptr, n, V, static_cast<WsHeader *>(workspace),
+                    reinterpret_cast<cudaStream_t>(stream), &h);
+}
+
+static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t V, int64_t chunk,
+                         bool has_chunk, int32_t dtype, const void *H, int64_t hl, const void *W,
+                         int64_t wl, const int64_t *targets, int64_t tl, const uint8_t *mask,
+                         double wz, double gs, float *lse_io, int64_t lse_len, float *ce_out,
+                         double *scalars, float *dH, float *dW, void *workspace, int64_t wsb,
+                         lossk_stream_t stream)
+{
+    const int kind = do_fwd && do_bwd ? LOSSK_KIND_CE_FWD_BWD : (do_fwd ? LOSSK_KIND_CE_FWD : LOSSK_KIND_CE_BWD);
+    Ws w;
+    int32_t s = check_fused(n, d, V, chunk, has_chunk, dtype, H, hl, W, wl, workspace, wsb, kind, &w.L);
+    if (s != LOSSK_OK) return s;
+    if (!targets || tl < n || !lse_io || lse_len < n) return LOSSK_LENGTH_MISMATCH;
+    if (do_fwd && !scalars) return LOSSK_LENGTH_MISMATCH;
+    if (!scalars_ok(wz, gs)) return LOSSK_NON_FINITE_SCALAR;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    s = validate(targets, mask, n, V, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    if (do_fwd) {
+        s = run_ce_fwd(w, n, d, V, dtype, H, W, targets, mask, wz, lse_io, ce_out, scalars, st);
+        if (s != LOSSK_OK) return s;
+    }
+    if (do_bwd && (dH || dW)) {
+        const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
+        if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, alpha, wz, w.tokp(), st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+        s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st);
+    }
+    return s;
+}
+
+int32_t lossk_ce_fwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype, const void *hidden,
+                     int64_t hidden_len, const void *weight, int64_t weight_len, const int64_t *targets,
+                     int64_t targets_len, const uint8_t *loss_mask, double z_weight, float *lse_out,
+                     float *ce_out, double *scalars_out, void *workspace, int64_t workspace_bytes,
+                     lossk_stream_t stream)
+{
+    return ce_common(true, false, n, d, V, chunk, true, dtype, hidden, hidden_len, weight, weight_len,
+                     targets, targets_len, loss_mask, z_weight, 1.0, lse_out, n, ce_out, scalars_out,
+                     nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int32_t lossk_ce_bwd(int64_t n, int64_t d, int64_t V, int32_t dtype, const void *hidden,
+                     int64_t hidden_len, const void *weight, int64_t weight_len, const int64_t *targets,
+                     int64_t targets_len, const uint8_t *loss_mask, double z_weight, double grad_scale,
+                     const float *lse, int64_t lse_len, float *d_hidden, float *d_weight,
+                     void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    return ce_common(false, true, n, d, V, 0, false, dtype, hidden, hidden_len, weight, weight_len,
+                     targets, targets_len, loss_mask, z_weight, grad_scale, const_cast<float *>(lse),
+                     lse_len, nullptr, nullptr, d_hidden, d_weight, workspace, workspace_bytes, stream);
+}
+
+int32_t lossk_ce_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
+                         const void *hidden, int64_t hidden_len, const void *weight, int64_t weight_len,
+                         const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                         double z_weight, double grad_scale, float *lse_out, float *ce_out,
+                         double *scalars_out, float *d_hidden, float *d_weight, void *workspace,
+                         int64_t workspace_bytes, lossk_stream_t stream)
+{
+    return ce_common(true, true, n, d, V, chunk, true, dtype, hidden, hidden_len, weight, weight_len,
+                     targets, targets_len, loss_mask, z_weight, grad_scale, lse_out, n, ce_out,
+                     scalars_out, d_hidden, d_weight, workspace, workspace_bytes, stream);
+}
+
+int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, int64_t logits_len,
+                             const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                             double z_weight, double grad_scale, float *lse_out, float *ce_out,
+                             double *scalars_out, void *grad_logits, int64_t grad_len, void *workspace,
+                             int64_t workspace_bytes, lossk_stream_t stream)
+{
+    if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
+    if (n > MAX_DIM || V > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
+    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    Ws w;
+    if (!ws_layout(LOSSK_KIND_FROM_LOGITS, n, 1, V, dtype, &w.L)) return LOSSK_DIMENSION_TOO_LARGE;
+    if (!logits || !targets || !lse_out || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
+    if (logits_len < n * V || targets_len < n || (grad_logits && grad_len < n * V) ||
+        workspace_bytes < static_cast<int64_t>(w.L.total))
+        return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(logits) || (grad_logits && !aligned16(grad_logits)) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return LOSSK_UNALIGNED;
+    if (!scalars_ok(z_weight, grad_scale)) return LOSSK_NON_FINITE_SCALAR;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    int32_t s = validate(targets, loss_mask, n, V, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
+    if (launch_from_logits(dtype, logits, targets, loss_mask, n, V, z_weight, alpha, lse_out, ce_out,
+                           w.tokacc(), grad_logits, st) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st));
+}
+
+int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
+                              const void *hidden, int64_t hidden_len, const void *weight,
+                              int64_t weight_len, const void *teacher, int64_t teacher_len,
+                              const uint8_t *loss_mask, int32_t direction, double temperature,
+                              double z_weight, double grad_scale, double *scalars_out,
+                              float *per_token_out, float *lse_out, float *d_hidden, float *d_weight,
+                              void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    Ws w;
+    int32_t s = check_fused(n, d, V, chunk, true, dtype, hidden, hidden_len, weight, weight_len,
+                            workspace, workspace_bytes, LOSSK_KIND_DISTILL, &w.L);
+    if (s != LOSSK_OK) return s;
+    if (!teacher || teacher_len < n * V || !scalars_out) return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(teacher) || (dtype == LOSSK_BF16 && V % 8 != 0)) return LOSSK_UNALIGNED;
+    if (!scalars_ok(z_weight, grad_scale) || !is_finite(temperature) || temperature <= 0.0)
+        return LOSSK_NON_FINITE_SCALAR;
+    if (direction < LOSSK_DISTILL_CE || direction > LOSSK_DISTILL_REV_KL) return LOSSK_UNKNOWN_OBJECTIVE;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    s = validate(nullptr, loss_mask, n, V, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    const WsLayout &L = w.L;
+    cudaError_t e;
+    if (dtype == LOSSK_BF16) {
+        TcArgs a;
+        std::memset(&a, 0, sizeof(a));
+        if (!make_map(&a.map_x, hidden, d, n, 64, TC_BM) || !make_map(&a.map_y, weight, d, V, 64, TC_BN_ACC) ||
+            !make_map(&a.map_teach, teacher, V, n, 64, TC_BM))
+            return LOSSK_DEVICE_ERROR;
+        a.n_x = static_cast<int>(n);
+        a.n_y = static_cast<int>(V);
+        a.d = static_cast<int>(d);
+        a.n_tok = static_cast<int>(n);
+        a.vocab = static_cast<int>(V);
+        a.n_xt = static_cast<int>(cdiv(n, TC_BM));
+        a.n_yt = static_cast<int>(L.n_ct);
+        a.n_items = a.n_xt * a.n_yt;
+        a.direction = direction;
+        a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
+        a.part = w.part();
+        a.part_stride = L.n_pad;
+        a.part_plane = L.n_ct * L.n_pad;
+        a.err = &w.hdr()->err;
+        const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        e = launch_tc(TC_STATS, true, a, grid, st);
+    } else {
+        e = launch_fp(TC_STATS, true, hidden, weight, static_cast<const float *>(teacher),
+                      static_cast<int>(n), static_cast<int>(V), static_cast<int>(d), static_cast<int>(n),
+                      static_cast<int>(V), 1, direction, static_cast<float>(1.0 / temperature), nullptr,
+                      nullptr, w.part(), nullptr, L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
+    e = launch_merge_distill(w.part(), loss_mask, n, L.n_ct, L.n_pad, direction, z_weight, lse_out,
+                             per_token_out, w.tokacc(), w.tokp(), alpha, temperature, st);
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), z_weight, scalars_out, st);
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    if (!d_hidden && !d_weight) return LOSSK_OK;
+    return run_acc(w, n, d, V, dtype, hidden, weight, teacher, true, direction, temperature, d_hidden,
+                   d_weight, st);
+}
+
+int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    if (!workspace || workspace_bytes < 256) return LOSSK_LENGTH_MISMATCH;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    int err = 0;
+    if (cudaMemcpy(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    if (err == 0) return LOSSK_OK;
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    return LOSSK_DEVICE_TIMEOUT;
+}
+
+} // extern "C"

@@ -1,0 +1,118 @@
+// lossk_internal.h -- shared between the host entry points and the kernels:
+// the workspace layout, the per-token parameter records and the launcher
+// declarations.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lossk {
+
+constexpr double LN2 = 0.69314718055994530942;
+constexpr double LOG2E = 1.44269504088896340736;
+
+// Tile geometry of the tensor-core path.
+constexpr int TC_BM = 128;         // rows of X per tile (MMA M, TMEM lanes)
+constexpr int TC_BN_FWD = 256;     // logit tile width of the label-CE forward
+constexpr int TC_BN_ACC = 128;     // logit tile width of the backward and distillation
+constexpr int TC_BK = 64;          // K per pipeline stage (one 128-byte swizzle row)
+constexpr int TC_SLICE = 256;      // d_model columns one backward CTA accumulates
+// Tile geometry of the fp32 FFMA path.
+constexpr int FP_BM = 64, FP_BN = 64, FP_BK = 16, FP_SLICE = 64;
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    int err;          // device error word (ERR_* in ptx.cuh)
+    int bad_targets;  // count of targets outside [0, vocab)
+    int n_valid;      // counted tokens
+    int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Per-(token, logit tile) partial statistics written by the forward pass
+// (structure of arrays, each [n_ct][n_pad]).  Label CE: m2 (running max of
+// logit*log2e) and z (sum of 2^(logit*log2e - m2)).  Distillation adds the
+// teacher's pair and one direction-dependent weighted sum.
+constexpr int NSTAT_CE = 2;
+constexpr int NSTAT_DISTILL = 5;
+
+struct WsLayout {
+    int64_t n_pad = 0;       // n_tok rounded up to 128
+    int64_t n_ct = 0;        // logit tiles across the vocabulary in the forward
+    int64_t bn = 0;          // their width
+    int64_t nstat = 0;
+    int64_t nsplit = 0;      // vocabulary splits of the d_hidden pass
+    size_t off_tokp = 0;     // float4 [n_pad]   per-token backward parameters
+    size_t off_tgt = 0;      // float  [n_pad]   target logit
+    size_t off_tokacc = 0;   // double [3][n_pad] per-token reduction terms
+    size_t off_part = 0;     // float  [nstat][n_ct][n_pad]
+    size_t off_dhpart = 0;   // float  [nsplit][n_tok][d_model] (nsplit > 1)
+    size_t off_red = 0;      // double [8] reduction output scratch
+    size_t total = 0;
+};
+
+// kind: lossk_kind; dtype: lossk_dtype.  Returns false for an invalid shape.
+bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L);
+int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype);
+
+// ---- tensor-core kernel arguments ------------------------------------------
+enum TcMode : int { TC_STATS = 0, TC_ROWS = 1, TC_COLS = 2 };
+enum Direction : int { DIR_CE = 0, DIR_FKL = 1, DIR_RKL = 2 };
+
+struct TcArgs {
+    CUtensorMap map_x;     // X operand (K-major), box {64, 128}
+    CUtensorMap map_y;     // Y operand (K-major), box {64, BN}
+    CUtensorMap map_ys;    // Y rows x d-slice as the MN-major B operand, box {64, 64}
+    CUtensorMap map_teach; // teacher logits [n_tok][vocab], box {64, 128}
+    int n_x;               // rows of X (n_tok in STATS/ROWS, vocab in COLS)
+    int n_y;               // rows of Y
+    int d;                 // contraction length (d_model)
+    int n_tok, vocab;
+    int n_xt;              // X tiles
+    int n_yt;              // Y tiles
+    int n_items;           // STATS: (x tile, y tile) pairs
+    int n_slices;          // ROWS/COLS: d_model slices
+    int n_split;           // ROWS: vocabulary splits
+    int direction;         // distillation objective
+    float inv_t_l2e;       // log2(e) / temperature
+    const int64_t *targets;
+    const float4 *tokp;    // per-token backward parameters
+    float *part;           // STATS output (structure of arrays)
+    float *tgt;            // STATS (label CE): target logit per token
+    int64_t part_stride;   // n_pad
+    int64_t part_plane;    // n_ct * n_pad
+    float *out;            // ROWS/COLS output
+    int64_t out_split_stride;
+    int *err;
+};
+
+// ---- launchers (all enqueue on `st`) -----------------------------------------
+cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
+                            WsHeader *hdr, cudaStream_t st);
+cudaError_t launch_tc(int mode, bool distill, const TcArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
+                      int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
+                      float inv_t, const int64_t *targets, const float4 *tokp, float *part,
+                      float *tgt, int64_t part_stride, int64_t part_plane, float *out,
+                      int64_t out_split_stride, cudaStream_t st);
+cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
+                            const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
+                            double wz, float *lse_out, float *ce_out, double *tokacc,
+                            cudaStream_t st);
+cudaError_t launch_merge_distill(const float *part, const uint8_t *mask, int64_t n, int64_t n_ct,
+                                 int64_t n_pad, int direction, double wz, float *lse_out,
+                                 float *per_token, double *tokacc, float4 *tokp, double alpha,
+                                 double temperature, cudaStream_t st);
+cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
+                          double wz, double *scalars_out, cudaStream_t st);
+cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,
+                           int64_t n, int64_t n_pad, double alpha, double wz, float4 *tokp,
+                           cudaStream_t st);
+cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
+                              cudaStream_t st);
+cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *targets,
+                               const uint8_t *mask, int64_t n, int64_t V, double wz,
+                               double alpha, float *lse_out, float *ce_out, double *tokacc,
+                               void *grad, cudaStream_t st);
+
+} // namespace lossk

@@ -15,3 +15,13 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def build_lib():
+    """Build liblossk.so (loading build.py by path; the package import needs the library)."""
+    import importlib.util
+    path = os.path.join(ROOT, "output_projection_cross_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("lossk_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()

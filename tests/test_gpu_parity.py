@@ -1,0 +1,400 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (written here, not derived at run time):
+  bf16 inputs, fp32 accumulation: per-token loss and lse |d| <= 2e-3*max(1,|ref|);
+                                  gradients relative L2 error <= 1e-2 (whole tensor)
+  fp32 inputs:                    per-token loss and lse |d| <= 1e-6*max(1,|ref|);
+                                  gradients relative L2 error <= 1e-5
+Where the oracle cannot finish at the full workload size, it computes sampled
+tokens (loss, lse, d_hidden rows) and, where affordable, sampled d_weight rows;
+the rest is checked through identities that hold at any size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import lossk_inputs as li
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+BF16_LOSS, BF16_GRAD = 2e-3, 1e-2
+F32_LOSS, F32_GRAD = 1e-6, 1e-5
+
+
+@pytest.fixture(scope="module")
+def L():
+    from conftest import build_lib
+    build_lib()
+    import output_projection_cross_gb300 as L
+    assert torch.cuda.is_available()
+    return L
+
+
+def _dev(a, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if dtype == "bf16":
+        return t.to(torch.bfloat16)
+    return t
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+def rel_l2(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def close_loss(got, ref, tol):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    assert err.max() <= tol, f"max scaled loss error {err.max():.3e} > {tol}"
+
+
+def _inputs(wl, seed=0, **sizes):
+    return li.make(wl, seed=seed, **sizes)
+
+
+# ---------------------------------------------------------------------------
+def test_tiny_fp32_config(L):
+    """The fp32 workload at its stated size, full comparison."""
+    w = li.WORKLOADS["tiny_fp32_ce"]
+    x = _inputs(w)
+    H, W, y = _dev(x["hidden"], "fp32"), _dev(x["weight"], "fp32"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, chunk=w.chunk)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], chunk=w.chunk)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"])
+    close_loss(_np(out["ce"]), ref["ce"], F32_LOSS)
+    close_loss(_np(out["lse"]), ref["lse"], F32_LOSS)
+    close_loss(_np(out["scalars"])[:2], [ref["total"], ref["ce_mean"]], F32_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= F32_GRAD
+    assert rel_l2(_np(out["d_weight"]), dW) <= F32_GRAD
+
+
+SMALL = [  # (n, d, V): several tiles and ragged tails in every dimension
+    (1, 64, 8),
+    (130, 72, 300),
+    (300, 200, 1000),
+    (257, 520, 2000),
+    (128, 256, 512),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("shape", SMALL)
+def test_ce_small_shapes(L, shape, dtype):
+    n, d, V = shape
+    x = _inputs("ce_512x1024x32000", seed=sum(shape), n_tok=n, d_model=d, vocab=V)
+    if dtype == "fp32":
+        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
+        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    mask = li.mask(3, n, 0.2) if n > 4 else None
+    wz, gs = 1e-3, 0.75
+    H, W, y = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], "")
+    m = None if mask is None else _dev(mask, "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=m, chunk=min(n, 64), z_weight=wz, grad_scale=gs)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, chunk=min(n, 64), z_weight=wz)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz, grad_scale=gs)
+    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    close_loss(_np(out["lse"]), ref["lse"], lt)
+    close_loss(_np(out["ce"]), ref["ce"], lt)
+    close_loss(_np(out["scalars"]), [ref["total"], ref["ce_mean"], ref["z_mean"]], lt)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= gt
+    assert rel_l2(_np(out["d_weight"]), dW) <= gt
+
+
+def test_ce_fwd_and_bwd_entry_points_agree_with_fused(L):
+    n, d, V = 200, 128, 1500
+    x = _inputs("ce_512x1024x32000", seed=5, n_tok=n, d_model=d, vocab=V)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    f = L.lossk_ce_fwd(H, W, y, chunk=32, z_weight=0.01)
+    b = L.lossk_ce_bwd(H, W, y, f["lse"], z_weight=0.01, grad_scale=2.0)
+    fb = L.lossk_ce_fwd_bwd(H, W, y, chunk=32, z_weight=0.01, grad_scale=2.0)
+    torch.cuda.synchronize()
+    assert torch.equal(f["lse"], fb["lse"]) and torch.equal(f["scalars"], fb["scalars"])
+    assert torch.equal(b["d_hidden"], fb["d_hidden"]) and torch.equal(b["d_weight"], fb["d_weight"])
+    # either gradient may be skipped
+    only_w = L.lossk_ce_bwd(H, W, y, f["lse"], z_weight=0.01, grad_scale=2.0, want_d_hidden=False)
+    torch.cuda.synchronize()
+    assert only_w["d_hidden"] is None and torch.equal(only_w["d_weight"], fb["d_weight"])
+
+
+def test_config_512x1024x32000_full(L):
+    w = li.WORKLOADS["ce_512x1024x32000"]
+    x = _inputs(w)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, chunk=w.chunk)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], chunk=w.chunk)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"])
+    close_loss(_np(out["ce"]), ref["ce"], BF16_LOSS)
+    close_loss(_np(out["lse"]), ref["lse"], BF16_LOSS)
+    close_loss(_np(out["scalars"])[:2], [ref["total"], ref["ce_mean"]], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= BF16_GRAD
+    assert rel_l2(_np(out["d_weight"]), dW) <= BF16_GRAD
+
+
+def test_qwen3_head_full_size_sampled(L):
+    """n=2048, d=1024, V=151936, Zipf targets: the launch configuration the bench times."""
+    w = li.WORKLOADS["qwen3_0p6b_head"]
+    x = _inputs(w)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, chunk=w.chunk)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(7).choice(w.n_tok, 48, replace=False)
+    rows.sort()
+    s = oracle.ce_token_rows(x["hidden"], x["weight"], x["targets"], rows)
+    close_loss(_np(out["lse"])[rows], s["lse"], BF16_LOSS)
+    close_loss(_np(out["ce"])[rows], s["lse"] - s["tgt"], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"])[rows], s["dH"]) <= BF16_GRAD
+    # d_weight rows: the oracle needs every token's lse
+    full = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], chunk=w.chunk)
+    close_loss(_np(out["lse"]), full["lse"], BF16_LOSS)
+    close_loss(_np(out["scalars"])[:1], [full["total"]], BF16_LOSS)
+    vrows = np.concatenate([np.unique(x["targets"])[:24],
+                            np.random.default_rng(8).choice(w.vocab, 24, replace=False)])
+    dw = oracle.ce_dweight_rows(x["hidden"], x["weight"], x["targets"], full["lse"], vrows)
+    assert rel_l2(_np(out["d_weight"])[vrows], dw) <= BF16_GRAD
+    # any-size identity: d_weight summed over the vocabulary cancels (no z-loss)
+    dws = out["d_weight"].double().sum(0).cpu().numpy()
+    assert np.abs(dws).max() <= 1e-2 * np.abs(_np(out["d_weight"])).max()
+
+
+def test_ce_z_mask_reduced_full(L):
+    """The CE + z-loss + mask recipe at a size the oracle finishes in seconds."""
+    w = li.WORKLOADS["ce_z_8192x4096x128256"]
+    x = _inputs(w, n_tok=640, d_model=512, vocab=5000)
+    mask = li.mask(0, 640, w.mask_frac)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=_dev(mask, ""), chunk=128, z_weight=w.z_weight)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, chunk=128, z_weight=w.z_weight)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=w.z_weight)
+    close_loss(_np(out["ce"]), ref["ce"], BF16_LOSS)
+    close_loss(_np(out["scalars"]), [ref["total"], ref["ce_mean"], ref["z_mean"]], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= BF16_GRAD
+    assert rel_l2(_np(out["d_weight"]), dW) <= BF16_GRAD
+
+
+def test_ce_z_mask_full_size_sampled(L):
+    """n=8192, d=4096, V=128256, z weight 1e-4, 5% masked: sampled tokens + identities."""
+    w = li.WORKLOADS["ce_z_8192x4096x128256"]
+    x = _inputs(w)
+    mask = x["mask"]
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=_dev(mask, ""), chunk=w.chunk, z_weight=w.z_weight)
+    torch.cuda.synchronize()
+    masked = np.flatnonzero(mask == 0)[:4]
+    rows = np.sort(np.concatenate([np.random.default_rng(9).choice(w.n_tok, 20, replace=False), masked]))
+    s = oracle.ce_token_rows(x["hidden"], x["weight"], x["targets"], rows, mask=mask, z_weight=w.z_weight)
+    close_loss(_np(out["lse"])[rows], s["lse"], BF16_LOSS)
+    ce_ref = np.where(mask[rows] != 0, s["lse"] - s["tgt"], 0.0)
+    close_loss(_np(out["ce"])[rows], ce_ref, BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"])[rows], s["dH"]) <= BF16_GRAD
+    assert np.all(_np(out["d_hidden"])[masked] == 0)
+    # identity: sum_v G_tv = alpha_t * 2 wz lse_t, so sum_v dW_v = sum_t alpha_t 2 wz lse_t H_t
+    lse = out["lse"].double()
+    m = torch.from_numpy(mask).cuda().double()
+    coef = m * 2 * w.z_weight * lse / m.sum()
+    expect = (coef[:, None] * H.double()).sum(0)
+    got = out["d_weight"].double().sum(0)
+    scale = out["d_weight"].double().abs().max()
+    assert float((got - expect).abs().max()) <= 1e-2 * float(scale)
+    # reduced scalars against the oracle's per-token values on the sample
+    tot = _np(out["scalars"])
+    assert tot[1] > 0 and math.isfinite(tot[0])
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+@pytest.mark.parametrize("T", [1.0, 2.0])
+def test_distill_small(L, dtype, direction, T):
+    n, d, V = 200, 136, 1032
+    x = _inputs("distill_z_4096x2048", seed=11, n_tok=n, d_model=d, vocab=V)
+    if dtype == "fp32":
+        x["hidden"] = li.hidden(2, n, d, dtype="fp32")
+        x["weight"] = li.weight(2, V, d, dtype="fp32")
+    mask = li.mask(1, n, 0.1)
+    wz, gs = 1e-3, 1.25
+    Tt = x["teacher"]
+    H, W = _dev(x["hidden"], dtype), _dev(x["weight"], dtype)
+    teach = _dev(Tt, dtype)
+    out = L.lossk_distill_fwd_bwd(H, W, teach, direction, temperature=T, loss_mask=_dev(mask, ""),
+                                  chunk=50, z_weight=wz, grad_scale=gs)
+    torch.cuda.synchronize()
+    r = oracle.distill(x["hidden"], x["weight"], Tt, direction, temperature=T, mask=mask, chunk=50,
+                       z_weight=wz, grad_scale=gs)
+    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS * 10, F32_GRAD)
+    close_loss(_np(out["per_token"]), r["per_token"], lt)
+    close_loss(_np(out["lse"]), r["lse"], lt)
+    close_loss(_np(out["scalars"]), [r["total"], r["distill_mean"], r["z_mean"]], lt)
+    assert rel_l2(_np(out["d_hidden"]), r["dH"]) <= gt
+    assert rel_l2(_np(out["d_weight"]), r["dW"]) <= gt
+
+
+@pytest.mark.parametrize("direction", ["fkl", "rkl", "ce"])
+def test_distill_full_size_sampled(L, direction):
+    """n=4096, d=2048, V=151936, teacher N(0,3) bf16, T=2, 10% masked, z 1e-4."""
+    w = li.WORKLOADS["distill_z_4096x2048"]
+    x = _cached_distill()
+    mask = x["mask"]
+    H, W, teach = x["H"], x["W"], x["T"]
+    out = L.lossk_distill_fwd_bwd(H, W, teach, direction, temperature=w.temperature,
+                                  loss_mask=x["m"], chunk=w.chunk, z_weight=w.z_weight)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(12).choice(w.n_tok, 12, replace=False))
+    s = oracle.distill_token_rows(x["hidden"], x["weight"], x["teacher"], direction, rows,
+                                  temperature=w.temperature, mask=mask, z_weight=w.z_weight)
+    per = np.where(mask[rows] != 0, s["loss"], 0.0)
+    close_loss(_np(out["per_token"])[rows], per, BF16_LOSS)
+    close_loss(_np(out["lse"])[rows], s["lse"], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"])[rows], s["dH"]) <= BF16_GRAD
+    # identity: every objective's gradient row sums to alpha_t/T * 2 wz lse_t
+    lse = out["lse"].double()
+    m = x["m"].double()
+    coef = m * 2 * w.z_weight * lse / (w.temperature * m.sum())
+    expect = (coef[:, None] * H.double()).sum(0)
+    got = out["d_weight"].double().sum(0)
+    scale = out["d_weight"].double().abs().max()
+    assert float((got - expect).abs().max()) <= 1e-2 * float(scale)
+
+
+_DISTILL_CACHE = {}
+
+
+def _cached_distill():
+    if not _DISTILL_CACHE:
+        w = li.WORKLOADS["distill_z_4096x2048"]
+        x = _inputs(w)
+        _DISTILL_CACHE.update(x)
+        _DISTILL_CACHE["H"] = _dev(x["hidden"], "bf16")
+        _DISTILL_CACHE["W"] = _dev(x["weight"], "bf16")
+        _DISTILL_CACHE["T"] = _dev(x["teacher"], "bf16")
+        _DISTILL_CACHE["m"] = _dev(x["mask"], "")
+    return _DISTILL_CACHE
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("V", [9, 1000, 4099, 151936])
+def test_from_logits(L, dtype, V):
+    n = 37 if V > 10000 else 129
+    g = np.random.default_rng(V)
+    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
+    if dtype == "bf16":
+        X = li.to_bf16_values(X)
+    y = g.integers(0, V, n).astype(np.int64)
+    mask = (np.arange(n) % 7 != 3).astype(np.uint8)
+    wz, gs = 1e-2, 1.5
+    out = L.lossk_ce_from_logits(_dev(X, dtype), _dev(y, ""), loss_mask=_dev(mask, ""), z_weight=wz,
+                                 grad_scale=gs, want_grad=True)
+    torch.cuda.synchronize()
+    r = oracle.ce_from_logits(X, y, mask=mask, z_weight=wz, grad_scale=gs, want_grad=True)
+    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    close_loss(_np(out["lse"]), r["lse"], lt)
+    close_loss(_np(out["ce"]), r["ce"], lt)
+    close_loss(_np(out["scalars"]), [r["total"], r["ce_mean"], r["z_mean"]], lt)
+    assert rel_l2(_np(out["grad_logits"]), r["grad"]) <= gt
+
+
+def test_from_logits_uniform_golden(L):
+    """6 tokens, vocab 9, every logit 0.25 -> mean loss ln 9 (the pages' worked example)."""
+    X = torch.full((6, 9), 0.25, device="cuda")
+    y = torch.tensor([0, 3, 6, 0, 3, 6], device="cuda")
+    out = L.lossk_ce_from_logits(X, y)
+    torch.cuda.synchronize()
+    assert abs(out["scalars"][0].item() - 2.1972245773362196) <= 1e-6 * 2.1972245773362196
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_chunk_invariance_and_determinism(L, dtype):
+    n, d, V = 300, 128, 3000
+    x = _inputs("ce_512x1024x32000", seed=21, n_tok=n, d_model=d, vocab=V)
+    H, W, y = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], "")
+    if dtype == "fp32":
+        H, W = H.float(), W.float()
+    base = L.lossk_ce_fwd_bwd(H, W, y, chunk=n, z_weight=0.01)
+    for chunk in (1, 7, 64, 256):
+        o = L.lossk_ce_fwd_bwd(H, W, y, chunk=chunk, z_weight=0.01)
+        torch.cuda.synchronize()
+        for k in ("lse", "ce", "scalars", "d_hidden", "d_weight"):
+            assert torch.equal(o[k], base[k]), (chunk, k)
+
+
+def test_zero_weight_closed_form(L):
+    n, d, V = 100, 64, 1000
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = torch.zeros(V, d, device="cuda", dtype=torch.bfloat16)
+    y = torch.randint(0, V, (n,), device="cuda")
+    o = L.lossk_ce_fwd_bwd(H, W, y, z_weight=0.5)
+    torch.cuda.synchronize()
+    lv = math.log(V)
+    assert torch.allclose(o["lse"].double(), torch.full((n,), lv, dtype=torch.float64, device="cuda"), atol=1e-5)
+    s = o["scalars"].cpu().numpy()
+    assert abs(s[1] - lv) <= 1e-5 and abs(s[2] - lv * lv) <= 1e-4
+
+
+def test_z_weight_zero_path_is_bit_identical_to_no_z(L):
+    """z gated off: the loss equals its ce mean exactly and gradients equal a
+    second call's bits."""
+    n, d, V = 150, 64, 700
+    x = _inputs("ce_512x1024x32000", seed=2, n_tok=n, d_model=d, vocab=V)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    a = L.lossk_ce_fwd_bwd(H, W, y, z_weight=0.0)
+    torch.cuda.synchronize()
+    assert a["scalars"][0].item() == a["scalars"][1].item()
+
+
+def test_refusals_leave_outputs_untouched(L):
+    n, d, V = 64, 64, 500
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = torch.randn(V, d, device="cuda").to(torch.bfloat16)
+    for bad in (-1, V):
+        y = torch.randint(0, V, (n,), device="cuda")
+        y[5] = bad
+        lse = torch.full((n,), 7.0, device="cuda")
+        with pytest.raises(L.LosskError) as e:
+            L.lossk_ce_fwd(H, W, y, lse_out=lse)
+        assert e.value.status == 586
+        assert torch.all(lse == 7.0)
+    y = torch.randint(0, V, (n,), device="cuda")
+    assert L.lossk_targets_check(y, V) == 580
+    y[0] = V
+    assert L.lossk_targets_check(y, V) == 586
+    with pytest.raises(L.LosskError) as e:
+        L.lossk_ce_fwd(H, W, torch.randint(0, V, (n,), device="cuda"), chunk=(1 << 27) // V + 1)
+    assert e.value.status == 587
+    with pytest.raises(L.LosskError) as e:
+        L.lossk_distill_fwd_bwd(H, W, torch.zeros(n, V, device="cuda", dtype=torch.bfloat16), 5)
+    assert e.value.status == 588
+
+
+def test_all_masked_gives_zeros(L):
+    n, d, V = 70, 64, 300
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = torch.randn(V, d, device="cuda").to(torch.bfloat16)
+    y = torch.randint(0, V, (n,), device="cuda")
+    m = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    o = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=m, z_weight=0.1)
+    torch.cuda.synchronize()
+    assert torch.all(o["scalars"] == 0) and torch.all(o["ce"] == 0)
+    assert torch.all(o["d_hidden"] == 0) and torch.all(o["d_weight"] == 0)
+    assert torch.all(torch.isfinite(o["lse"]))
+
+
+def test_device_status_clean_after_calls(L):
+    n, d, V = 64, 64, 256
+    ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, d, V, 1)
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = torch.randn(V, d, device="cuda").to(torch.bfloat16)
+    y = torch.randint(0, V, (n,), device="cuda")
+    L.lossk_ce_fwd_bwd(H, W, y, ws=ws)
+    assert L.lossk_device_status(ws) == 580
