@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused LM-head loss on GB300.
+
+One step = one fused cross-entropy forward + backward (lossk_ce_fwd_bwd:
+validation, logit statistics, merge, token mean, d_hidden, d_weight) over one
+synthetic batch of the Qwen3-0.6B head shape: n_tok=2048, d_model=1024,
+vocab=151936, chunk 256, bf16, Zipf(1.1) targets.  Inputs are resident in
+HBM when the timed region starts; the weight (311 MB) alone is larger than
+L2, so no flush is needed between steps.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank takes its own batch (batch index = rank, same
+weight) on its own GPU:
+the ranks share no data, so N ranks are N independent replicas and the
+whole-job value is N * n_tok / (max step time over ranks) ("weak").
+
+Printed: one JSON line on rank 0 (see the design doc for every key).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd tokens/s at Qwen3 shape; % of bf16 tensor peak"
+WORKLOAD = "qwen3_0p6b_head"
+# Which kernels' work counts as algorithmic (FLOPs per launch, in units of
+# n*d*V multiply-adds x 2): statistics = one logit contraction; each backward
+# pass = one logit contraction (recompute once) + its gradient contraction.
+ALGO_FLOPS_NDV = {"tc_stats": 2.0, "tc_rows": 4.0, "tc_cols": 4.0,
+                  "fp_stats": 2.0, "fp_rows": 4.0, "fp_cols": 4.0}
+HBM_KERNELS = {"from_logits", "validate", "merge_ce", "merge_distill", "reduce", "tokp_ce",
+               "sum_splits"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def args_parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the extra path measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    return ap.parse_args()
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(n_tok_per_rank, world, max_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * n_tok_per_rank / (max_ms / 1e3)
+
+
+# ---- clocks -------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid):
+        self.uuid = gpu_uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0.3 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+# ---- traffic from the committed ncu summary -----------------------------------
+
+def kernel_src_sha():
+    h = hashlib.sha256()
+    for f in ("k_tc.cu", "ptx.cuh", "lossk_internal.h"):
+        h.update(open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(kernel)
+    if not e or e.get("kernel_src_sha") != kernel_src_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---- CPU baseline (the oracle, as it stands) --------------------------------------
+
+def oracle_step(x, k, chunk):
+    import oracle
+    H, W, y = x["hidden"][:k], x["weight"], x["targets"][:k]
+    m = None if x["mask"] is None else x["mask"][:k]
+    oracle.ce_fwd(H, W, y, mask=m, chunk=min(chunk, k))
+    oracle.ce_bwd(H, W, y, mask=m)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(x, chunk, seconds):
+    """Oracle fwd+bwd on the first k tokens of the batch; k sized to ~`seconds`."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+    t0 = time.perf_counter()
+    oracle_step(x, 2, chunk)
+    t2 = time.perf_counter() - t0
+    k = int(max(2, min(len(x["targets"]), 2 * seconds / max(t2, 1e-3))))
+    t0 = time.perf_counter()
+    oracle_step(x, k, chunk)
+    dt = time.perf_counter() - t0
+    return {"value": k / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {k} tokens of the batch (full d_model and vocab), fp64 fwd+bwd, "
+                      f"{dt:.1f} s"}
+
+
+# ---- our implementation -----------------------------------------------------------------
+
+def run_ours(a, rank, world, local):
+    import numpy as np
+    import torch
+
+    import lossk_inputs as li
+    import output_projection_cross_gb300 as L
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = li.WORKLOADS[WORKLOAD]
+    x = li.make(w, seed=0, batch=rank)
+    H = torch.from_numpy(x["hidden"]).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy(x["weight"]).to(dev).to(torch.bfloat16)
+    y = torch.from_numpy(x["targets"]).to(dev)
+    n, d, V = w.n_tok, w.d_model, w.vocab
+    ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, d, V, L.lossk.BF16, dev)
+    out = dict(lse_out=torch.empty(n, device=dev), ce_out=torch.empty(n, device=dev),
+               scalars_out=torch.empty(3, dtype=torch.float64, device=dev),
+               d_hidden=torch.empty(n, d, device=dev), d_weight=torch.empty(V, d, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        L.lossk_ce_fwd_bwd(H, W, y, chunk=w.chunk, z_weight=w.z_weight, ws=ws, **out)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert L.lossk_device_status(ws) == 580
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = Clocks(uuid)
+    L.lossk_profile_read(reset=True)
+    L.lossk_profile_enable(True)
+    launches0 = L.lossk_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    launches = L.lossk_launch_count() - launches0
+    L.lossk_profile_enable(False)
+    prof = L.lossk_profile_read(reset=True)
+    ms = e0.elapsed_time(e1) / a.steps
+    ms_max = max_over_ranks(ms, world)
+    assert L.lossk_device_status(ws) == 580
+
+    pk = peaks()
+    value = aggregate(n, world, ms_max)
+    flops6 = 6.0 * n * d * V
+    res = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_max,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded: hidden N(0,1), weight N(0,0.02), Zipf(1.1) targets)",
+           "config": {"workload": WORKLOAD, "n_tok": n, "d_model": d, "vocab": V,
+                      "chunk": w.chunk, "targets": w.targets,
+                      "l2": "inputs larger than L2 (bf16 weight 311 MB > 126 MB L2); no flush",
+                      "parallelism": f"{world} independent replica(s), one batch per rank"}}
+    tflops = flops6 / (ms_max / 1e3) / 1e12
+    res["tensor_peak"] = {"flops_per_step": flops6, "counted_as": "6*n*d*V",
+                          "achieved_tflops": tflops, "peak_tflops": pk["bf16_tflops_sustained"],
+                          "peak": f"bf16 sustained ({pk['source']})",
+                          "frac": tflops / pk["bf16_tflops_sustained"]}
+    # dominant kernel roofline (live CUDA-event durations over the timed region)
+    kern = {k: {"avg_ms": v[0] / v[1], "launches": v[1], "share": v[0] / (ms * a.steps)}
+            for k, v in prof.items()}
+    dom = max(prof, key=lambda k: prof[k][0])
+    avg = prof[dom][0] / prof[dom][1]
+    if dom in ALGO_FLOPS_NDV:
+        fl = ALGO_FLOPS_NDV[dom] * n * d * V
+        ach = fl / (avg / 1e3) / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        res["roofline"] = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
+                           "unit": "TFLOP/s", "frac": ach / peak,
+                           "peak_kind": f"bf16 sustained, {pk['source']}",
+                           "algorithmic_per_launch": fl,
+                           "traffic": ncu_traffic(dom)}
+    res["kernels"] = kern
+    res["gpu_launches"] = launches
+    res["clocks"] = ck
+
+    if not a.no_e2e:
+        res["e2e"] = e2e(a, x, H, W, y, out, step, stream, n, world)
+    if not a.quick and rank == 0:
+        res["paths"] = extra_paths(L, dev, pk)
+    if rank == 0 and world == 1 and not a.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(x, w.chunk, a.cpu_seconds)
+    return res
+
+
+def e2e(a, x, H, W, y, out, step, stream, n, world):
+    """The same step through the C ABI with host buffers: each step copies its
+    inputs from pinned host memory and its outputs back, inside the timed region."""
+    import numpy as np
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hH = torch.from_numpy(x["hidden"]).to(torch.bfloat16).pin_memory()
+    hW = torch.from_numpy(x["weight"]).to(torch.bfloat16).pin_memory()
+    hy = torch.from_numpy(x["targets"]).pin_memory()
+    o_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    bi = hH.numel() * 2 + hW.numel() * 2 + hy.numel() * 8
+    bo = sum(v.numel() * v.element_size() for v in o_h.values())
+
+    def e2e_step():
+        H.copy_(hH, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        y.copy_(hy, non_blocking=True)
+        step()
+        for k, v in out.items():
+            o_h[k].copy_(v, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    k_e2e = max(3, min(a.steps, 10))
+    e0.record(stream)
+    for _ in range(k_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / k_e2e, world)
+    # the results of the last e2e step match the device-resident ones
+    assert np.array_equal(o_h["scalars_out"].numpy(), out["scalars_out"].cpu().numpy())
+    return {"value": aggregate(n, world, e2e_ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+
+
+def _time(fn, reps, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def extra_paths(L, dev, pk):
+    """The other rows of the hot path, timed the same way: distillation at
+    n=4096, d=2048, V=151936 (T=2, 10% masked, z 1e-4) and cross-entropy from
+    materialised bf16 logits at the Qwen3 head shape (HBM stream)."""
+    import torch
+
+    import lossk_inputs as li
+    res = {}
+    w = li.WORKLOADS["distill_z_4096x2048"]
+    x = li.make(w, seed=0)
+    H = torch.from_numpy(x["hidden"]).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy(x["weight"]).to(dev).to(torch.bfloat16)
+    T = torch.from_numpy(x["teacher"]).to(dev).to(torch.bfloat16)
+    m = torch.from_numpy(x["mask"]).to(dev)
+    del x
+    ws = L.workspace(L.lossk.KIND_DISTILL, w.n_tok, w.d_model, w.vocab, 1, dev)
+    bufs = dict(d_hidden=torch.empty(w.n_tok, w.d_model, device=dev),
+                d_weight=torch.empty(w.vocab, w.d_model, device=dev))
+    for direction in w.directions:
+        def fn():
+            L.lossk_distill_fwd_bwd(H, W, T, direction, temperature=w.temperature, loss_mask=m,
+                                    chunk=w.chunk, z_weight=w.z_weight, ws=ws, **bufs)
+        L.lossk_profile_read(reset=True)
+        L.lossk_profile_enable(True)
+        ms = _time(fn, 3)
+        L.lossk_profile_enable(False)
+        prof = L.lossk_profile_read(reset=True)
+        fl = 6.0 * w.n_tok * w.d_model * w.vocab
+        res[f"distill_{direction}"] = {
+            "workload": w.name, "ms": ms, "tokens_per_s": w.n_tok / (ms / 1e3),
+            "tensor_frac_6ndV": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+            "kernels_ms": {k: v[0] / v[1] for k, v in prof.items()}}
+    del H, W, T, bufs
+    torch.cuda.empty_cache()
+    # CE from materialised logits (HBM-bound): read 622 MB bf16, write 622 MB grad
+    n, V = 2048, 151936
+    g = torch.Generator(device=dev).manual_seed(0)
+    X = torch.randn(n, V, device=dev, generator=g).to(torch.bfloat16)
+    y = torch.randint(0, V, (n,), device=dev, generator=g)
+    grad = torch.empty_like(X)
+    ws = L.workspace(L.lossk.KIND_FROM_LOGITS, n, 1, V, 1, dev)
+    for want in (False, True):
+        def fn():
+            L.lossk_ce_from_logits(X, y, grad_logits=grad if want else None, want_grad=want, ws=ws)
+        L.lossk_profile_read(reset=True)
+        L.lossk_profile_enable(True)
+        ms = _time(fn, 5)
+        L.lossk_profile_enable(False)
+        prof = L.lossk_profile_read(reset=True)
+        kms = prof["from_logits"][0] / prof["from_logits"][1]
+        nbytes = X.numel() * 2 * (2 if want else 1)
+        res["from_logits" + ("_grad" if want else "")] = {
+            "workload": "logits bf16 [2048][151936]", "ms": ms,
+            "kernel_ms": kms, "algorithmic_bytes": nbytes,
+            "achieved_gbs": nbytes / (kms / 1e3) / 1e9,
+            "frac_hbm": nbytes / (kms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    return res
+
+
+# ---- the reference arm: the oracle, as it stands ------------------------------------
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return None
+    import lossk_inputs as li
+    w = li.WORKLOADS[WORKLOAD]
+    x = li.make(w, seed=0)
+    os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+    # size one step's sample so that warmup + steps fit in about three minutes
+    t0 = time.perf_counter()
+    oracle_step(x, 2, w.chunk)
+    t2 = time.perf_counter() - t0
+    per_step = min(8.0, 170.0 / max(1, a.steps + a.warmup))
+    k = int(max(1, min(w.n_tok, 2 * per_step / max(t2, 1e-3))))
+    for _ in range(a.warmup):
+        oracle_step(x, k, w.chunk)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle_step(x, k, w.chunk)
+    dt = (time.perf_counter() - t0) / a.steps
+    v = k / dt
+    sample = f"first {k} tokens of the batch per step (full d_model and vocab), fp64 fwd+bwd"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_tok": w.n_tok, "d_model": w.d_model,
+                       "vocab": w.vocab, "chunk": w.chunk, "targets": w.targets},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    a = args_parse()
+    if a.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks exit at once
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(a, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, local = dist_init()
+    res = run_ours(a, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -239,6 +239,21 @@ int32_t lossk_distill_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int
  * error word: 580 (none), 590 (a bounded device wait timed out) or 589. */
 int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
 
+/* ---- tracing ----------------------------------------------------------------
+ * Every kernel the library launches belongs to one of LOSSK_N_KERNELS kinds
+ * (lossk_kernel_name gives its name).  lossk_launch_count() is the number of
+ * kernels launched by this process so far.  With lossk_profile_enable(1),
+ * each launch is bracketed by a CUDA event pair recorded on its own stream
+ * (no synchronisation is added); lossk_profile_read() waits for the recorded
+ * events, adds their durations per kind into total_ms[kind] and
+ * launches[kind] (host arrays of `cap` entries), and clears them if `reset`.
+ * Returns the number of kinds written, or -1 on a CUDA error. */
+#define LOSSK_N_KERNELS 13
+const char *lossk_kernel_name(int32_t kind);
+int64_t lossk_launch_count(void);
+int32_t lossk_profile_enable(int32_t on);
+int32_t lossk_profile_read(double *total_ms, int64_t *launches, int32_t cap, int32_t reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -64,8 +64,10 @@ WORKLOADS = {
 }
 
 
-def rng(seed: int, stream: int) -> np.random.Generator:
-    return np.random.default_rng([seed, stream])
+def rng(seed: int, stream: int, batch: int = 0) -> np.random.Generator:
+    """Batch 0 is the workload's own batch; batch b > 0 is another batch drawn
+    with the same recipe (a data-parallel rank's share), same weight."""
+    return np.random.default_rng([seed, stream] if batch == 0 else [seed, stream, batch])
 
 
 def to_bf16_values(x: np.ndarray) -> np.ndarray:
@@ -75,27 +77,27 @@ def to_bf16_values(x: np.ndarray) -> np.ndarray:
         torch.bfloat16).to(torch.float32).numpy()
 
 
-def _normal(seed, stream, shape, std, dtype):
-    x = rng(seed, stream).standard_normal(size=shape, dtype=np.float32)
+def _normal(seed, stream, shape, std, dtype, batch=0):
+    x = rng(seed, stream, batch).standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
     return to_bf16_values(x) if dtype == "bf16" else x
 
 
-def hidden(seed, n, d, std=1.0, dtype="bf16"):
-    return _normal(seed, STREAM_HIDDEN, (n, d), std, dtype)
+def hidden(seed, n, d, std=1.0, dtype="bf16", batch=0):
+    return _normal(seed, STREAM_HIDDEN, (n, d), std, dtype, batch)
 
 
 def weight(seed, V, d, std=0.02, dtype="bf16"):
     return _normal(seed, STREAM_WEIGHT, (V, d), std, dtype)
 
 
-def teacher(seed, n, V, std=3.0):
-    return _normal(seed, STREAM_TEACHER, (n, V), std, "bf16")
+def teacher(seed, n, V, std=3.0, batch=0):
+    return _normal(seed, STREAM_TEACHER, (n, V), std, "bf16", batch)
 
 
-def targets(seed, n, V, kind="uniform"):
-    g = rng(seed, STREAM_TARGETS)
+def targets(seed, n, V, kind="uniform", batch=0):
+    g = rng(seed, STREAM_TARGETS, batch)
     if kind == "uniform":
         return g.integers(0, V, size=n, dtype=np.int64)
     if kind.startswith("zipf"):
@@ -108,20 +110,22 @@ def targets(seed, n, V, kind="uniform"):
     raise ValueError(kind)
 
 
-def mask(seed, n, frac):
+def mask(seed, n, frac, batch=0):
     """uint8 mask, 1 = token counts; exactly round(frac*n) tokens are 0."""
     m = np.ones(n, dtype=np.uint8)
     k = int(round(frac * n))
     if k:
-        m[rng(seed, STREAM_MASK).choice(n, k, replace=False)] = 0
+        m[rng(seed, STREAM_MASK, batch).choice(n, k, replace=False)] = 0
     return m
 
 
-def make(w: Workload | str, seed: int = 0, n_tok=None, d_model=None, vocab=None):
+def make(w: Workload | str, seed: int = 0, n_tok=None, d_model=None, vocab=None, batch=0):
     """Draw a workload's inputs (optionally at overridden sizes, same recipe).
 
     Returns a dict of float32/int64/uint8 numpy arrays: hidden [n][d],
     weight [V][d], targets [n], mask [n] or None, teacher [n][V] or None.
+    `batch` selects another batch (hidden, targets, mask, teacher) for the
+    same weight.
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
@@ -129,10 +133,10 @@ def make(w: Workload | str, seed: int = 0, n_tok=None, d_model=None, vocab=None)
     d = d_model or w.d_model
     V = vocab or w.vocab
     out = {
-        "hidden": hidden(seed, n, d, w.hidden_std, w.dtype),
+        "hidden": hidden(seed, n, d, w.hidden_std, w.dtype, batch),
         "weight": weight(seed, V, d, w.weight_std, w.dtype),
-        "targets": targets(seed, n, V, w.targets),
-        "mask": mask(seed, n, w.mask_frac) if w.mask_frac > 0 else None,
-        "teacher": teacher(seed, n, V, w.teacher_std) if w.teacher_std > 0 else None,
+        "targets": targets(seed, n, V, w.targets, batch),
+        "mask": mask(seed, n, w.mask_frac, batch) if w.mask_frac > 0 else None,
+        "teacher": teacher(seed, n, V, w.teacher_std, batch) if w.teacher_std > 0 else None,
     }
     return out

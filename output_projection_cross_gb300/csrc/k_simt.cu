@@ -57,31 +57,60 @@ cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t
 }
 
 // ---------------------------------------------------------------------------
-__global__ void merge_ce_kernel(const float *__restrict__ part, const float *__restrict__ tgt,
-                                const int64_t *__restrict__ targets, const uint8_t *__restrict__ mask,
-                                int64_t n, int64_t n_ct, int64_t n_pad, double wz,
-                                float *__restrict__ lse_out, float *__restrict__ ce_out,
-                                double *__restrict__ tokacc)
+// Merging the per-tile partials of each token.  A block covers 32 tokens
+// (threadIdx.x, so every load of one tile's partials is a 128-byte line) and
+// splits the tiles into MG contiguous groups (threadIdx.y).  Pass 1 takes the
+// maximum; pass 2 sums z_c * 2^(m_c - M) per group in double (the exp2 is
+// the fp32 ex2.approx, relative error about 2^-22 per term); the MG group
+// sums are then added in group order.  The tile-to-thread map depends only
+// on n_ct, so the result is the same bits for every run.
+constexpr int MG = 8;
+
+__device__ __forceinline__ void tile_range(int64_t n_ct, int g, int64_t &c0, int64_t &c1)
 {
-    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (t >= n) return;
+    c0 = n_ct * g / MG;
+    c1 = n_ct * (g + 1) / MG;
+}
+
+__global__ void __launch_bounds__(32 * MG) merge_ce_kernel(
+    const float *__restrict__ part, const float *__restrict__ tgt, const uint8_t *__restrict__ mask,
+    int64_t n, int64_t n_ct, int64_t n_pad, double wz, float *__restrict__ lse_out,
+    float *__restrict__ ce_out, double *__restrict__ tokacc)
+{
+    __shared__ float smax[MG][32];
+    __shared__ double ssum[MG][32];
+    const int tx = threadIdx.x, g = threadIdx.y;
+    const int64_t t = blockIdx.x * 32 + tx;
+    const bool live = t < n;
     const float *m2 = part;
-    const float *z = part + n_ct * n_pad;
+    const float *zz = part + n_ct * n_pad;
+    int64_t c0, c1;
+    tile_range(n_ct, g, c0, c1);
     float M = -INFINITY;
-    for (int64_t c = 0; c < n_ct; ++c) M = fmaxf(M, m2[c * n_pad + t]);
+    if (live)
+        for (int64_t c = c0; c < c1; ++c) M = fmaxf(M, m2[c * n_pad + t]);
+    smax[g][tx] = M;
+    __syncthreads();
+    M = smax[0][tx];
+    for (int k = 1; k < MG; ++k) M = fmaxf(M, smax[k][tx]);
     double Z = 0.0;
-    for (int64_t c = 0; c < n_ct; ++c)
-        Z += static_cast<double>(z[c * n_pad + t]) * exp2(static_cast<double>(m2[c * n_pad + t]) - M);
+    if (live)
+        for (int64_t c = c0; c < c1; ++c)
+            Z += static_cast<double>(zz[c * n_pad + t] * ex2_approx(m2[c * n_pad + t] - M));
+    ssum[g][tx] = Z;
+    __syncthreads();
+    if (g != 0 || !live) return;
+    Z = ssum[0][tx];
+    for (int k = 1; k < MG; ++k) Z += ssum[k][tx];
     const double lse = (static_cast<double>(M) + log2(Z)) * LN2;
     const bool on = mask ? (mask[t] != 0) : true;
     const double ce = on ? lse - static_cast<double>(tgt[t]) : 0.0;
-    const double zz = on ? lse * lse : 0.0;
+    const double z2 = on ? lse * lse : 0.0;
     lse_out[t] = static_cast<float>(lse);
     if (ce_out) ce_out[t] = static_cast<float>(ce);
-    tokacc[t] = ce + wz * zz;
+    tokacc[t] = ce + wz * z2;
     tokacc[n_pad + t] = ce;
-    tokacc[2 * n_pad + t] = zz;
-    (void)targets;
+    tokacc[2 * n_pad + t] = z2;
 }
 
 cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
@@ -89,40 +118,70 @@ cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *
                             double wz, float *lse_out, float *ce_out, double *tokacc,
                             cudaStream_t st)
 {
-    merge_ce_kernel<<<static_cast<int>((n + 127) / 128), 128, 0, st>>>(
-        part, tgt, targets, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
+    (void)targets;
+    merge_ce_kernel<<<static_cast<unsigned>((n + 31) / 32), dim3(32, MG), 0, st>>>(
+        part, tgt, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-__global__ void merge_distill_kernel(const float *__restrict__ part, const uint8_t *__restrict__ mask,
-                                     int64_t n, int64_t n_ct, int64_t n_pad, int direction,
-                                     double wz, float *__restrict__ lse_out,
-                                     float *__restrict__ per_token, double *__restrict__ tokacc,
-                                     float4 *__restrict__ tokp, double alpha, double temperature)
+__global__ void __launch_bounds__(32 * MG) merge_distill_kernel(
+    const float *__restrict__ part, const uint8_t *__restrict__ mask, int64_t n, int64_t n_ct,
+    int64_t n_pad, int direction, double wz, float *__restrict__ lse_out,
+    float *__restrict__ per_token, double *__restrict__ tokacc, float4 *__restrict__ tokp,
+    double alpha, double temperature)
 {
-    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (t >= n_pad) return;
-    if (t >= n) {
-        tokp[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        return;
-    }
+    __shared__ float smax[2][MG][32];
+    __shared__ double ssum[3][MG][32];
+    const int tx = threadIdx.x, g = threadIdx.y;
+    const int64_t t = blockIdx.x * 32 + tx;
+    const bool live = t < n;         // the grid covers exactly n_pad tokens
     const int64_t pl = n_ct * n_pad;
     const float *ms = part, *zs = part + pl, *mt = part + 2 * pl, *zt = part + 3 * pl,
                 *xx = part + 4 * pl;
+    int64_t c0, c1;
+    tile_range(n_ct, g, c0, c1);
     float Ms = -INFINITY, Mt = -INFINITY;
-    for (int64_t c = 0; c < n_ct; ++c) {
-        Ms = fmaxf(Ms, ms[c * n_pad + t]);
-        Mt = fmaxf(Mt, mt[c * n_pad + t]);
+    if (live)
+        for (int64_t c = c0; c < c1; ++c) {
+            Ms = fmaxf(Ms, ms[c * n_pad + t]);
+            Mt = fmaxf(Mt, mt[c * n_pad + t]);
+        }
+    smax[0][g][tx] = Ms;
+    smax[1][g][tx] = Mt;
+    __syncthreads();
+    Ms = smax[0][0][tx];
+    Mt = smax[1][0][tx];
+    for (int k = 1; k < MG; ++k) {
+        Ms = fmaxf(Ms, smax[0][k][tx]);
+        Mt = fmaxf(Mt, smax[1][k][tx]);
     }
     double Zs = 0.0, Zt = 0.0, X = 0.0;
-    for (int64_t c = 0; c < n_ct; ++c) {
-        const int64_t o = c * n_pad + t;
-        const double fs = exp2(static_cast<double>(ms[o]) - Ms);
-        const double ft = exp2(static_cast<double>(mt[o]) - Mt);
-        Zs += zs[o] * fs;
-        Zt += zt[o] * ft;
-        X += xx[o] * (direction == DIR_RKL ? fs : ft);
+    if (live)
+        for (int64_t c = c0; c < c1; ++c) {
+            const int64_t o = c * n_pad + t;
+            const float fs = ex2_approx(ms[o] - Ms);
+            const float ft = ex2_approx(mt[o] - Mt);
+            Zs += static_cast<double>(zs[o] * fs);
+            Zt += static_cast<double>(zt[o] * ft);
+            X += static_cast<double>(xx[o] * (direction == DIR_RKL ? fs : ft));
+        }
+    ssum[0][g][tx] = Zs;
+    ssum[1][g][tx] = Zt;
+    ssum[2][g][tx] = X;
+    __syncthreads();
+    if (g != 0) return;
+    if (!live) {
+        tokp[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    Zs = ssum[0][0][tx];
+    Zt = ssum[1][0][tx];
+    X = ssum[2][0][tx];
+    for (int k = 1; k < MG; ++k) {
+        Zs += ssum[0][k][tx];
+        Zt += ssum[1][k][tx];
+        X += ssum[2][k][tx];
     }
     const double lse_s = (static_cast<double>(Ms) + log2(Zs)) * LN2;
     const double lse_t = (static_cast<double>(Mt) + log2(Zt)) * LN2;
@@ -133,12 +192,12 @@ __global__ void merge_distill_kernel(const float *__restrict__ part, const uint8
     else L = E - lse_s + lse_t;
     const bool on = mask ? (mask[t] != 0) : true;
     const double Lm = on ? L : 0.0;
-    const double zz = on ? lse_s * lse_s : 0.0;
+    const double z2 = on ? lse_s * lse_s : 0.0;
     if (lse_out) lse_out[t] = static_cast<float>(lse_s);
     if (per_token) per_token[t] = static_cast<float>(Lm);
-    tokacc[t] = Lm + wz * zz;
+    tokacc[t] = Lm + wz * z2;
     tokacc[n_pad + t] = Lm;
-    tokacc[2 * n_pad + t] = zz;
+    tokacc[2 * n_pad + t] = z2;
     const double at = on ? alpha / temperature : 0.0;
     float4 P;
     P.x = static_cast<float>(lse_s * LOG2E);
@@ -158,7 +217,7 @@ cudaError_t launch_merge_distill(const float *part, const uint8_t *mask, int64_t
                                  float *per_token, double *tokacc, float4 *tokp, double alpha,
                                  double temperature, cudaStream_t st)
 {
-    merge_distill_kernel<<<static_cast<int>((n_pad + 127) / 128), 128, 0, st>>>(
+    merge_distill_kernel<<<static_cast<unsigned>((n_pad + 31) / 32), dim3(32, MG), 0, st>>>(
         part, mask, n, n_ct, n_pad, direction, wz, lse_out, per_token, tokacc, tokp, alpha,
         temperature);
     return cudaGetLastError();

@@ -5,9 +5,11 @@
 #include "../../include/lossk.h"
 #include "lossk_internal.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 using namespace lossk;
 
@@ -77,6 +79,68 @@ bool make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---- tracing: launch counter and optional per-kernel event timing ------------
+std::atomic<int64_t> g_launches{0};
+
+struct Profiler {
+    std::mutex mu;
+    std::atomic<bool> on{false};
+    struct Pending {
+        int kind;
+        cudaEvent_t a, b;
+    };
+    std::vector<Pending> pending;
+    std::vector<cudaEvent_t> pool;
+    double ms[KK_N] = {};
+    int64_t count[KK_N] = {};
+    cudaEvent_t get()
+    {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        return e;
+    }
+};
+
+Profiler &profiler()
+{
+    static Profiler p;
+    return p;
+}
+
+// Brackets one kernel launch: counts it and, when profiling is on, records an
+// event pair around it on its stream.
+class Launch {
+  public:
+    Launch(int kind, cudaStream_t st) : kind_(kind), st_(st)
+    {
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        Profiler &p = profiler();
+        if (!p.on.load(std::memory_order_relaxed)) return;
+        std::lock_guard<std::mutex> g(p.mu);
+        a_ = p.get();
+        b_ = p.get();
+        if (a_ && b_ && cudaEventRecord(a_, st_) == cudaSuccess) active_ = true;
+    }
+    ~Launch()
+    {
+        if (!active_) return;
+        Profiler &p = profiler();
+        std::lock_guard<std::mutex> g(p.mu);
+        if (cudaEventRecord(b_, st_) == cudaSuccess) p.pending.push_back({kind_, a_, b_});
+    }
+
+  private:
+    int kind_;
+    cudaStream_t st_;
+    cudaEvent_t a_ = nullptr, b_ = nullptr;
+    bool active_ = false;
+};
+
 struct Hdr {
     int err, bad, n_valid;
 };
@@ -87,7 +151,10 @@ int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DE
 int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V, WsHeader *hdr,
                  cudaStream_t st, Hdr *h)
 {
-    if (launch_validate(targets, mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    {
+        Launch k(KK_VALIDATE, st);
+        if (launch_validate(targets, mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    }
     int buf[3] = {0, 0, 0};
     if (cudaMemcpyAsync(buf, hdr, sizeof(buf), cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return LOSSK_DEVICE_ERROR;
@@ -140,16 +207,22 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
         a.part_plane = L.n_ct * L.n_pad;
         a.err = &w.hdr()->err;
         const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        Launch k(KK_TC_STATS, st);
         e = launch_tc(TC_STATS, false, a, grid, st);
     } else {
+        Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, false, H, W, nullptr, static_cast<int>(n), static_cast<int>(V),
                       static_cast<int>(d), static_cast<int>(n), static_cast<int>(V), 1, 0, 1.f,
                       targets, nullptr, w.part(), w.tgt(), L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    e = launch_merge_ce(w.part(), w.tgt(), targets, mask, n, L.n_ct, L.n_pad, wz, lse_out, ce_out,
-                        w.tokacc(), st);
+    {
+        Launch k(KK_MERGE_CE, st);
+        e = launch_merge_ce(w.part(), w.tgt(), targets, mask, n, L.n_ct, L.n_pad, wz, lse_out,
+                            ce_out, w.tokacc(), st);
+    }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    Launch k(KK_REDUCE, st);
     return status_of(launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st));
 }
 
@@ -190,9 +263,13 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.out_split_stride = n * d;
             a.err = &w.hdr()->err;
             const int grid = a.n_xt * a.n_slices * a.n_split;
-            e = launch_tc(rows ? TC_ROWS : TC_COLS, distill, a, grid, st);
+            {
+                Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
+                e = launch_tc(rows ? TC_ROWS : TC_COLS, distill, a, grid, st);
+            }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {
+                Launch k(KK_SUM_SPLITS, st);
                 e = launch_sum_splits(w.dhpart(), L.nsplit, n * d, d_hidden, st);
                 if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             }
@@ -206,12 +283,16 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             const int64_t nx = rows ? n : V, ny = rows ? V : n;
             const int64_t nsplit = rows ? L.nsplit : 1;
             float *out = (rows && nsplit > 1) ? w.dhpart() : dst;
-            e = launch_fp(rows ? TC_ROWS : TC_COLS, distill, X, Y, static_cast<const float *>(teacher),
+            {
+                Launch k(rows ? KK_FP_ROWS : KK_FP_COLS, st);
+                e = launch_fp(rows ? TC_ROWS : TC_COLS, distill, X, Y, static_cast<const float *>(teacher),
                           static_cast<int>(nx), static_cast<int>(ny), static_cast<int>(d),
                           static_cast<int>(n), static_cast<int>(V), static_cast<int>(nsplit),
                           direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, 0, 0, out, n * d, st);
+            }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && nsplit > 1) {
+                Launch k(KK_SUM_SPLITS, st);
                 e = launch_sum_splits(w.dhpart(), nsplit, n * d, d_hidden, st);
                 if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             }
@@ -405,8 +486,11 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     }
     if (do_bwd && (dH || dW)) {
         const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
-        if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, alpha, wz, w.tokp(), st) != cudaSuccess)
-            return LOSSK_DEVICE_ERROR;
+        {
+            Launch k(KK_TOKP, st);
+            if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, alpha, wz, w.tokp(), st) != cudaSuccess)
+                return LOSSK_DEVICE_ERROR;
+        }
         s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st);
     }
     return s;
@@ -471,9 +555,13 @@ int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *lo
     int32_t s = validate(targets, loss_mask, n, V, w.hdr(), st, &h);
     if (s != LOSSK_OK) return s;
     const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
-    if (launch_from_logits(dtype, logits, targets, loss_mask, n, V, z_weight, alpha, lse_out, ce_out,
-                           w.tokacc(), grad_logits, st) != cudaSuccess)
-        return LOSSK_DEVICE_ERROR;
+    {
+        Launch k(KK_FROM_LOGITS, st);
+        if (launch_from_logits(dtype, logits, targets, loss_mask, n, V, z_weight, alpha, lse_out,
+                               ce_out, w.tokacc(), grad_logits, st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    Launch k(KK_REDUCE, st);
     return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st));
 }
 
@@ -522,8 +610,10 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
         a.part_plane = L.n_ct * L.n_pad;
         a.err = &w.hdr()->err;
         const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        Launch k(KK_TC_STATS, st);
         e = launch_tc(TC_STATS, true, a, grid, st);
     } else {
+        Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, true, hidden, weight, static_cast<const float *>(teacher),
                       static_cast<int>(n), static_cast<int>(V), static_cast<int>(d), static_cast<int>(n),
                       static_cast<int>(V), 1, direction, static_cast<float>(1.0 / temperature), nullptr,
@@ -531,10 +621,16 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
-    e = launch_merge_distill(w.part(), loss_mask, n, L.n_ct, L.n_pad, direction, z_weight, lse_out,
-                             per_token_out, w.tokacc(), w.tokp(), alpha, temperature, st);
+    {
+        Launch k(KK_MERGE_DISTILL, st);
+        e = launch_merge_distill(w.part(), loss_mask, n, L.n_ct, L.n_pad, direction, z_weight,
+                                 lse_out, per_token_out, w.tokacc(), w.tokp(), alpha, temperature, st);
+    }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), z_weight, scalars_out, st);
+    {
+        Launch k(KK_REDUCE, st);
+        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), z_weight, scalars_out, st);
+    }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     if (!d_hidden && !d_weight) return LOSSK_OK;
     return run_acc(w, n, d, V, dtype, hidden, weight, teacher, true, direction, temperature, d_hidden,
@@ -554,6 +650,53 @@ int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stre
     if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
         return LOSSK_DEVICE_ERROR;
     return LOSSK_DEVICE_TIMEOUT;
+}
+
+const char *lossk_kernel_name(int32_t kind)
+{
+    static const char *names[KK_N] = {"validate",     "tc_stats",      "tc_rows",     "tc_cols",
+                                      "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
+                                      "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
+                                      "from_logits"};
+    return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
+}
+
+int64_t lossk_launch_count(void) { return g_launches.load(); }
+
+int32_t lossk_profile_enable(int32_t on)
+{
+    profiler().on.store(on != 0);
+    return LOSSK_OK;
+}
+
+int32_t lossk_profile_read(double *total_ms, int64_t *launches, int32_t cap, int32_t reset)
+{
+    Profiler &p = profiler();
+    std::lock_guard<std::mutex> g(p.mu);
+    int32_t rc = 0;
+    for (auto &q : p.pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(q.b) != cudaSuccess || cudaEventElapsedTime(&ms, q.a, q.b) != cudaSuccess)
+            rc = -1;
+        else {
+            p.ms[q.kind] += ms;
+            p.count[q.kind] += 1;
+        }
+        p.pool.push_back(q.a);
+        p.pool.push_back(q.b);
+    }
+    p.pending.clear();
+    const int32_t k = cap < KK_N ? cap : KK_N;
+    for (int32_t i = 0; i < k; ++i) {
+        if (total_ms) total_ms[i] = p.ms[i];
+        if (launches) launches[i] = p.count[i];
+    }
+    if (reset)
+        for (int i = 0; i < KK_N; ++i) {
+            p.ms[i] = 0.0;
+            p.count[i] = 0;
+        }
+    return rc < 0 ? rc : k;
 }
 
 } // extern "C"

@@ -86,6 +86,24 @@ struct TcArgs {
     int *err;
 };
 
+// Kernel kinds, for the launch counter and the optional per-kernel timing.
+enum KernelKind : int {
+    KK_VALIDATE = 0,
+    KK_TC_STATS,
+    KK_TC_ROWS,
+    KK_TC_COLS,
+    KK_FP_STATS,
+    KK_FP_ROWS,
+    KK_FP_COLS,
+    KK_MERGE_CE,
+    KK_MERGE_DISTILL,
+    KK_REDUCE,
+    KK_TOKP,
+    KK_SUM_SPLITS,
+    KK_FROM_LOGITS,
+    KK_N
+};
+
 // ---- launchers (all enqueue on `st`) -----------------------------------------
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);

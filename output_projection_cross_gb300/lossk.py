@@ -57,6 +57,10 @@ def _load():
                                          _i64, _vp, _i32, _dbl, _dbl, _dbl, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _i64, _vp]),
         "lossk_device_status": (_i32, [_vp, _i64, _vp]),
+        "lossk_kernel_name": (ctypes.c_char_p, [_i32]),
+        "lossk_launch_count": (_i64, []),
+        "lossk_profile_enable": (_i32, [_i32]),
+        "lossk_profile_read": (_i32, [ctypes.POINTER(_dbl), ctypes.POINTER(_i64), _i32, _i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -69,7 +73,9 @@ lib = _load()
 EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk_logit_cells",
             "lossk_work_fits", "lossk_peak_logit_cells", "lossk_workspace_bytes",
             "lossk_targets_check", "lossk_ce_fwd", "lossk_ce_bwd", "lossk_ce_fwd_bwd",
-            "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status")
+            "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status",
+            "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
+N_KERNELS = 13
 
 
 class LosskError(RuntimeError):
@@ -290,3 +296,27 @@ def lossk_distill_fwd_bwd(hidden, weight, teacher_logits, direction="fkl", tempe
 
 def lossk_device_status(ws, stream=None) -> int:
     return lib.lossk_device_status(_ptr(ws), ws.numel(), _stream(stream))
+
+
+# ---- tracing ------------------------------------------------------------------
+
+def lossk_kernel_name(kind: int) -> str:
+    return lib.lossk_kernel_name(kind).decode()
+
+
+def lossk_launch_count() -> int:
+    return lib.lossk_launch_count()
+
+
+def lossk_profile_enable(on: bool = True) -> None:
+    lib.lossk_profile_enable(1 if on else 0)
+
+
+def lossk_profile_read(reset: bool = True) -> dict:
+    """{kernel name: (total ms, launches)} for the kernels launched while profiling."""
+    ms = (_dbl * N_KERNELS)()
+    cnt = (_i64 * N_KERNELS)()
+    k = lib.lossk_profile_read(ms, cnt, N_KERNELS, 1 if reset else 0)
+    if k < 0:
+        raise LosskError(589, "lossk_profile_read")
+    return {lossk_kernel_name(i): (ms[i], cnt[i]) for i in range(k) if cnt[i]}

@@ -24,7 +24,7 @@ import torch
 import oracle
 from oracle import brute
 
-torch.set_default_dtype(torch.float64)
+F64 = torch.float64
 
 
 def _rand(seed, n, d, V, hs=1.0, ws=0.3):
@@ -345,7 +345,7 @@ def _torch_distill(H, W, Tt, direction, T, mask, wz):
     else:
         L = torch.nn.functional.kl_div(lp, a, reduction="none", log_target=True).sum(1)
     lse = torch.logsumexp(H @ W.T / T, dim=1)
-    m = torch.ones(H.shape[0]) if mask is None else torch.tensor(mask, dtype=torch.float64)
+    m = torch.ones(H.shape[0], dtype=F64) if mask is None else torch.tensor(mask, dtype=F64)
     return ((L + wz * lse * lse) * m).sum() / m.sum(), L
 
 
