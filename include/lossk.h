@@ -239,6 +239,36 @@ int32_t lossk_distill_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int
  * error word: 580 (none), 590 (a bounded device wait timed out) or 589. */
 int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
 
+/* lossk_ce_from_logits without a workspace, for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers have no way to give the library scratch memory: a plug-in
+ * inside another framework whose device memory is all owned by that
+ * framework's arena, or a runtime whose memory plan is fixed at start-up and
+ * which treats any allocation made during a step as an error.  This variant
+ * computes exactly what lossk_ce_from_logits computes (same kernels, same
+ * outputs, same status codes) but keeps its scratch -- a 256-byte header and
+ * three doubles per token -- in a device array built into the library, so
+ * the call allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library routine).  The caller still passes every input and output.
+ *
+ * Limits and rules:
+ *  - n_tok <= 16384 (the array holds 256 + 3*8*16384 bytes, about 384 KB,
+ *    held by every GPU that loads the library until the process exits);
+ *    larger n_tok returns 583.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture on that device.
+ *  - All calls share the one array, which keeps the previous call's
+ *    contents; each call clears the header before use.  Calls that overlap
+ *    on the GPU (two streams, or two host threads on one device) race on it
+ *    and must be serialised by the caller. */
+int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype, const void *logits,
+                                    int64_t logits_len, const int64_t *targets, int64_t targets_len,
+                                    const uint8_t *loss_mask, double z_weight, double grad_scale,
+                                    float *lse_out, float *ce_out, double *scalars_out,
+                                    void *grad_logits, int64_t grad_len, lossk_stream_t stream);
+
 /* ---- tracing ----------------------------------------------------------------
  * Every kernel the library launches belongs to one of LOSSK_N_KERNELS kinds
  * (lossk_kernel_name gives its name).  lossk_launch_count() is the number of

@@ -57,6 +57,8 @@ def _load():
                                          _i64, _vp, _i32, _dbl, _dbl, _dbl, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _i64, _vp]),
         "lossk_device_status": (_i32, [_vp, _i64, _vp]),
+        "lossk_ce_from_logits_static": (_i32, [_i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _dbl,
+                                               _dbl, _vp, _vp, _vp, _vp, _i64, _vp]),
         "lossk_kernel_name": (ctypes.c_char_p, [_i32]),
         "lossk_launch_count": (_i64, []),
         "lossk_profile_enable": (_i32, [_i32]),
@@ -74,7 +76,7 @@ EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk
             "lossk_work_fits", "lossk_peak_logit_cells", "lossk_workspace_bytes",
             "lossk_targets_check", "lossk_ce_fwd", "lossk_ce_bwd", "lossk_ce_fwd_bwd",
             "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status",
-            "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
+            "lossk_ce_from_logits_static", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
 N_KERNELS = 13
 
 
@@ -259,6 +261,30 @@ def lossk_ce_from_logits(logits, targets, loss_mask=None, z_weight=0.0, grad_sca
                                   _ptr(lse_out), _ptr(ce_out), _ptr(scalars_out), _ptr(grad_logits),
                                   _len(grad_logits), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lossk_ce_from_logits")
+    return {"lse": lse_out, "ce": ce_out, "scalars": scalars_out, "grad_logits": grad_logits}
+
+
+def lossk_ce_from_logits_static(logits, targets, loss_mask=None, z_weight=0.0, grad_scale=1.0,
+                                want_grad=False, lse_out=None, ce_out=None, scalars_out=None,
+                                grad_logits=None, stream=None):
+    """lossk_ce_from_logits without a workspace: scratch lives in a device array built
+    into the library (n_tok <= 16384).  Outputs left as None are created here with torch;
+    a caller that must not allocate passes them all in."""
+    for t, nm in ((logits, "logits"), (targets, "targets"), (loss_mask, "loss_mask")):
+        _contig(t, nm)
+    n, V = logits.shape
+    dt = _dtype_code(logits)
+    dev = logits.device
+    lse_out = lse_out if lse_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    ce_out = ce_out if ce_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    scalars_out = scalars_out if scalars_out is not None else torch.empty(3, dtype=torch.float64, device=dev)
+    if want_grad and grad_logits is None:
+        grad_logits = torch.empty_like(logits)
+    st = lib.lossk_ce_from_logits_static(n, V, dt, _ptr(logits), _len(logits), _ptr(targets),
+                                         _len(targets), _ptr(loss_mask), z_weight, grad_scale,
+                                         _ptr(lse_out), _ptr(ce_out), _ptr(scalars_out),
+                                         _ptr(grad_logits), _len(grad_logits), _stream(stream))
+    _check(st, "lossk_ce_from_logits_static")
     return {"lse": lse_out, "ce": ce_out, "scalars": scalars_out, "grad_logits": grad_logits}
 
 
