@@ -1,0 +1,432 @@
+// k_bwd.cu -- the backward passes of the fused LM-head loss on tcgen05, with
+// each recomputed grad_logits tile shared across a thread-block cluster.
+//
+// d_hidden = G W and d_weight = G^T H need a [128 x d_model] fp32 accumulator
+// per tile, wider than tensor memory (512 columns).  So the accumulator is
+// split into 256-column d-slices, one per CTA of a cluster of c CTAs.  All
+// CTAs of a cluster share one "fixed" tile (token tile for d_hidden, vocabulary
+// tile for d_weight) and walk the same "loop" tiles.  Loop tile y's logits
+// S = H_tok . W_voc^T (token rows x vocabulary columns, contraction over the
+// whole d_model) are computed once, by CTA y % c; its epilogue turns them into
+// grad_logits G (bf16) -- "Fuse distillation + z-loss ...", "What it does":
+// prob_coeff * softmax - label_coeff * onehot, with the z term folded into
+// prob_coeff, or the distribution-family form -- and writes G into grad slot
+// y % R of its own shared memory, then pushes it to the other CTAs with bulk
+// shared-to-distributed-shared copies.  Every CTA then adds G times its
+// d-slice of the loop tile into its accumulator:
+//   d_hidden (BWD_ROWS): D[tok][slice] += G[tok][voc] . W[voc][slice]  (A = G, K-major)
+//   d_weight (BWD_COLS): D[voc][slice] += G^T[voc][tok] . H[tok][slice] (A = G, MN-major)
+// A grad slot is reused once every CTA's MMA has consumed it: each CTA's
+// tcgen05.commit arrives (multicast) on the next producer's slot barrier.
+//
+// Roles per CTA (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2-5 epilogue (one token row per thread).  TMEM: two 128-column
+// logit buffers and the 256-column accumulator.  Every wait is bounded.
+#include "lossk_internal.h"
+#include "ptx.cuh"
+
+namespace lossk {
+
+template <bool DISTILL> struct BwdCfg {
+    static constexpr int BN = 128;                  // loop-tile rows per logit tile
+    static constexpr int STAGE_BYTES = 32768;       // X+Y k-slices, or 64 rows x 256-column slice
+    static constexpr int STAGES = 3;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int G_TILE = 32768;            // 128 x 128 bf16
+    static constexpr int R_MAX = DISTILL ? 2 : 4;   // grad slots
+    static constexpr int G_BYTES = R_MAX * G_TILE;
+    // Two teacher buffers: with one, the producer would wait for epilogue r
+    // before issuing tile r+1's logit stages, while epilogue r can wait (for
+    // its grad slot) on MMAs issued after those stages.
+    static constexpr int T_BYTES = DISTILL ? 2 * 32768 : 0;
+    static constexpr int NBARS = 2 * STAGES + 2 + 2 + 1 + 4 + 2 * R_MAX + 1;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + G_BYTES + T_BYTES + NBARS * 8 + 16;
+    static_assert(SMEM_BYTES <= 232448, "fits the 227 KB per-CTA shared memory limit");
+};
+
+__device__ __forceinline__ float bw_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bw_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void bw_wait_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > 200000000ull) return;
+}
+
+template <int MODE, bool DISTILL>
+__global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
+{
+    using C = BwdCfg<DISTILL>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *ring = smem;
+    uint8_t *gbuf = ring + C::RING_BYTES;
+    uint8_t *teach = gbuf + C::G_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(teach + C::T_BYTES);
+    uint64_t *full = bars;                 // [S]
+    uint64_t *empty = full + S;            // [S]
+    uint64_t *tfull = empty + S;           // [2] logit tile ready in TMEM buffer
+    uint64_t *tempty = tfull + 2;          // [2] epilogue done with TMEM buffer
+    uint64_t *accfull = tempty + 2;
+    uint64_t *thfull = accfull + 1;        // [2] teacher tile landed
+    uint64_t *thempty = thfull + 2;        // [2] teacher tile consumed
+    uint64_t *gfull = thempty + 2;         // [R_MAX] grad slot filled (4 warp arrivals + bytes)
+    uint64_t *gempty = gfull + C::R_MAX;   // [R_MAX] grad slot consumed by every CTA (c arrivals)
+    uint64_t *drain = gempty + C::R_MAX;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *err = a.err;
+    const int c = a.n_cl, R = a.g_slots;
+    const int crank = static_cast<int>(cluster_ctarank());
+    int cid = blockIdx.x / c;
+    const int dg = cid % a.n_dg;
+    cid /= a.n_dg;
+    const int fixed = cid % a.n_fixed;
+    const int split = cid / a.n_fixed;
+    const int slice0 = (dg * c + crank) * TC_SLICE;
+    const int yt_begin = static_cast<int>((static_cast<int64_t>(split) * a.n_loop) / a.n_split);
+    const int yt_end = static_cast<int>((static_cast<int64_t>(split + 1) * a.n_loop) / a.n_split);
+    const int ny = yt_end - yt_begin;
+    const int nr = (ny + c - 1) / c;                       // rounds of c loop tiles
+    const int n_own = crank < ny ? (ny - crank + c - 1) / c : 0;
+    const int s_own = crank % R;                           // this CTA's grad slot
+    // token / vocabulary origin of loop tile y (0-based within the split)
+    auto tile_origin = [&](int y, int &tok0, int &voc0) {
+        const int t = yt_begin + y;
+        if (MODE == BWD_ROWS) { tok0 = fixed * 128; voc0 = t * 128; }
+        else { voc0 = fixed * 128; tok0 = t * 128; }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(accfull, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&thfull[b], 1);
+            mbar_init(&thempty[b], 128);
+        }
+        for (int s = 0; s < C::R_MAX; ++s) {
+            mbar_init(&gfull[s], 4);
+            mbar_init(&gempty[s], c);
+        }
+        mbar_init(drain, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();            // every CTA's barriers exist before any remote arrive or copy
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    constexpr uint32_t ACC_COL = 256;
+    const int nk = (a.d + TC_BK - 1) / TC_BK;
+
+    if (warp == 0 && lane == 0) {
+        // ================= TMA producer =================
+        tma_prefetch_desc(&a.map_h);
+        tma_prefetch_desc(&a.map_w);
+        tma_prefetch_desc(&a.map_ys);
+        if (DISTILL) tma_prefetch_desc(&a.map_teach);
+        int st = 0;
+        uint32_t ph = 0, issued = 0, last_ph = 0;
+        bool ok = true;
+        auto acquire = [&]() -> uint8_t * {
+            if (!mbar_wait(&empty[st], ph ^ 1, err)) return nullptr;
+            mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+            issued |= 1u << st;
+            last_ph = (last_ph & ~(1u << st)) | (ph << st);
+            return ring + st * C::STAGE_BYTES;
+        };
+        auto advance = [&]() {
+            if (++st == S) { st = 0; ph ^= 1; }
+        };
+        int teach_issued = 0;
+        for (int r = 0; r <= nr && ok; ++r) {
+            const int y = r * c + crank;
+            if (r < nr && y < ny) {                     // own tile of round r (own index m = r)
+                int tok0, voc0;
+                tile_origin(y, tok0, voc0);
+                if (DISTILL) {
+                    const int tb = r & 1;
+                    if (!mbar_wait(&thempty[tb], ((r >> 1) & 1) ^ 1, err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&thfull[tb], 2 * 128 * 64 * 2);
+                    uint8_t *tp = teach + tb * 32768;
+                    tma_load_2d(tp, &a.map_teach, &thfull[tb], voc0, tok0);
+                    tma_load_2d(tp + 16384, &a.map_teach, &thfull[tb], voc0 + 64, tok0);
+                    teach_issued = r + 1;
+                }
+                for (int kb = 0; kb < nk; ++kb) {
+                    uint8_t *sp = acquire();
+                    if (!sp) { ok = false; break; }
+                    tma_load_2d(sp, &a.map_h, &full[st], kb * TC_BK, tok0);
+                    tma_load_2d(sp + 16384, &a.map_w, &full[st], kb * TC_BK, voc0);
+                    advance();
+                }
+                if (!ok) break;
+            }
+            if (r >= 1) {
+                const int y_end = min(r * c, ny);
+                for (int yy = (r - 1) * c; yy < y_end && ok; ++yy) {
+                    int tok0, voc0;
+                    tile_origin(yy, tok0, voc0);
+                    const int row0 = MODE == BWD_ROWS ? voc0 : tok0;
+                    for (int h = 0; h < 2; ++h) {
+                        uint8_t *sp = acquire();
+                        if (!sp) { ok = false; break; }
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sp + q * 8192, &a.map_ys, &full[st], slice0 + q * 64,
+                                        row0 + h * 64);
+                        advance();
+                    }
+                }
+            }
+        }
+        for (int s = 0; s < S; ++s)
+            if (issued & (1u << s)) bw_wait_drain(&full[s], (last_ph >> s) & 1);
+        for (int m = teach_issued - 2; m < teach_issued; ++m)
+            if (DISTILL && m >= 0) bw_wait_drain(&thfull[m & 1], (m >> 1) & 1);
+    } else if (warp == 1 && lane == 0) {
+        // ================= MMA issuer =================
+        constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t ID_ACC = idesc_bf16_f32(128, TC_SLICE, MODE == BWD_COLS ? 1 : 0, 1);
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true, first_acc = true;
+        for (int r = 0; r <= nr && ok; ++r) {
+            const int y = r * c + crank;
+            if (r < nr && y < ny) {
+                const int b = r & 1;
+                if (!mbar_wait(&tempty[b], ((r >> 1) & 1) ^ 1, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_s = tmem + b * 128;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(ring + st * C::STAGE_BYTES);
+#pragma unroll
+                    for (int k = 0; k < TC_BK / 16; ++k)
+                        tc_mma_bf16(d_s, sdesc_sw128(sa + k * 32, 16, 1024),
+                                    sdesc_sw128(sa + 16384 + k * 32, 16, 1024), ID_S, (kb | k) != 0);
+                    tc_commit(&empty[st]);
+                    if (++st == S) { st = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[b]);
+            }
+            if (r >= 1) {
+                const int y_end = min(r * c, ny);
+                for (int yy = (r - 1) * c; yy < y_end && ok; ++yy) {
+                    const int s = yy % R;
+                    if (!mbar_wait(&gfull[s], (yy / R) & 1, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t g_base = smem_u32(gbuf + s * C::G_TILE);
+                    for (int h = 0; h < 2; ++h) {
+                        if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sb = smem_u32(ring + st * C::STAGE_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint64_t adesc;
+                            if (MODE == BWD_ROWS)   // K = vocabulary columns of G
+                                adesc = sdesc_sw128(g_base + h * 16384 + k * 32, 16, 1024);
+                            else                    // K = token rows of G, M = vocabulary (MN-major)
+                                adesc = sdesc_sw128(g_base + h * 8192 + k * 2048, 16384, 1024);
+                            tc_mma_bf16(tmem + ACC_COL, adesc, sdesc_sw128(sb + k * 2048, 8192, 1024),
+                                        ID_ACC, first_acc ? 0u : 1u);
+                            first_acc = false;
+                        }
+                        tc_commit(&empty[st]);
+                        if (++st == S) { st = 0; ph ^= 1; }
+                    }
+                    if (!ok) break;
+                    // slot s is next filled by CTA (yy + R) % c: tell it once this MMA is done
+                    if (yy + R < ny) tc_commit_multicast(&gempty[s], static_cast<uint16_t>(1u << ((yy + R) % c)));
+                }
+            }
+        }
+        if (ok) tc_commit(accfull);
+        tc_commit(drain);
+        bw_wait_drain(drain, 0);
+    } else if (warp >= 2) {
+        // ================= epilogue =================
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;               // token row of the logit tile
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const float L2E = static_cast<float>(LOG2E);
+        const float kT = a.inv_t_l2e;
+        const float4 P0 = DISTILL ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                  : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+        uint8_t *gslot = gbuf + s_own * C::G_TILE;
+        bool ok = true;
+        float4 P = P0;
+        if (MODE == BWD_ROWS) {                       // the token tile is fixed
+            const int t = fixed * 128 + r;
+            if (t < a.n_tok) P = a.tokp[t];
+        }
+        for (int m = 0; m < n_own && ok; ++m) {
+            const int y = m * c + crank;
+            int tok0, voc0;
+            tile_origin(y, tok0, voc0);
+            if (MODE == BWD_COLS) {
+                const int t = tok0 + r;
+                P = t < a.n_tok ? a.tokp[t] : P0;
+            }
+            const int b = m & 1;
+            ok = mbar_wait(&tfull[b], (m >> 1) & 1, err);
+            if (DISTILL && ok) ok = mbar_wait(&thfull[b], (m >> 1) & 1, err);
+            // grad slot free in every CTA: wait for the consumption of the tile R
+            // before this one (none for the first own tile of CTAs below R)
+            const int kslot = m - (crank < R ? 1 : 0);
+            if (ok && kslot >= 0) ok = mbar_wait(&gempty[s_own], kslot & 1, err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const int rel = DISTILL ? 0 : __float_as_int(P.w) - voc0;
+            const uint32_t tbuf = trow + b * 128;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t v[32];
+                tmem_ld32(tbuf + q * 32, v);
+                tmem_ld_wait();
+                float tv[32];
+                if (DISTILL) {
+                    const uint8_t *rowp = teach + b * 32768 + (q >> 1) * 16384 + r * 128;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int phys = (((q & 1) * 4 + c4) ^ (r & 7)) << 4;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(rowp + phys);
+                        tv[c4 * 8 + 0] = bw_lo(w.x); tv[c4 * 8 + 1] = bw_hi(w.x);
+                        tv[c4 * 8 + 2] = bw_lo(w.y); tv[c4 * 8 + 3] = bw_hi(w.y);
+                        tv[c4 * 8 + 4] = bw_lo(w.z); tv[c4 * 8 + 5] = bw_hi(w.z);
+                        tv[c4 * 8 + 6] = bw_lo(w.w); tv[c4 * 8 + 7] = bw_hi(w.w);
+                    }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float g[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float s = __uint_as_float(v[i + u]);
+                        if (!DISTILL) {
+                            float gv = P.y * ex2_approx(fmaf(s, L2E, -P.x));
+                            if (rel == q * 32 + i + u) gv -= P.z;
+                            g[u] = gv;
+                        } else {
+                            const float a2 = s * kT, b2 = tv[i + u] * kT;
+                            const float qv = ex2_approx(a2 - P.x);
+                            if (a.direction == DIR_RKL)
+                                g[u] = P.z * qv * fmaf(a2 - b2, static_cast<float>(LN2), P.w);
+                            else
+                                g[u] = P.z * qv - P.w * ex2_approx(b2 - P.y);
+                        }
+                    }
+                    pk[i >> 1] = pack_bf16x2(g[0], g[1]);
+                }
+                uint8_t *grow = gslot + (q >> 1) * 16384 + r * 128;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int phys = (((q & 1) * 4 + c4) ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(grow + phys) =
+                        make_uint4(pk[c4 * 4 + 0], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+            if (DISTILL) mbar_arrive(&thempty[b]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // this warp's 32 rows: 4 KB in each of the two 64-column blocks
+                mbar_arrive(&gfull[s_own]);
+                const uint32_t src0 = smem_u32(gslot) + quad * 32 * 128;
+                const uint32_t bar_local = smem_u32(&gfull[s_own]);
+                for (int qq = 1; qq < c; ++qq) {
+                    const uint32_t dst = static_cast<uint32_t>((crank + qq) % c);
+                    const uint32_t rbar = mapa_shared(bar_local, dst);
+                    mbar_arrive_expect_tx_remote(rbar, 8192);
+                    bulk_copy_s2cluster(mapa_shared(src0, dst), src0, 4096, rbar);
+                    bulk_copy_s2cluster(mapa_shared(src0 + 16384, dst), src0 + 16384, 4096, rbar);
+                }
+            }
+        }
+        if (ok) {
+            ok = mbar_wait(accfull, 0, err);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const int row = fixed * 128 + r;      // token (ROWS) or vocabulary (COLS) row
+                const int n_rows = MODE == BWD_ROWS ? a.n_tok : a.vocab;
+                float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
+                             static_cast<int64_t>(row) * a.d;
+#pragma unroll 1
+                for (int q = 0; q < TC_SLICE / 32; ++q) {
+                    uint32_t v[32];
+                    tmem_ld32(trow + ACC_COL + q * 32, v);
+                    tmem_ld_wait();
+                    const int col = slice0 + q * 32;
+                    if (row < n_rows && col < a.d) {
+                        if (col + 32 <= a.d) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4 *>(dst + col + i) =
+                                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        } else {
+                            for (int i = 0; i < 32; ++i)
+                                if (col + i < a.d) dst[col + i] = __uint_as_float(v[i]);
+                        }
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    // No CTA leaves while another may still copy into, or arrive on, its shared memory.
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int MODE, bool DISTILL>
+static cudaError_t launch_bwd_one(const BwdArgs &a, int grid, cudaStream_t st)
+{
+    using C = BwdCfg<DISTILL>;
+    auto k = bwd_kernel<MODE, DISTILL>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.n_cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int grid, cudaStream_t st)
+{
+    if (mode == BWD_ROWS)
+        return distill ? launch_bwd_one<BWD_ROWS, true>(a, grid, st) : launch_bwd_one<BWD_ROWS, false>(a, grid, st);
+    return distill ? launch_bwd_one<BWD_COLS, true>(a, grid, st) : launch_bwd_one<BWD_COLS, false>(a, grid, st);
+}
+
+} // namespace lossk

@@ -235,37 +235,36 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
     cudaError_t e = cudaSuccess;
     const float inv_t = static_cast<float>(1.0 / temperature);
     if (dtype == LOSSK_BF16) {
+        const BwdGeom g = bwd_geometry(d, distill);
         for (int pass = 0; pass < 2; ++pass) {
             float *dst = pass == 0 ? d_hidden : d_weight;
             if (!dst) continue;
             const bool rows = pass == 0;
-            TcArgs a;
+            BwdArgs a;
             std::memset(&a, 0, sizeof(a));
-            const void *X = rows ? H : W, *Y = rows ? W : H;
-            const int64_t nx = rows ? n : V, ny = rows ? V : n;
-            if (!make_map(&a.map_x, X, d, nx, 64, TC_BM) || !make_map(&a.map_y, Y, d, ny, 64, TC_BN_ACC) ||
-                !make_map(&a.map_ys, Y, d, ny, 64, 64))
+            if (!make_map(&a.map_h, H, d, n, 64, 128) || !make_map(&a.map_w, W, d, V, 64, 128) ||
+                !make_map(&a.map_ys, rows ? W : H, d, rows ? V : n, 64, 64))
                 return LOSSK_DEVICE_ERROR;
-            if (distill && !make_map(&a.map_teach, teacher, V, n, 64, TC_BM)) return LOSSK_DEVICE_ERROR;
-            a.n_x = static_cast<int>(nx);
-            a.n_y = static_cast<int>(ny);
-            a.d = static_cast<int>(d);
+            if (distill && !make_map(&a.map_teach, teacher, V, n, 64, 128)) return LOSSK_DEVICE_ERROR;
             a.n_tok = static_cast<int>(n);
             a.vocab = static_cast<int>(V);
-            a.n_xt = static_cast<int>(cdiv(nx, TC_BM));
-            a.n_yt = static_cast<int>(cdiv(ny, TC_BN_ACC));
-            a.n_slices = static_cast<int>(cdiv(d, TC_SLICE));
+            a.d = static_cast<int>(d);
+            a.n_fixed = static_cast<int>(cdiv(rows ? n : V, 128));
+            a.n_loop = static_cast<int>(cdiv(rows ? V : n, 128));
             a.n_split = rows ? static_cast<int>(L.nsplit) : 1;
+            a.n_cl = g.n_cl;
+            a.n_dg = g.n_dg;
+            a.g_slots = g.g_slots;
             a.direction = direction;
             a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
             a.tokp = w.tokp();
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
             a.out_split_stride = n * d;
             a.err = &w.hdr()->err;
-            const int grid = a.n_xt * a.n_slices * a.n_split;
+            const int grid = a.n_fixed * a.n_split * a.n_dg * a.n_cl;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
-                e = launch_tc(rows ? TC_ROWS : TC_COLS, distill, a, grid, st);
+                e = launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, a, grid, st);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {
@@ -329,6 +328,19 @@ bool scalars_ok(double wz, double gs) { return is_finite(wz) && wz >= 0.0 && is_
 
 // ===========================================================================
 namespace lossk {
+
+BwdGeom bwd_geometry(int64_t d, bool distill)
+{
+    const int64_t ns = cdiv(d, TC_SLICE);               // 256-column slices
+    BwdGeom g;
+    g.n_dg = static_cast<int>(cdiv(ns, 8));
+    g.n_cl = static_cast<int>(cdiv(ns, g.n_dg));
+    const int r_max = distill ? 2 : 4;
+    g.g_slots = 1;
+    for (int r = r_max; r >= 1; --r)
+        if (g.n_cl % r == 0) { g.g_slots = r; break; }
+    return g;
+}
 
 int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
 {

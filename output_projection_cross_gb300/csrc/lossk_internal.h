@@ -86,6 +86,36 @@ struct TcArgs {
     int *err;
 };
 
+// ---- backward (cluster-shared grad tiles) kernel arguments -------------------
+enum BwdMode : int { BWD_ROWS = 1, BWD_COLS = 2 };
+
+struct BwdArgs {
+    CUtensorMap map_h;     // hidden [n_tok][d], box {64, 128}
+    CUtensorMap map_w;     // weight [vocab][d], box {64, 128}
+    CUtensorMap map_ys;    // the loop tensor (weight for d_hidden, hidden for d_weight), box {64, 64}
+    CUtensorMap map_teach; // teacher logits [n_tok][vocab], box {64, 128}
+    int n_tok, vocab, d;
+    int n_fixed;           // fixed tiles: token tiles (d_hidden) or vocabulary tiles (d_weight)
+    int n_loop;            // loop tiles: vocabulary tiles (d_hidden) or token tiles (d_weight)
+    int n_split;           // splits of the loop range (d_hidden)
+    int n_cl;              // CTAs per cluster = 256-column d-slices per group
+    int n_dg;              // d-groups (clusters per fixed tile and split)
+    int g_slots;           // grad slots in use (divides n_cl)
+    int direction;
+    float inv_t_l2e;
+    const float4 *tokp;
+    float *out;
+    int64_t out_split_stride;
+    int *err;
+};
+
+// Cluster geometry of the backward for a d_model: slices of 256 columns, at
+// most 8 CTAs per cluster, d-groups beyond that.
+struct BwdGeom {
+    int n_cl, n_dg, g_slots;
+};
+BwdGeom bwd_geometry(int64_t d, bool distill);
+
 // Kernel kinds, for the launch counter and the optional per-kernel timing.
 enum KernelKind : int {
     KK_VALIDATE = 0,
@@ -108,6 +138,7 @@ enum KernelKind : int {
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);
 cudaError_t launch_tc(int mode, bool distill, const TcArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
                       float inv_t, const int64_t *targets, const float4 *tokp, float *part,

@@ -80,8 +80,11 @@ SMALL = [  # (n, d, V): several tiles and ragged tails in every dimension
     (1, 64, 8),
     (130, 72, 300),
     (300, 200, 1000),
-    (257, 520, 2000),
+    (257, 520, 2000),     # 3 d-slices: a cluster of 3
     (128, 256, 512),
+    (300, 768, 1000),     # cluster of 3, fewer token tiles than CTAs in the d_weight pass
+    (200, 1280, 1500),    # cluster of 5 (one grad slot)
+    (130, 2304, 600),     # 9 slices: two d-groups of 5
 ]
 
 
