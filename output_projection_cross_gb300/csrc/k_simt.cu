@@ -322,24 +322,39 @@ template <> struct Vec<uint16_t> { static constexpr int N = 8; };
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
+// 16-byte loads of a logit row.  `keep` leaves the line in L2 (the row is read
+// again for its gradient); otherwise the load streams past L2.
 template <typename T>
-__device__ __forceinline__ void load_vec(const T *p, float *f);
+__device__ __forceinline__ void load_vec(const T *p, float *f, bool keep);
 template <>
-__device__ __forceinline__ void load_vec<float>(const float *p, float *f)
+__device__ __forceinline__ void load_vec<float>(const float *p, float *f, bool keep)
 {
-    const float4 v = __ldcs(reinterpret_cast<const float4 *>(p));
+    const float4 *q = reinterpret_cast<const float4 *>(p);
+    const float4 v = keep ? __ldg(q) : __ldcs(q);
     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
 }
 template <>
-__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *p, float *f)
+__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *p, float *f, bool keep)
 {
-    const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    const uint4 v = keep ? __ldg(q) : __ldcs(q);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         f[2 * i] = __uint_as_float(w[i] << 16);
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
+}
+
+// 16-byte streaming store of NV gradient values.
+__device__ __forceinline__ void store_vec(float *p, const float *g)
+{
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(g[0], g[1], g[2], g[3]));
+}
+__device__ __forceinline__ void store_vec(uint16_t *p, const float *g)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                                                    pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7])));
 }
 
 __device__ __forceinline__ void online_add(float &m, float &z, float x2)
@@ -381,7 +396,7 @@ __global__ void __launch_bounds__(512) from_logits_kernel(const T *__restrict__ 
         const int64_t nvec = V / NV;
         for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
             float f[NV];
-            load_vec<T>(x + i * NV, f);
+            load_vec<T>(x + i * NV, f, grad != nullptr);
 #pragma unroll
             for (int u = 0; u < NV; ++u) online_add(m, z, f[u] * L2E);
         }
@@ -428,6 +443,20 @@ __global__ void __launch_bounds__(512) from_logits_kernel(const T *__restrict__ 
     const float c = on ? static_cast<float>(alpha * (1.0 + 2.0 * wz * lse2 * LN2)) : 0.f;
     const int64_t y = targets[t];
     T *g = grad + t * V;
+    if (vec_ok) {
+        const int64_t nvec = V / NV;
+        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float f[NV], gv[NV];
+            load_vec<T>(x + i * NV, f, false);
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                gv[u] = c * ex2_approx(fmaf(f[u], L2E, -lse2));
+                if (i * NV + u == y) gv[u] -= at;
+            }
+            store_vec(g + i * NV, gv);
+        }
+        return;
+    }
     for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
         float gv = c * ex2_approx(fmaf(to_f(x[i]), L2E, -lse2));
         if (i == y) gv -= at;

@@ -188,9 +188,11 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
     const WsLayout &L = w.L;
     cudaError_t e;
     if (dtype == LOSSK_BF16) {
+        // CTA pairs: 256 tokens x 256 vocabulary per MMA, each CTA loading its
+        // own 128 token rows and half (128 rows) of each vocabulary tile.
         TcArgs a;
         std::memset(&a, 0, sizeof(a));
-        if (!make_map(&a.map_x, H, d, n, 64, TC_BM) || !make_map(&a.map_y, W, d, V, 64, TC_BN_FWD))
+        if (!make_map(&a.map_x, H, d, n, 64, TC_BM) || !make_map(&a.map_y, W, d, V, 64, 128))
             return LOSSK_DEVICE_ERROR;
         a.n_x = static_cast<int>(n);
         a.n_y = static_cast<int>(V);
@@ -199,16 +201,16 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
         a.vocab = static_cast<int>(V);
         a.n_xt = static_cast<int>(cdiv(n, TC_BM));
         a.n_yt = static_cast<int>(L.n_ct);
-        a.n_items = a.n_xt * a.n_yt;
+        a.n_items = static_cast<int>(cdiv(a.n_xt, 2)) * a.n_yt;
         a.targets = targets;
         a.part = w.part();
         a.tgt = w.tgt();
         a.part_stride = L.n_pad;
         a.part_plane = L.n_ct * L.n_pad;
         a.err = &w.hdr()->err;
-        const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
         Launch k(KK_TC_STATS, st);
-        e = launch_tc(TC_STATS, false, a, grid, st);
+        e = launch_fwd2(a, 2 * pairs, st);
     } else {
         Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, false, H, W, nullptr, static_cast<int>(n), static_cast<int>(V),

@@ -139,6 +139,7 @@ cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t
                             WsHeader *hdr, cudaStream_t st);
 cudaError_t launch_tc(int mode, bool distill, const TcArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_fwd2(const TcArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
                       float inv_t, const int64_t *targets, const float4 *tokp, float *part,
