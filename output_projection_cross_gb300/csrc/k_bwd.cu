@@ -30,6 +30,10 @@ namespace lossk {
 template <bool DISTILL> struct BwdCfg {
     static constexpr int BN = 128;                  // loop-tile rows per logit tile
     static constexpr int STAGE_BYTES = 32768;       // X+Y k-slices, or 64 rows x 256-column slice
+    // One grad slot per CTA of a 4-CTA cluster: with fewer slots, the grad tile
+    // of a loop tile waits for the accumulate of another tile of the same
+    // round in every CTA, which serialises each round.  That leaves room for
+    // three 32 KB ring stages.
     static constexpr int STAGES = 3;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int G_TILE = 32768;            // 128 x 128 bf16
@@ -284,15 +288,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int b = m & 1;
             ok = mbar_wait(&tfull[b], (m >> 1) & 1, err);
             if (DISTILL && ok) ok = mbar_wait(&thfull[b], (m >> 1) & 1, err);
-            // grad slot free in every CTA: wait for the consumption of the tile R
-            // before this one (none for the first own tile of CTAs below R)
-            const int kslot = m - (crank < R ? 1 : 0);
-            if (ok && kslot >= 0) ok = mbar_wait(&gempty[s_own], kslot & 1, err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int rel = DISTILL ? 0 : __float_as_int(P.w) - voc0;
             const uint32_t tbuf = trow + b * 128;
-#pragma unroll 1
+            uint32_t pk[64];
+#pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t v[32];
                 tmem_ld32(tbuf + q * 32, v);
@@ -310,7 +311,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                         tv[c4 * 8 + 6] = bw_lo(w.w); tv[c4 * 8 + 7] = bw_hi(w.w);
                     }
                 }
-                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float g[2];
@@ -330,19 +330,29 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                                 g[u] = P.z * qv - P.w * ex2_approx(b2 - P.y);
                         }
                     }
-                    pk[i >> 1] = pack_bf16x2(g[0], g[1]);
+                    pk[q * 16 + (i >> 1)] = pack_bf16x2(g[0], g[1]);
                 }
+            }
+            // the tile is in registers: give the TMEM buffer and teacher tile back
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+            if (DISTILL) mbar_arrive(&thempty[b]);
+            // grad slot free in every CTA: wait for the consumption of the tile R
+            // before this one (none for the first own tile of CTAs below R)
+            const int kslot = m - (crank < R ? 1 : 0);
+            if (kslot >= 0) ok = mbar_wait(&gempty[s_own], kslot & 1, err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
                 uint8_t *grow = gslot + (q >> 1) * 16384 + r * 128;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const int phys = (((q & 1) * 4 + c4) ^ (r & 7)) << 4;
                     *reinterpret_cast<uint4 *>(grow + phys) =
-                        make_uint4(pk[c4 * 4 + 0], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                        make_uint4(pk[q * 16 + c4 * 4 + 0], pk[q * 16 + c4 * 4 + 1],
+                                   pk[q * 16 + c4 * 4 + 2], pk[q * 16 + c4 * 4 + 3]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[b]);
-            if (DISTILL) mbar_arrive(&thempty[b]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {

@@ -346,14 +346,25 @@ BwdGeom bwd_geometry(int64_t d, bool distill)
 
 int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
 {
+    // The d_hidden pass has one cluster per (token tile, d-group, vocabulary
+    // split).  A 152-SM GB300 holds 36 four-CTA clusters at a time, so aim for
+    // 144 clusters (four full waves) on the tensor-core path, and for about
+    // two CTAs per SM on the FFMA path.  Shape-only, so results never depend
+    // on the device.
     const bool tc = dtype == LOSSK_BF16;
     const int64_t bm = tc ? TC_BM : FP_BM, bn = tc ? TC_BN_ACC : FP_BN, sl = tc ? TC_SLICE : FP_SLICE;
-    const int64_t base = cdiv(n, bm) * cdiv(d, sl);
     const int64_t n_yt = cdiv(V, bn);
-    const int64_t target = 296;   // about two CTAs per SM on a 148-152 SM part
-    if (base >= target) return 1;
-    int64_t s = cdiv(target, base);
     const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
+    int64_t s;
+    if (tc) {
+        const int64_t ns = cdiv(d, sl);
+        const int64_t clusters = cdiv(n, bm) * cdiv(ns, 8);     // token tiles x d-groups
+        s = clusters >= 144 ? 1 : 144 / clusters;
+    } else {
+        const int64_t base = cdiv(n, bm) * cdiv(d, sl);
+        s = base >= 296 ? 1 : cdiv(296, base);
+    }
+    if (s < 1) s = 1;
     return s < cap ? s : cap;
 }
 

@@ -60,6 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Cluster-scope acquire: for barriers that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Error codes a kernel writes into the workspace's error word.
 enum : int { ERR_NONE = 0, ERR_TIMEOUT = 1 };
 
@@ -76,6 +90,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(err) != ERR_NONE) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(err, ERR_NONE, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// As mbar_wait, with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *err,
+                                                  uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*reinterpret_cast<volatile int *>(err) != ERR_NONE) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(err, ERR_NONE, ERR_TIMEOUT);
