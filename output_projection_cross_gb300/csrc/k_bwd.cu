@@ -37,14 +37,13 @@ template <bool DISTILL> struct BwdCfg {
     static constexpr int STAGES = 3;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int G_TILE = 32768;            // 128 x 128 bf16
-    static constexpr int R_MAX = DISTILL ? 2 : 4;   // grad slots
+    static constexpr int R_MAX = 4;                 // grad slots
     static constexpr int G_BYTES = R_MAX * G_TILE;
-    // Two teacher buffers: with one, the producer would wait for epilogue r
-    // before issuing tile r+1's logit stages, while epilogue r can wait (for
-    // its grad slot) on MMAs issued after those stages.
-    static constexpr int T_BYTES = DISTILL ? 2 * 32768 : 0;
-    static constexpr int NBARS = 2 * STAGES + 2 + 2 + 1 + 4 + 2 * R_MAX + 1;
-    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + G_BYTES + T_BYTES + NBARS * 8 + 16;
+    // Teacher logits are read by the epilogue straight from global memory (one
+    // contiguous 256-byte row segment per thread and tile), so they take no
+    // shared memory.
+    static constexpr int NBARS = 2 * STAGES + 2 + 2 + 1 + 2 * R_MAX + 1;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + G_BYTES + NBARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB per-CTA shared memory limit");
 };
 
@@ -68,16 +67,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *ring = smem;
     uint8_t *gbuf = ring + C::RING_BYTES;
-    uint8_t *teach = gbuf + C::G_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(teach + C::T_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbuf + C::G_BYTES);
     uint64_t *full = bars;                 // [S]
     uint64_t *empty = full + S;            // [S]
     uint64_t *tfull = empty + S;           // [2] logit tile ready in TMEM buffer
     uint64_t *tempty = tfull + 2;          // [2] epilogue done with TMEM buffer
     uint64_t *accfull = tempty + 2;
-    uint64_t *thfull = accfull + 1;        // [2] teacher tile landed
-    uint64_t *thempty = thfull + 2;        // [2] teacher tile consumed
-    uint64_t *gfull = thempty + 2;         // [R_MAX] grad slot filled (4 warp arrivals + bytes)
+    uint64_t *gfull = accfull + 1;         // [R_MAX] grad slot filled (4 warp arrivals + bytes)
     uint64_t *gempty = gfull + C::R_MAX;   // [R_MAX] grad slot consumed by every CTA (c arrivals)
     uint64_t *drain = gempty + C::R_MAX;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -115,10 +111,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             mbar_init(&tempty[b], 128);
         }
         mbar_init(accfull, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&thfull[b], 1);
-            mbar_init(&thempty[b], 128);
-        }
         for (int s = 0; s < C::R_MAX; ++s) {
             mbar_init(&gfull[s], 4);
             mbar_init(&gempty[s], c);
@@ -140,7 +132,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         tma_prefetch_desc(&a.map_h);
         tma_prefetch_desc(&a.map_w);
         tma_prefetch_desc(&a.map_ys);
-        if (DISTILL) tma_prefetch_desc(&a.map_teach);
         int st = 0;
         uint32_t ph = 0, issued = 0, last_ph = 0;
         bool ok = true;
@@ -154,21 +145,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         auto advance = [&]() {
             if (++st == S) { st = 0; ph ^= 1; }
         };
-        int teach_issued = 0;
         for (int r = 0; r <= nr && ok; ++r) {
             const int y = r * c + crank;
             if (r < nr && y < ny) {                     // own tile of round r (own index m = r)
                 int tok0, voc0;
                 tile_origin(y, tok0, voc0);
-                if (DISTILL) {
-                    const int tb = r & 1;
-                    if (!mbar_wait(&thempty[tb], ((r >> 1) & 1) ^ 1, err)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&thfull[tb], 2 * 128 * 64 * 2);
-                    uint8_t *tp = teach + tb * 32768;
-                    tma_load_2d(tp, &a.map_teach, &thfull[tb], voc0, tok0);
-                    tma_load_2d(tp + 16384, &a.map_teach, &thfull[tb], voc0 + 64, tok0);
-                    teach_issued = r + 1;
-                }
                 for (int kb = 0; kb < nk; ++kb) {
                     uint8_t *sp = acquire();
                     if (!sp) { ok = false; break; }
@@ -197,8 +178,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         for (int s = 0; s < S; ++s)
             if (issued & (1u << s)) bw_wait_drain(&full[s], (last_ph >> s) & 1);
-        for (int m = teach_issued - 2; m < teach_issued; ++m)
-            if (DISTILL && m >= 0) bw_wait_drain(&thfull[m & 1], (m >> 1) & 1);
     } else if (warp == 1 && lane == 0) {
         // ================= MMA issuer =================
         constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);
@@ -287,7 +266,22 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             }
             const int b = m & 1;
             ok = mbar_wait(&tfull[b], (m >> 1) & 1, err);
-            if (DISTILL && ok) ok = mbar_wait(&thfull[b], (m >> 1) & 1, err);
+            // Teacher row segment teacher[token][voc0 .. voc0+127] of this thread:
+            // 16-byte loads, each chunk fetched one chunk ahead of its use.
+            const int tok = tok0 + r;
+            const bool trow_ok = DISTILL && tok < a.n_tok;
+            const uint4 *tsrc = DISTILL ? reinterpret_cast<const uint4 *>(
+                                              a.teacher + static_cast<int64_t>(trow_ok ? tok : 0) * a.vocab + voc0)
+                                        : nullptr;
+            const int tvalid = min(128, a.vocab - voc0);       // columns of this tile inside the vocabulary
+            auto tload = [&](int q, uint4 (&w)[4]) {
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    w[c4] = (trow_ok && q * 32 + c4 * 8 < tvalid) ? __ldg(tsrc + q * 4 + c4)
+                                                                   : make_uint4(0, 0, 0, 0);
+            };
+            uint4 tw[4] = {};
+            if (DISTILL) tload(0, tw);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int rel = DISTILL ? 0 : __float_as_int(P.w) - voc0;
@@ -297,20 +291,18 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             for (int q = 0; q < 4; ++q) {
                 uint32_t v[32];
                 tmem_ld32(tbuf + q * 32, v);
-                tmem_ld_wait();
                 float tv[32];
                 if (DISTILL) {
-                    const uint8_t *rowp = teach + b * 32768 + (q >> 1) * 16384 + r * 128;
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
-                        const int phys = (((q & 1) * 4 + c4) ^ (r & 7)) << 4;
-                        const uint4 w = *reinterpret_cast<const uint4 *>(rowp + phys);
-                        tv[c4 * 8 + 0] = bw_lo(w.x); tv[c4 * 8 + 1] = bw_hi(w.x);
-                        tv[c4 * 8 + 2] = bw_lo(w.y); tv[c4 * 8 + 3] = bw_hi(w.y);
-                        tv[c4 * 8 + 4] = bw_lo(w.z); tv[c4 * 8 + 5] = bw_hi(w.z);
-                        tv[c4 * 8 + 6] = bw_lo(w.w); tv[c4 * 8 + 7] = bw_hi(w.w);
+                        tv[c4 * 8 + 0] = bw_lo(tw[c4].x); tv[c4 * 8 + 1] = bw_hi(tw[c4].x);
+                        tv[c4 * 8 + 2] = bw_lo(tw[c4].y); tv[c4 * 8 + 3] = bw_hi(tw[c4].y);
+                        tv[c4 * 8 + 4] = bw_lo(tw[c4].z); tv[c4 * 8 + 5] = bw_hi(tw[c4].z);
+                        tv[c4 * 8 + 6] = bw_lo(tw[c4].w); tv[c4 * 8 + 7] = bw_hi(tw[c4].w);
                     }
+                    if (q < 3) tload(q + 1, tw);
                 }
+                tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float g[2];
@@ -333,10 +325,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     pk[q * 16 + (i >> 1)] = pack_bf16x2(g[0], g[1]);
                 }
             }
-            // the tile is in registers: give the TMEM buffer and teacher tile back
+            // the tile is in registers: give the TMEM buffer back
             tc_fence_before();
             mbar_arrive(&tempty[b]);
-            if (DISTILL) mbar_arrive(&thempty[b]);
             // grad slot free in every CTA: wait for the consumption of the tile R
             // before this one (none for the first own tile of CTAs below R)
             const int kslot = m - (crank < R ? 1 : 0);

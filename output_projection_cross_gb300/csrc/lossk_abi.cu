@@ -247,7 +247,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             if (!make_map(&a.map_h, H, d, n, 64, 128) || !make_map(&a.map_w, W, d, V, 64, 128) ||
                 !make_map(&a.map_ys, rows ? W : H, d, rows ? V : n, 64, 64))
                 return LOSSK_DEVICE_ERROR;
-            if (distill && !make_map(&a.map_teach, teacher, V, n, 64, 128)) return LOSSK_DEVICE_ERROR;
+            a.teacher = distill ? static_cast<const uint16_t *>(teacher) : nullptr;
             a.n_tok = static_cast<int>(n);
             a.vocab = static_cast<int>(V);
             a.d = static_cast<int>(d);
@@ -337,7 +337,8 @@ BwdGeom bwd_geometry(int64_t d, bool distill)
     BwdGeom g;
     g.n_dg = static_cast<int>(cdiv(ns, 8));
     g.n_cl = static_cast<int>(cdiv(ns, g.n_dg));
-    const int r_max = distill ? 2 : 4;
+    const int r_max = 4;
+    (void)distill;
     g.g_slots = 1;
     for (int r = r_max; r >= 1; --r)
         if (g.n_cl % r == 0) { g.g_slots = r; break; }

@@ -93,7 +93,7 @@ struct BwdArgs {
     CUtensorMap map_h;     // hidden [n_tok][d], box {64, 128}
     CUtensorMap map_w;     // weight [vocab][d], box {64, 128}
     CUtensorMap map_ys;    // the loop tensor (weight for d_hidden, hidden for d_weight), box {64, 64}
-    CUtensorMap map_teach; // teacher logits [n_tok][vocab], box {64, 128}
+    const uint16_t *teacher; // teacher logits [n_tok][vocab] (bf16), read by the epilogue
     int n_tok, vocab, d;
     int n_fixed;           // fixed tiles: token tiles (d_hidden) or vocabulary tiles (d_weight)
     int n_loop;            // loop tiles: vocabulary tiles (d_hidden) or token tiles (d_weight)
