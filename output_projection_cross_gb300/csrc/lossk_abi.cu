@@ -263,10 +263,10 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
             a.out_split_stride = n * d;
             a.err = &w.hdr()->err;
-            const int grid = a.n_fixed * a.n_split * a.n_dg * a.n_cl;
+            const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
-                e = launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, a, grid, st);
+                e = launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, a, n_units, st);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {

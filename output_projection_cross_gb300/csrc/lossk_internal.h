@@ -138,7 +138,8 @@ enum KernelKind : int {
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);
 cudaError_t launch_tc(int mode, bool distill, const TcArgs &a, int grid, cudaStream_t st);
-cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int grid, cudaStream_t st);
+// Persistent clusters: at most as many as fit at once, walking `n_units` units.
+cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int n_units, cudaStream_t st);
 cudaError_t launch_fwd2(const TcArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,

@@ -112,6 +112,41 @@ def test_ce_small_shapes(L, shape, dtype):
     assert rel_l2(_np(out["d_weight"]), dW) <= gt
 
 
+@pytest.mark.parametrize("shape", [(700, 1280, 12000), (300, 1024, 32000)])
+def test_ce_persistent_clusters(L, shape):
+    """More work units than co-resident clusters, so each backward cluster walks
+    several units (slot hand-over across units, accumulator reuse): a cluster of
+    5 with one grad slot and ragged splits, and a cluster of 4."""
+    n, d, V = shape
+    x = _inputs("ce_512x1024x32000", seed=31, n_tok=n, d_model=d, vocab=V)
+    mask = li.mask(5, n, 0.1)
+    wz, gs = 1e-3, 1.5
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=_dev(mask, ""), chunk=64, z_weight=wz, grad_scale=gs)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, chunk=64, z_weight=wz)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz, grad_scale=gs)
+    close_loss(_np(out["ce"]), ref["ce"], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= BF16_GRAD
+    assert rel_l2(_np(out["d_weight"]), dW) <= BF16_GRAD
+
+
+@pytest.mark.parametrize("direction", ["fkl", "rkl"])
+def test_distill_persistent_clusters(L, direction):
+    n, d, V = 600, 1024, 8192
+    x = _inputs("distill_z_4096x2048", seed=32, n_tok=n, d_model=d, vocab=V)
+    mask = li.mask(6, n, 0.1)
+    out = L.lossk_distill_fwd_bwd(_dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"),
+                                  _dev(x["teacher"], "bf16"), direction, temperature=2.0,
+                                  loss_mask=_dev(mask, ""), z_weight=1e-3)
+    torch.cuda.synchronize()
+    r = oracle.distill(x["hidden"], x["weight"], x["teacher"], direction, temperature=2.0,
+                       mask=mask, z_weight=1e-3)
+    close_loss(_np(out["per_token"]), r["per_token"], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), r["dH"]) <= BF16_GRAD
+    assert rel_l2(_np(out["d_weight"]), r["dW"]) <= BF16_GRAD
+
+
 def test_ce_fwd_and_bwd_entry_points_agree_with_fused(L):
     n, d, V = 200, 128, 1500
     x = _inputs("ce_512x1024x32000", seed=5, n_tok=n, d_model=d, vocab=V)
