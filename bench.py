@@ -159,7 +159,7 @@ class Clocks:
 
 def kernel_src_sha():
     h = hashlib.sha256()
-    for f in ("k_tc.cu", "ptx.cuh", "lossk_internal.h"):
+    for f in ("k_fwd2.cu", "k_bwd.cu", "k_tc.cu", "lossk_abi.cu", "ptx.cuh", "lossk_internal.h"):
         h.update(open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
