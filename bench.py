@@ -35,11 +35,12 @@ METRIC = "fused linear-CE fwd+bwd tokens/s at Qwen3 shape; % of bf16 tensor peak
 WORKLOAD = "qwen3_0p6b_head"
 # Which kernels' work counts as algorithmic (FLOPs per launch, in units of
 # n*d*V multiply-adds x 2): statistics = one logit contraction; each backward
-# pass = one logit contraction (recompute once) + its gradient contraction.
-ALGO_FLOPS_NDV = {"tc_stats": 2.0, "tc_rows": 4.0, "tc_cols": 4.0,
+# pass = one logit contraction (recompute once) + its gradient contraction; the
+# fused forward + d_hidden pass = one logit contraction + the d_hidden one.
+ALGO_FLOPS_NDV = {"tc_stats": 2.0, "tc_rows": 4.0, "tc_cols": 4.0, "tc_fused": 4.0,
                   "fp_stats": 2.0, "fp_rows": 4.0, "fp_cols": 4.0}
 HBM_KERNELS = {"from_logits", "validate", "merge_ce", "merge_distill", "reduce", "tokp_ce",
-               "sum_splits"}
+               "sum_splits", "tgt_logit", "merge_fused", "combine_dh"}
 
 
 def peaks():

@@ -28,6 +28,19 @@
 // logits.  An "emptied" barrier keeps the next unit's first accumulate from
 // overwriting the accumulator before the epilogue has stored it.
 //
+// BWD_FUSED is the d_hidden schedule run as the forward pass too, before any
+// log-sum-exp is known.  Its grad tile is the unnormalised
+//   G'[t][v] = 2^(s[t][v] log2e - r_t),   r_t = s[t][y_t] log2e + 64,
+// a per-token reference shift fixed before the pass (the target logit lies at
+// or below the row maximum, so the largest term of a row is at least 2^-64 and
+// nothing that matters underflows).  Each CTA also sums G' over the valid
+// vocabulary columns of its own loop tiles (per tile in fp32, across tiles in
+// fp64) and writes that sum per (split, CTA, token).  With Z_t the sum of
+// those partials, p = G'/Z_t, lse_t = (r_t + log2 Z_t) ln 2 and
+//   d_hidden_t = a_t (1 + 2 w_z lse_t) D_t / Z_t - a_t W[y_t],
+// which a later kernel applies; that kernel, not this one, also detects a row
+// whose shifted terms left the safe range.
+//
 // Roles per CTA (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
 // issuer, warps 2-5 epilogue (one token row per thread).  TMEM: two 128-column
 // logit buffers and the 256-column accumulator.  Every wait is bounded.
@@ -95,6 +108,9 @@ template <int MODE, bool DISTILL>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
 {
     using C = BwdCfg<DISTILL>;
+    constexpr bool FUSED = MODE == BWD_FUSED;
+    constexpr bool ROWS = MODE != BWD_COLS;     // the token tile is the fixed one
+    static_assert(!(FUSED && DISTILL), "the fused pass is label cross-entropy only");
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -122,7 +138,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     const int s_own = crank % R;                           // this CTA's grad slot
     auto tile_origin = [&](const BwdUnit &w, int y, int &tok0, int &voc0) {
         const int t = w.yt_begin + y;
-        if (MODE == BWD_ROWS) { tok0 = w.fixed * 128; voc0 = t * 128; }
+        if (ROWS) { tok0 = w.fixed * 128; voc0 = t * 128; }
         else { voc0 = w.fixed * 128; tok0 = t * 128; }
     };
     // Step i of the schedule issues round i's own logit tile and the
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 for (int yy = prev.r * c; yy < y_end && ok; ++yy) {
                     int tok0, voc0;
                     tile_origin(prev.w, yy, tok0, voc0);
-                    const int row0 = MODE == BWD_ROWS ? voc0 : tok0;
+                    const int row0 = ROWS ? voc0 : tok0;
                     for (int h = 0; h < 2; ++h) {
                         uint8_t *sp = acquire();
                         if (!sp) { ok = false; break; }
@@ -295,7 +311,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             uint64_t adesc;
-                            if (MODE == BWD_ROWS)   // K = vocabulary columns of G
+                            if (ROWS)               // K = vocabulary columns of G
                                 adesc = sdesc_sw128(g_base + h * 16384 + k * 32, 16, 1024);
                             else                    // K = token rows of G, M = vocabulary (MN-major)
                                 adesc = sdesc_sw128(g_base + h * 8192 + k * 2048, 16384, 1024);
@@ -344,7 +360,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const BwdUnit w = bwd_unit(a, u);
             const int n_own = crank < w.ny ? (w.ny - crank + c - 1) / c : 0;
             float4 P = P0;
-            if (MODE == BWD_ROWS) {                   // the token tile is fixed
+            double zsum = 0.0;                        // fused pass: this CTA's sum of G' for its row
+            if (ROWS) {                               // the token tile is fixed
                 const int t = w.fixed * 128 + r;
                 if (t < a.n_tok) P = a.tokp[t];
             }
@@ -379,6 +396,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 const int rel = DISTILL ? 0 : __float_as_int(P.w) - voc0;
                 const uint32_t tbuf = trow + b * 128;
                 uint32_t pk[64];
+                float zt = 0.f;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t v[32];
@@ -401,7 +419,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 #pragma unroll
                         for (int uu = 0; uu < 2; ++uu) {
                             const float s = __uint_as_float(v[i + uu]);
-                            if (!DISTILL) {
+                            if (FUSED) {
+                                const float gv = ex2_approx(fmaf(s, L2E, -P.x));
+                                g[uu] = gv;
+                                zt += (q * 32 + i + uu < tvalid) ? gv : 0.f;
+                            } else if (!DISTILL) {
                                 float gv = P.y * ex2_approx(fmaf(s, L2E, -P.x));
                                 if (rel == q * 32 + i + uu) gv -= P.z;
                                 g[uu] = gv;
@@ -417,6 +439,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                         pk[q * 16 + (i >> 1)] = pack_bf16x2(g[0], g[1]);
                     }
                 }
+                if (FUSED) zsum += static_cast<double>(zt);
                 // the tile is in registers: give the TMEM buffer back
                 tc_fence_before();
                 mbar_arrive(&tempty[b]);
@@ -457,13 +480,21 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 }
             }
             if (!ok) break;
+            if (FUSED && w.dg == 0) {
+                // every d-group recomputes the same logits; the first one reports the sums
+                const int t = w.fixed * 128 + r;
+                const int split = u / (a.n_fixed * a.n_dg);
+                if (t < a.n_tok)
+                    a.zpart[(static_cast<int64_t>(split) * c + crank) * a.zpart_stride + t] =
+                        static_cast<float>(zsum);
+            }
             // the unit's accumulator: store this CTA's rows of its d-slice
             ok = mbar_wait(accfull, k & 1, err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int slice0 = (w.dg * c + crank) * TC_SLICE;
             const int row = w.fixed * 128 + r;        // token (ROWS) or vocabulary (COLS) row
-            const int n_rows = MODE == BWD_ROWS ? a.n_tok : a.vocab;
+            const int n_rows = ROWS ? a.n_tok : a.vocab;
             const int split = u / (a.n_fixed * a.n_dg);
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(row) * a.d;
@@ -535,6 +566,7 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
 
 cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int n_units, cudaStream_t st)
 {
+    if (mode == BWD_FUSED) return launch_bwd_one<BWD_FUSED, false>(a, n_units, st);
     if (mode == BWD_ROWS)
         return distill ? launch_bwd_one<BWD_ROWS, true>(a, n_units, st) : launch_bwd_one<BWD_ROWS, false>(a, n_units, st);
     return distill ? launch_bwd_one<BWD_COLS, true>(a, n_units, st) : launch_bwd_one<BWD_COLS, false>(a, n_units, st);

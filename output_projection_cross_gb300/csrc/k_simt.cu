@@ -10,6 +10,13 @@
 //   reduce         fixed-shape double-precision tree over tokens -> the means
 //   tokp_ce        per-token backward parameters of the label loss
 //   sum_splits     d_hidden partials of the vocabulary splits, in split order
+//   tgt_logit      fused path: the target logit s[t][y_t] per token and the
+//                  reference shift r_t the fused pass exponentiates against
+//   merge_fused    fused path: per token, the pass's sums of 2^(s log2e - r_t)
+//                  -> lse, ce, z and the backward parameters; flags a row
+//                  whose sum left the range the shift covers
+//   combine_dh     fused path: d_hidden = coef_t * (sum of split partials)
+//                  - a_t W[y_t], in split order
 //   from_logits    cross-entropy from materialised logits (ce_from_logits_flat):
 //                  a row-streaming, HBM-bound kernel with an optional
 //                  grad_logits write
@@ -48,7 +55,7 @@ __global__ void validate_kernel(const int64_t *__restrict__ targets, const uint8
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st)
 {
-    cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 2 * sizeof(int), st);
+    cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 3 * sizeof(int), st);   // bad, n_valid, redo
     if (e != cudaSuccess) return e;
     int grid = static_cast<int>((n + 255) / 256);
     if (grid > 1024) grid = 1024;
@@ -308,6 +315,156 @@ cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, 
     if (grid > 4096) grid = 4096;
     sum_splits_kernel<<<static_cast<int>(grid), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(part), nsplit, c4, reinterpret_cast<float4 *>(out));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// The fused forward + d_hidden path.  See k_bwd.cu (BWD_FUSED) for the pass
+// itself: it exponentiates every logit against r_t = s[t][y_t] log2e + 64 and
+// reports, per (split, CTA, token), the sum of those terms.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One warp per token: 16-byte loads of the hidden row and the target's weight
+// row, fp32 products summed per lane in k order, then a fixed xor tree.
+__global__ void __launch_bounds__(256) tgt_logit_kernel(const uint16_t *__restrict__ H,
+                                                        const uint16_t *__restrict__ W,
+                                                        const int64_t *__restrict__ targets, int64_t n,
+                                                        int64_t d, int64_t n_pad, float *__restrict__ tgt,
+                                                        float4 *__restrict__ tokp)
+{
+    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= n_pad) return;
+    if (t >= n) {
+        if (lane == 0) {
+            tgt[t] = 0.f;
+            tokp[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
+    }
+    const uint4 *h = reinterpret_cast<const uint4 *>(H + t * d);
+    const uint4 *w = reinterpret_cast<const uint4 *>(W + targets[t] * d);
+    float acc = 0.f;
+    for (int64_t k = lane; k < d / 8; k += 32) {
+        const uint4 a = h[k], b = w[k];
+        acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
+        acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
+        acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
+        acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
+        acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
+        acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
+        acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
+        acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        tgt[t] = acc;
+        tokp[t] = make_float4(fmaf(acc, static_cast<float>(LOG2E), FUSED_SHIFT), 0.f, 0.f, 0.f);
+    }
+}
+
+cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
+                             int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st)
+{
+    tgt_logit_kernel<<<static_cast<unsigned>((n_pad + 7) / 8), 256, 0, st>>>(H, W, targets, n, d, n_pad,
+                                                                          tgt, tokp);
+    return cudaGetLastError();
+}
+
+// One thread per token.  Z = sum of the nz partials in index order (double);
+// with r_t the shift, lse_t = (r_t + log2 Z) ln 2.  The row is flagged for the
+// exact recomputation when Z is outside [2^-80, 2^90] (or not a number): the
+// shifted terms are only trusted while the largest stays far from the fp32
+// and bf16 limits.  The flag is raised for masked rows too, since their lse is
+// an output.
+__global__ void merge_fused_kernel(const float *__restrict__ zpart, int64_t nz, const float *__restrict__ tgt,
+                                   const int64_t *__restrict__ targets, const uint8_t *__restrict__ mask,
+                                   int64_t n, int64_t n_pad, double alpha, double wz,
+                                   float *__restrict__ lse_out, float *__restrict__ ce_out,
+                                   double *__restrict__ tokacc, float4 *__restrict__ tokp,
+                                   float2 *__restrict__ dhc, WsHeader *hdr)
+{
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= n_pad) return;
+    if (t >= n) {
+        tokp[t] = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+        dhc[t] = make_float2(0.f, 0.f);
+        return;
+    }
+    double Z = 0.0;
+    for (int64_t j = 0; j < nz; ++j) Z += static_cast<double>(zpart[j * n_pad + t]);
+    if (!(Z >= 0x1p-80 && Z <= 0x1p90)) hdr->redo = 1;
+    const double r = static_cast<double>(tokp[t].x);
+    const float lse_f = static_cast<float>((r + log2(Z)) * LN2);
+    const double lse = lse_f;
+    const bool on = mask ? (mask[t] != 0) : true;
+    const double ce = on ? lse - static_cast<double>(tgt[t]) : 0.0;
+    const double z2 = on ? lse * lse : 0.0;
+    lse_out[t] = lse_f;
+    if (ce_out) ce_out[t] = static_cast<float>(ce);
+    tokacc[t] = ce + wz * z2;
+    tokacc[n_pad + t] = ce;
+    tokacc[2 * n_pad + t] = z2;
+    const double at = on ? alpha : 0.0;
+    const double cz = at * (1.0 + 2.0 * wz * lse);
+    tokp[t] = make_float4(static_cast<float>(lse * LOG2E), static_cast<float>(cz), static_cast<float>(at),
+                          __int_as_float(static_cast<int>(targets[t])));
+    dhc[t] = make_float2(static_cast<float>(cz / Z), static_cast<float>(at));
+}
+
+cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,
+                               const uint8_t *mask, int64_t n, int64_t n_pad, double alpha, double wz,
+                               float *lse_out, float *ce_out, double *tokacc, float4 *tokp,
+                               float2 *dhc, WsHeader *hdr, cudaStream_t st)
+{
+    merge_fused_kernel<<<static_cast<unsigned>((n_pad + 127) / 128), 128, 0, st>>>(
+        zpart, nz, tgt, targets, mask, n, n_pad, alpha, wz, lse_out, ce_out, tokacc, tokp, dhc, hdr);
+    return cudaGetLastError();
+}
+
+// d_hidden[t][k] = coef_t * sum_s part[s][t][k] - a_t W[y_t][k], the splits
+// added in split order.  `part` may be `out` itself (one split): every
+// element is read before the same thread writes it.  A non-finite result
+// flags the call for the exact recomputation (it would also come out of
+// non-finite inputs, where the recomputation gives the same values).
+__global__ void combine_dh_kernel(const float4 *part, int64_t nsplit, int64_t n, int64_t d4,
+                                  const uint16_t *__restrict__ W, const int64_t *__restrict__ targets,
+                                  const float2 *__restrict__ dhc, float4 *out, WsHeader *hdr)
+{
+    const int64_t count4 = n * d4;
+    bool bad = false;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / d4, k4 = i - t * d4;
+        float4 acc = part[i];
+        for (int64_t s = 1; s < nsplit; ++s) {
+            const float4 v = part[s * count4 + i];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const float2 c = dhc[t];
+        const uint2 wv = *reinterpret_cast<const uint2 *>(W + targets[t] * (d4 * 4) + k4 * 4);
+        float4 o;
+        o.x = fmaf(c.x, acc.x, -c.y * bf_lo(wv.x));
+        o.y = fmaf(c.x, acc.y, -c.y * bf_hi(wv.x));
+        o.z = fmaf(c.x, acc.z, -c.y * bf_lo(wv.y));
+        o.w = fmaf(c.x, acc.w, -c.y * bf_hi(wv.y));
+        bad |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
+        out[i] = o;
+    }
+    if (bad) hdr->redo = 1;
+}
+
+cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int64_t d,
+                              const uint16_t *W, const int64_t *targets, const float2 *dhc,
+                              float *out, WsHeader *hdr, cudaStream_t st)
+{
+    const int64_t c4 = n * (d / 4);   // d_model % 8 == 0 on this path
+    int64_t grid = (c4 + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    combine_dh_kernel<<<static_cast<int>(grid), 256, 0, st>>>(
+        reinterpret_cast<const float4 *>(part), nsplit, n, d / 4, W, targets, dhc,
+        reinterpret_cast<float4 *>(out), hdr);
     return cudaGetLastError();
 }
 

@@ -178,6 +178,8 @@ struct Ws {
     double *tokacc() const { return reinterpret_cast<double *>(base + L.off_tokacc); }
     float *part() const { return reinterpret_cast<float *>(base + L.off_part); }
     float *dhpart() const { return reinterpret_cast<float *>(base + L.off_dhpart); }
+    float *zpart() const { return reinterpret_cast<float *>(base + L.off_zpart); }
+    float2 *dhc() const { return reinterpret_cast<float2 *>(base + L.off_dhc); }
 };
 
 // ---- the forward statistics pass + merge + reduction (label CE) ------------
@@ -302,6 +304,70 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
     return LOSSK_OK;
 }
 
+// ---- forward + d_hidden in one pass (label CE, bf16) ---------------------------
+// The d_hidden schedule of the backward run before any lse exists: every logit
+// is exponentiated against the per-token shift r_t = s[t][y_t] log2e + 64
+// (tgt_logit), the pass accumulates D = G' W and reports the sums of G'
+// (BWD_FUSED in k_bwd.cu), merge_fused turns the sums into lse, ce, z and the
+// d_weight parameters, and combine_dh scales D into d_hidden.  One logit pass
+// less than the separate forward and d_hidden passes.  A row whose shifted
+// terms left the trusted range raises the workspace's redo word; the caller
+// then recomputes everything on the separate passes.
+int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
+                  const int64_t *targets, const uint8_t *mask, double wz, double alpha,
+                  float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st)
+{
+    const WsLayout &L = w.L;
+    const uint16_t *Hb = static_cast<const uint16_t *>(H), *Wb = static_cast<const uint16_t *>(W);
+    cudaError_t e;
+    {
+        Launch k(KK_TGT_LOGIT, st);
+        e = launch_tgt_logit(Hb, Wb, targets, n, d, L.n_pad, w.tgt(), w.tokp(), st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    const BwdGeom g = bwd_geometry(d, false);
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!make_map(&a.map_h, H, d, n, 64, 128) || !make_map(&a.map_w, W, d, V, 64, 128) ||
+        !make_map(&a.map_ys, W, d, V, 64, 64))
+        return LOSSK_DEVICE_ERROR;
+    a.n_tok = static_cast<int>(n);
+    a.vocab = static_cast<int>(V);
+    a.d = static_cast<int>(d);
+    a.n_fixed = static_cast<int>(cdiv(n, 128));
+    a.n_loop = static_cast<int>(cdiv(V, 128));
+    a.n_split = static_cast<int>(L.nsplit);
+    a.n_cl = g.n_cl;
+    a.n_dg = g.n_dg;
+    a.g_slots = g.g_slots;
+    a.inv_t_l2e = static_cast<float>(LOG2E);
+    a.tokp = w.tokp();
+    float *part = L.nsplit > 1 ? w.dhpart() : d_hidden;
+    a.out = part;
+    a.out_split_stride = n * d;
+    a.zpart = w.zpart();
+    a.zpart_stride = L.n_pad;
+    a.err = &w.hdr()->err;
+    {
+        Launch k(KK_TC_FUSED, st);
+        e = launch_bwd(BWD_FUSED, false, a, a.n_fixed * a.n_split * a.n_dg, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    {
+        Launch k(KK_MERGE_FUSED, st);
+        e = launch_merge_fused(w.zpart(), L.nsplit * g.n_cl, w.tgt(), targets, mask, n, L.n_pad, alpha,
+                               wz, lse_out, ce_out, w.tokacc(), w.tokp(), w.dhc(), w.hdr(), st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    {
+        Launch k(KK_REDUCE, st);
+        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    Launch k(KK_COMBINE_DH, st);
+    return status_of(launch_combine_dh(part, L.nsplit, n, d, Wb, targets, w.dhc(), d_hidden, w.hdr(), st));
+}
+
 // Checks shared by the fused calls, in the documented order up to 585.
 int32_t check_fused(int64_t n, int64_t d, int64_t V, int64_t chunk, bool has_chunk, int32_t dtype,
                     const void *H, int64_t hl, const void *W, int64_t wl, const void *workspace,
@@ -393,6 +459,13 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (fwd) off = align256(off + sizeof(float) * L->nstat * L->n_ct * L->n_pad);
     L->off_dhpart = off;
     if (bwd && L->nsplit > 1) off = align256(off + sizeof(float) * L->nsplit * n * d);
+    // The training-step call on the tensor-core path folds d_hidden into the
+    // forward (run_fused); it keeps the separate passes' space for its fallback.
+    const bool fused = kind == LOSSK_KIND_CE_FWD_BWD && tc;
+    L->off_zpart = off;
+    if (fused) off = align256(off + sizeof(float) * L->nsplit * 8 * L->n_pad);
+    L->off_dhc = off;
+    if (fused) off = align256(off + sizeof(float2) * L->n_pad);
     L->off_red = off;
     off = align256(off + 64);
     L->total = off;
@@ -506,6 +579,22 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     Hdr h;
     s = validate(targets, mask, n, V, w.hdr(), st, &h);
     if (s != LOSSK_OK) return s;
+    if (do_fwd && do_bwd && dH && dtype == LOSSK_BF16) {
+        const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
+        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dH, st);
+        if (s == LOSSK_OK && dW)
+            s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st);
+        if (s != LOSSK_OK) return s;
+        // The call's second read-back: a device timeout, or a row the shifted
+        // pass could not represent (then every output is recomputed by the
+        // separate passes below, which need no shift).
+        int flags[4] = {0, 0, 0, 0};
+        if (cudaMemcpyAsync(flags, w.hdr(), sizeof(flags), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+        if (flags[0]) return LOSSK_DEVICE_TIMEOUT;
+        if (!flags[3]) return LOSSK_OK;
+    }
     if (do_fwd) {
         s = run_ce_fwd(w, n, d, V, dtype, H, W, targets, mask, wz, lse_io, ce_out, scalars, st);
         if (s != LOSSK_OK) return s;
@@ -683,7 +772,8 @@ const char *lossk_kernel_name(int32_t kind)
     static const char *names[KK_N] = {"validate",     "tc_stats",      "tc_rows",     "tc_cols",
                                       "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
                                       "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
-                                      "from_logits"};
+                                      "from_logits",  "tc_fused",      "tgt_logit",   "merge_fused",
+                                      "combine_dh"};
     return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
 }
 

@@ -25,7 +25,8 @@ struct WsHeader {
     int err;          // device error word (ERR_* in ptx.cuh)
     int bad_targets;  // count of targets outside [0, vocab)
     int n_valid;      // counted tokens
-    int pad[61];
+    int redo;         // fused pass: a row left the range its reference shift covers
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -47,6 +48,8 @@ struct WsLayout {
     size_t off_tokacc = 0;   // double [3][n_pad] per-token reduction terms
     size_t off_part = 0;     // float  [nstat][n_ct][n_pad]
     size_t off_dhpart = 0;   // float  [nsplit][n_tok][d_model] (nsplit > 1)
+    size_t off_zpart = 0;    // float  [nsplit * 8][n_pad] fused pass: sums of G' per (split, CTA)
+    size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
     size_t off_red = 0;      // double [8] reduction output scratch
     size_t total = 0;
 };
@@ -87,7 +90,12 @@ struct TcArgs {
 };
 
 // ---- backward (cluster-shared grad tiles) kernel arguments -------------------
-enum BwdMode : int { BWD_ROWS = 1, BWD_COLS = 2 };
+// BWD_FUSED: the d_hidden schedule run as the forward pass as well, with a
+// per-token reference shift in place of the log-sum-exp (k_bwd.cu).
+enum BwdMode : int { BWD_ROWS = 1, BWD_COLS = 2, BWD_FUSED = 3 };
+
+// The fused pass's reference: r_t = s[t][y_t] log2e + FUSED_SHIFT (log2 units).
+constexpr float FUSED_SHIFT = 64.f;
 
 struct BwdArgs {
     CUtensorMap map_h;     // hidden [n_tok][d], box {64, 128}
@@ -106,6 +114,8 @@ struct BwdArgs {
     const float4 *tokp;
     float *out;
     int64_t out_split_stride;
+    float *zpart;          // BWD_FUSED: sums of G' [n_split * n_cl][zpart_stride]
+    int64_t zpart_stride;
     int *err;
 };
 
@@ -131,6 +141,10 @@ enum KernelKind : int {
     KK_TOKP,
     KK_SUM_SPLITS,
     KK_FROM_LOGITS,
+    KK_TC_FUSED,
+    KK_TGT_LOGIT,
+    KK_MERGE_FUSED,
+    KK_COMBINE_DH,
     KK_N
 };
 
@@ -161,6 +175,18 @@ cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8
                            cudaStream_t st);
 cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
                               cudaStream_t st);
+// The fused forward + d_hidden path (label CE, bf16): target logit and
+// reference shift per token; merge of the fused pass's sums into lse, ce, z
+// and the backward parameters; d_hidden from the split partials.
+cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
+                             int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st);
+cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,
+                               const uint8_t *mask, int64_t n, int64_t n_pad, double alpha, double wz,
+                               float *lse_out, float *ce_out, double *tokacc, float4 *tokp,
+                               float2 *dhc, WsHeader *hdr, cudaStream_t st);
+cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int64_t d,
+                              const uint16_t *W, const int64_t *targets, const float2 *dhc,
+                              float *out, WsHeader *hdr, cudaStream_t st);
 cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *targets,
                                const uint8_t *mask, int64_t n, int64_t V, double wz,
                                double alpha, float *lse_out, float *ce_out, double *tokacc,
