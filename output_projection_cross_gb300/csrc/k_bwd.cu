@@ -498,22 +498,26 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int split = u / (a.n_fixed * a.n_dg);
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(row) * a.d;
+            // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
+            // stores (rows are d_model floats apart, d_model % 8 == 0, so every
+            // chunk start is 32-byte aligned).
 #pragma unroll 1
-            for (int q = 0; q < TC_SLICE / 32; ++q) {
-                uint32_t v[32];
-                tmem_ld32(trow + ACC_COL + q * 32, v);
+            for (int q = 0; q < TC_SLICE / 32; q += 2) {
+                uint32_t v[2][32];
+                tmem_ld32(trow + ACC_COL + q * 32, v[0]);
+                tmem_ld32(trow + ACC_COL + (q + 1) * 32, v[1]);
                 tmem_ld_wait();
-                const int col = slice0 + q * 32;
-                if (row < n_rows && col < a.d) {
-                    if (col + 32 <= a.d) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(dst + col + i) =
-                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (col + i < a.d) dst[col + i] = __uint_as_float(v[i]);
+                for (int h = 0; h < 2; ++h) {
+                    const int col = slice0 + (q + h) * 32;
+                    if (row < n_rows && col < a.d) {
+                        if (col + 32 <= a.d) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 8) st_global_v8(dst + col + i, &v[h][i]);
+                        } else {
+                            for (int i = 0; i < 32; ++i)
+                                if (col + i < a.d) dst[col + i] = __uint_as_float(v[h][i]);
+                        }
                     }
                 }
             }

@@ -369,6 +369,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
                  : "memory");
 }
 
+// 256-bit global store of eight 32-bit words (the address is 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // ---- math -------------------------------------------------------------------------
 
 __device__ __forceinline__ float ex2_approx(float x)
