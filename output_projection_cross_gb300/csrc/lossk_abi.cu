@@ -180,7 +180,36 @@ struct Ws {
     float *dhpart() const { return reinterpret_cast<float *>(base + L.off_dhpart); }
     float *zpart() const { return reinterpret_cast<float *>(base + L.off_zpart); }
     float2 *dhc() const { return reinterpret_cast<float2 *>(base + L.off_dhc); }
+    uint16_t *gring() const { return reinterpret_cast<uint16_t *>(base + L.off_gring); }
 };
+
+// Tensor maps and shape fields of a cluster pass.  rows: d_hidden / fused
+// (fixed = hidden token tiles, loop = vocabulary); otherwise d_weight (fixed =
+// weight vocabulary tiles, loop = tokens).
+bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
+              BwdArgs *a)
+{
+    std::memset(a, 0, sizeof(*a));
+    const void *Fx = rows ? H : W, *Lp = rows ? W : H;
+    const int64_t nf = rows ? n : V, nl = rows ? V : n;
+    if (!make_map(&a->map_fix, Fx, d, nf, 64, 128) || !make_map(&a->map_loop, Lp, d, nl, 64, BWD_BN) ||
+        !make_map(&a->map_ys, Lp, d, nl, 64, 64) || !make_map(&a->map_g, w.gring(), 128, G_RING_ROWS, 64, 128))
+        return false;
+    const BwdGeom g = bwd_geometry(d, false);
+    a->gscr = w.gring();
+    a->n_tok = static_cast<int>(n);
+    a->vocab = static_cast<int>(V);
+    a->d = static_cast<int>(d);
+    a->n_fixed = static_cast<int>(cdiv(nf, 128));
+    a->n_loop = static_cast<int>(cdiv(nl, BWD_BN));
+    a->n_split = 1;
+    a->n_cl = g.n_cl;
+    a->n_dg = g.n_dg;
+    a->tokp = w.tokp();
+    a->out_split_stride = n * d;
+    a->err = &w.hdr()->err;
+    return true;
+}
 
 // ---- the forward statistics pass + merge + reduction (label CE) ------------
 int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
@@ -239,32 +268,17 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
     cudaError_t e = cudaSuccess;
     const float inv_t = static_cast<float>(1.0 / temperature);
     if (dtype == LOSSK_BF16) {
-        const BwdGeom g = bwd_geometry(d, distill);
         for (int pass = 0; pass < 2; ++pass) {
             float *dst = pass == 0 ? d_hidden : d_weight;
             if (!dst) continue;
             const bool rows = pass == 0;
             BwdArgs a;
-            std::memset(&a, 0, sizeof(a));
-            if (!make_map(&a.map_h, H, d, n, 64, 128) || !make_map(&a.map_w, W, d, V, 64, 128) ||
-                !make_map(&a.map_ys, rows ? W : H, d, rows ? V : n, 64, 64))
-                return LOSSK_DEVICE_ERROR;
+            if (!bwd_args(w, rows, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
             a.teacher = distill ? static_cast<const uint16_t *>(teacher) : nullptr;
-            a.n_tok = static_cast<int>(n);
-            a.vocab = static_cast<int>(V);
-            a.d = static_cast<int>(d);
-            a.n_fixed = static_cast<int>(cdiv(rows ? n : V, 128));
-            a.n_loop = static_cast<int>(cdiv(rows ? V : n, 128));
             a.n_split = rows ? static_cast<int>(L.nsplit) : 1;
-            a.n_cl = g.n_cl;
-            a.n_dg = g.n_dg;
-            a.g_slots = g.g_slots;
             a.direction = direction;
             a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
-            a.tokp = w.tokp();
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
-            a.out_split_stride = n * d;
-            a.err = &w.hdr()->err;
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
@@ -327,21 +341,9 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     const BwdGeom g = bwd_geometry(d, false);
     BwdArgs a;
-    std::memset(&a, 0, sizeof(a));
-    if (!make_map(&a.map_h, H, d, n, 64, 128) || !make_map(&a.map_w, W, d, V, 64, 128) ||
-        !make_map(&a.map_ys, W, d, V, 64, 64))
-        return LOSSK_DEVICE_ERROR;
-    a.n_tok = static_cast<int>(n);
-    a.vocab = static_cast<int>(V);
-    a.d = static_cast<int>(d);
-    a.n_fixed = static_cast<int>(cdiv(n, 128));
-    a.n_loop = static_cast<int>(cdiv(V, 128));
+    if (!bwd_args(w, true, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
     a.n_split = static_cast<int>(L.nsplit);
-    a.n_cl = g.n_cl;
-    a.n_dg = g.n_dg;
-    a.g_slots = g.g_slots;
     a.inv_t_l2e = static_cast<float>(LOG2E);
-    a.tokp = w.tokp();
     float *part = L.nsplit > 1 ? w.dhpart() : d_hidden;
     a.out = part;
     a.out_split_stride = n * d;
@@ -403,11 +405,7 @@ BwdGeom bwd_geometry(int64_t d, bool distill)
     BwdGeom g;
     g.n_dg = static_cast<int>(cdiv(ns, 8));
     g.n_cl = static_cast<int>(cdiv(ns, g.n_dg));
-    const int r_max = 4;
     (void)distill;
-    g.g_slots = 1;
-    for (int r = r_max; r >= 1; --r)
-        if (g.n_cl % r == 0) { g.g_slots = r; break; }
     return g;
 }
 
@@ -466,6 +464,8 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (fused) off = align256(off + sizeof(float) * L->nsplit * 8 * L->n_pad);
     L->off_dhc = off;
     if (fused) off = align256(off + sizeof(float2) * L->n_pad);
+    L->off_gring = off;
+    if (bwd && tc) off = align256(off + sizeof(uint16_t) * 128 * static_cast<size_t>(G_RING_ROWS));
     L->off_red = off;
     off = align256(off + 64);
     L->total = off;

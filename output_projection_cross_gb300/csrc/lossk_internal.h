@@ -50,6 +50,7 @@ struct WsLayout {
     size_t off_dhpart = 0;   // float  [nsplit][n_tok][d_model] (nsplit > 1)
     size_t off_zpart = 0;    // float  [nsplit * 8][n_pad] fused pass: sums of G' per (split, CTA)
     size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
+    size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the cluster passes
     size_t off_red = 0;      // double [8] reduction output scratch
     size_t total = 0;
 };
@@ -97,18 +98,27 @@ enum BwdMode : int { BWD_ROWS = 1, BWD_COLS = 2, BWD_FUSED = 3 };
 // The fused pass's reference: r_t = s[t][y_t] log2e + FUSED_SHIFT (log2 units).
 constexpr float FUSED_SHIFT = 64.f;
 
+// Loop supertile: the logit tile of the cluster passes is 128 fixed rows x
+// BWD_BN loop columns.  Grad-tile ring: G_SLOTS slots of one supertile
+// (2 x 128 x 128 bf16) per CTA, for at most G_MAX_CTAS CTAs.
+constexpr int BWD_BN = 256;
+constexpr int G_SLOTS = 2;
+constexpr int G_MAX_CTAS = 160;
+constexpr int64_t G_RING_ROWS = int64_t(G_MAX_CTAS) * G_SLOTS * 2 * 128;   // rows of 128 bf16
+
 struct BwdArgs {
-    CUtensorMap map_h;     // hidden [n_tok][d], box {64, 128}
-    CUtensorMap map_w;     // weight [vocab][d], box {64, 128}
-    CUtensorMap map_ys;    // the loop tensor (weight for d_hidden, hidden for d_weight), box {64, 64}
+    CUtensorMap map_fix;   // the fixed tensor (hidden for d_hidden, weight for d_weight), box {64, 128}
+    CUtensorMap map_loop;  // the loop tensor as the logit MMA's B operand, box {64, 256}
+    CUtensorMap map_ys;    // the loop tensor rows x d-slice (MN-major B of the accumulate), box {64, 64}
+    CUtensorMap map_g;     // the grad-tile ring [G_RING_ROWS][128] bf16, box {64, 128}
+    uint16_t *gscr;        // the grad-tile ring itself
     const uint16_t *teacher; // teacher logits [n_tok][vocab] (bf16), read by the epilogue
     int n_tok, vocab, d;
     int n_fixed;           // fixed tiles: token tiles (d_hidden) or vocabulary tiles (d_weight)
-    int n_loop;            // loop tiles: vocabulary tiles (d_hidden) or token tiles (d_weight)
+    int n_loop;            // loop supertiles (BWD_BN columns): vocabulary (d_hidden) or tokens (d_weight)
     int n_split;           // splits of the loop range (d_hidden)
     int n_cl;              // CTAs per cluster = 256-column d-slices per group
     int n_dg;              // d-groups (clusters per fixed tile and split)
-    int g_slots;           // grad slots in use (divides n_cl)
     int direction;
     float inv_t_l2e;
     const float4 *tokp;
@@ -122,7 +132,7 @@ struct BwdArgs {
 // Cluster geometry of the backward for a d_model: slices of 256 columns, at
 // most 8 CTAs per cluster, d-groups beyond that.
 struct BwdGeom {
-    int n_cl, n_dg, g_slots;
+    int n_cl, n_dg;
 };
 BwdGeom bwd_geometry(int64_t d, bool distill);
 
