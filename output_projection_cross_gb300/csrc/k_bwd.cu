@@ -348,143 +348,198 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const float kT = a.inv_t_l2e;
         const float4 P0 = DISTILL ? make_float4(0.f, 0.f, 0.f, 0.f)
                                   : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
-        bool ok = true;
         int m_all = 0;                                // own logit tiles consumed so far
-        for (int k = 0, u = cluster; u < n_units && ok; ++k, u += n_clusters) {
-            const BwdUnit w = bwd_unit(a, u);
-            const int n_own = crank < w.ny ? (w.ny - crank + c - 1) / c : 0;
-            const int fixrow = w.fixed * 128 + r;     // token (d_hidden) or vocabulary (d_weight) row
-            float4 P = P0;
-            if (ROWS && fixrow < a.n_tok) P = a.tokp[fixrow];
-            double zsum = 0.0;                        // fused pass: this CTA's sum of G' for its row
-            for (int m = 0; m < n_own && ok; ++m, ++m_all) {
-                const int y = m * c + crank;
-                const int loop0 = (w.yt_begin + y) * BWD_BN;
-                const int g = m_all % G_SLOTS;
-                // the slot's previous tile has been loaded by every CTA of the cluster
-                ok = mbar_wait_cluster(&gfree[g], ((m_all / G_SLOTS) & 1) ^ 1, err);
-                if (!ROWS) {
-                    // per-token parameters of this supertile's 256 token columns (each warp
-                    // keeps its own copy, so no barrier spans warps that may unwind apart)
-                    __syncwarp();
+        auto n_own_of = [&](const BwdUnit &w) { return crank < w.ny ? (w.ny - crank + c - 1) / c : 0; };
+        auto params_of = [&](const BwdUnit &w) {      // d_hidden: the fixed token row's parameters
+            const int fixrow = w.fixed * 128 + r;
+            return (ROWS && fixrow < a.n_tok) ? a.tokp[fixrow] : P0;
+        };
+        // The first row of the teacher block of own supertile m of unit w, for
+        // an L2 prefetch one supertile ahead of its use.
+        auto teacher_prefetch = [&](const BwdUnit &w, int m) {
+            const int fixrow = w.fixed * 128 + r;
+            const int loop0 = (w.yt_begin + m * c + crank) * BWD_BN;
+            if (ROWS) {
+                if (fixrow >= a.n_tok) return;
+                const uint16_t *p = a.teacher + static_cast<int64_t>(fixrow) * a.vocab + loop0;
 #pragma unroll
-                    for (int i = 0; i < BWD_BN / 32; ++i) {
-                        const int t = loop0 + lane + i * 32;
-                        sP[lane + i * 32] = t < a.n_tok ? a.tokp[t] : P0;
-                    }
-                    __syncwarp();
+                for (int i = 0; i < 4; ++i)
+                    if (loop0 + i * 64 < a.vocab) prefetch_l2(p + i * 64);
+            } else {
+                const int fix0 = w.fixed * 128;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = loop0 + r + h * 128;
+                    if (t >= a.n_tok) continue;
+                    const uint16_t *p = a.teacher + static_cast<int64_t>(t) * a.vocab + fix0;
+                    prefetch_l2(p);
+                    if (fix0 + 64 < a.vocab) prefetch_l2(p + 64);
                 }
-                ok = ok && mbar_wait(tfull, m_all & 1, err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();
-                const int ncols = min(BWD_BN, (ROWS ? a.vocab : a.n_tok) - loop0);   // valid loop columns
-                const int rel = ROWS && !DISTILL ? __float_as_int(P.w) - loop0 : 0;
-                // teacher logits of this thread's row and the supertile's columns
-                const bool t_ok = DISTILL && (ROWS ? fixrow < a.n_tok : fixrow < a.vocab);
-                const uint16_t *tbase =
-                    DISTILL ? a.teacher + (ROWS ? static_cast<int64_t>(t_ok ? fixrow : 0) * a.vocab + loop0
-                                                : static_cast<int64_t>(loop0) * a.vocab + (t_ok ? fixrow : 0))
-                            : nullptr;
-                uint32_t tw[16];                      // a chunk's 32 teacher values (bf16 pairs)
-                auto tload = [&](int q) {
-                    if (ROWS) {
-                        // one contiguous 64-byte row segment: four 16-byte loads
-                        const uint4 *src = reinterpret_cast<const uint4 *>(tbase + q * 32);
+            }
+        };
+        // One own logit tile (the m-th of unit w): wait for its ring slot and
+        // its logits, form G in registers, store it into the slot, publish.
+        auto tile = [&](const BwdUnit &w, int m, const float4 &P, double &zsum) -> bool {
+            const int fixrow = w.fixed * 128 + r;     // token (d_hidden) or vocabulary (d_weight) row
+            const int y = m * c + crank;
+            const int loop0 = (w.yt_begin + y) * BWD_BN;
+            const int g = m_all % G_SLOTS;
+            // the slot's previous tile has been loaded by every CTA of the cluster
+            bool ok = mbar_wait_cluster(&gfree[g], ((m_all / G_SLOTS) & 1) ^ 1, err);
+            if (!ROWS) {
+                // per-token parameters of this supertile's 256 token columns (each warp
+                // keeps its own copy, so no barrier spans warps that may unwind apart)
+                __syncwarp();
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            const uint4 v4 = (t_ok && q * 32 + c4 * 8 < ncols) ? __ldg(src + c4)
-                                                                                : make_uint4(0, 0, 0, 0);
-                            tw[c4 * 4 + 0] = v4.x; tw[c4 * 4 + 1] = v4.y;
-                            tw[c4 * 4 + 2] = v4.z; tw[c4 * 4 + 3] = v4.w;
-                        }
-                    } else {
-                        // one element per token row; a warp reads 64 contiguous bytes per token
+                for (int i = 0; i < BWD_BN / 32; ++i) {
+                    const int t = loop0 + lane + i * 32;
+                    sP[lane + i * 32] = t < a.n_tok ? a.tokp[t] : P0;
+                }
+                __syncwarp();
+            }
+            if (DISTILL && m + 1 < n_own_of(w)) teacher_prefetch(w, m + 1);
+            ok = ok && mbar_wait(tfull, m_all & 1, err);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            tc_fence_after();
+            const int ncols = min(BWD_BN, (ROWS ? a.vocab : a.n_tok) - loop0);   // valid loop columns
+            const int rel = ROWS && !DISTILL ? __float_as_int(P.w) - loop0 : 0;
+            // teacher logits of this thread's row and the supertile's columns
+            const bool t_ok = DISTILL && (ROWS ? fixrow < a.n_tok : fixrow < a.vocab);
+            const uint16_t *tbase =
+                DISTILL ? a.teacher + (ROWS ? static_cast<int64_t>(t_ok ? fixrow : 0) * a.vocab + loop0
+                                            : static_cast<int64_t>(loop0) * a.vocab + (t_ok ? fixrow : 0))
+                        : nullptr;
+            uint32_t tw[16];                          // a chunk's 32 teacher values (bf16 pairs)
+            auto tload = [&](int q) {
+                if (ROWS) {
+                    // one contiguous 64-byte row segment: four 16-byte loads
+                    const uint4 *src = reinterpret_cast<const uint4 *>(tbase + q * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int j = q * 32 + i;
-                            const uint32_t lo = (t_ok && j < ncols)
-                                                    ? __ldg(tbase + static_cast<int64_t>(j) * a.vocab) : 0u;
-                            const uint32_t hi = (t_ok && j + 1 < ncols)
-                                                    ? __ldg(tbase + static_cast<int64_t>(j + 1) * a.vocab) : 0u;
-                            tw[i >> 1] = lo | (hi << 16);
-                        }
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint4 v4 = (t_ok && q * 32 + c4 * 8 < ncols) ? __ldg(src + c4)
+                                                                            : make_uint4(0, 0, 0, 0);
+                        tw[c4 * 4 + 0] = v4.x; tw[c4 * 4 + 1] = v4.y;
+                        tw[c4 * 4 + 2] = v4.z; tw[c4 * 4 + 3] = v4.w;
                     }
-                };
-                if (DISTILL) tload(0);
-                uint16_t *gdst = a.gscr + static_cast<int64_t>(((blockIdx.x * G_SLOTS + g) * 2) * 128 + r) * 128;
-                float zt = 0.f;
-#pragma unroll 1
-                for (int q = 0; q < BWD_BN / 32; ++q) {
-                    uint32_t v[32];
-                    tmem_ld32(trow + q * 32, v);
-                    uint32_t tcur[16];
-                    if (DISTILL) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) tcur[i] = tw[i];
-                        if (q + 1 < BWD_BN / 32) tload(q + 1);
-                    }
-                    tmem_ld_wait();
-                    uint32_t pk[16];
+                } else {
+                    // one element per token row; a warp reads 64 contiguous bytes per token
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        float gg[2];
-#pragma unroll
-                        for (int uu = 0; uu < 2; ++uu) {
-                            const int j = q * 32 + i + uu;           // loop column within the supertile
-                            const float s = __uint_as_float(v[i + uu]);
-                            const float4 Pq = ROWS ? P : sP[j];
-                            if (FUSED) {
-                                const float gv = ex2_approx(fmaf(s, L2E, -Pq.x));
-                                gg[uu] = gv;
-                                zt += j < ncols ? gv : 0.f;
-                            } else if (!DISTILL) {
-                                float gv = Pq.y * ex2_approx(fmaf(s, L2E, -Pq.x));
-                                if (ROWS ? (rel == j) : (__float_as_int(Pq.w) == fixrow)) gv -= Pq.z;
-                                gg[uu] = gv;
-                            } else {
-                                const float tv = uu ? bw_hi(tcur[i >> 1]) : bw_lo(tcur[i >> 1]);
-                                const float a2 = s * kT, b2 = tv * kT;
-                                const float qv = ex2_approx(a2 - Pq.x);
-                                if (a.direction == DIR_RKL)
-                                    gg[uu] = Pq.z * qv * fmaf(a2 - b2, static_cast<float>(LN2), Pq.w);
-                                else
-                                    gg[uu] = Pq.z * qv - Pq.w * ex2_approx(b2 - Pq.y);
-                            }
-                        }
-                        pk[i >> 1] = pack_bf16x2(gg[0], gg[1]);
+                        const int j = q * 32 + i;
+                        const uint32_t lo = (t_ok && j < ncols)
+                                                ? __ldg(tbase + static_cast<int64_t>(j) * a.vocab) : 0u;
+                        const uint32_t hi = (t_ok && j + 1 < ncols)
+                                                ? __ldg(tbase + static_cast<int64_t>(j + 1) * a.vocab) : 0u;
+                        tw[i >> 1] = lo | (hi << 16);
                     }
-                    // columns q*32 .. q*32+31: sub-tile q/4, 64 bytes at column (q%4)*32
-                    uint16_t *dst = gdst + (q >> 2) * (128 * 128) + (q & 3) * 32;
-                    st_global_v8(dst, pk);
-                    st_global_v8(dst + 16, pk + 8);
                 }
-                if (FUSED) zsum += static_cast<double>(zt);
-                // the tile is out of TMEM: give the buffer back, then publish the slot
-                tc_fence_before();
-                mbar_arrive(tempty);
-                fence_proxy_async_global();
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t rb = smem_u32(&gready[crank * G_SLOTS + g]);
-                    for (int q = 0; q < c; ++q) mbar_arrive_remote(mapa_shared(rb, q));
+            };
+            if (DISTILL) tload(0);
+            uint16_t *gdst = a.gscr + static_cast<int64_t>(((blockIdx.x * G_SLOTS + g) * 2) * 128 + r) * 128;
+            float zt = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < BWD_BN / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld32(trow + q * 32, v);
+                uint32_t tcur[16];
+                if (DISTILL) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) tcur[i] = tw[i];
+                    if (q + 1 < BWD_BN / 32) tload(q + 1);
                 }
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float gg[2];
+#pragma unroll
+                    for (int uu = 0; uu < 2; ++uu) {
+                        const int j = q * 32 + i + uu;           // loop column within the supertile
+                        const float s = __uint_as_float(v[i + uu]);
+                        const float4 Pq = ROWS ? P : sP[j];
+                        if (FUSED) {
+                            const float gv = ex2_approx(fmaf(s, L2E, -Pq.x));
+                            gg[uu] = gv;
+                            zt += j < ncols ? gv : 0.f;
+                        } else if (!DISTILL) {
+                            float gv = Pq.y * ex2_approx(fmaf(s, L2E, -Pq.x));
+                            if (ROWS ? (rel == j) : (__float_as_int(Pq.w) == fixrow)) gv -= Pq.z;
+                            gg[uu] = gv;
+                        } else {
+                            const float tv = uu ? bw_hi(tcur[i >> 1]) : bw_lo(tcur[i >> 1]);
+                            const float a2 = s * kT, b2 = tv * kT;
+                            const float qv = ex2_approx(a2 - Pq.x);
+                            if (a.direction == DIR_RKL)
+                                gg[uu] = Pq.z * qv * fmaf(a2 - b2, static_cast<float>(LN2), Pq.w);
+                            else
+                                gg[uu] = Pq.z * qv - Pq.w * ex2_approx(b2 - Pq.y);
+                        }
+                    }
+                    pk[i >> 1] = pack_bf16x2(gg[0], gg[1]);
+                }
+                // columns q*32 .. q*32+31: sub-tile q/4, 64 bytes at column (q%4)*32
+                uint16_t *dst = gdst + (q >> 2) * (128 * 128) + (q & 3) * 32;
+                st_global_v8(dst, pk);
+                st_global_v8(dst + 16, pk + 8);
             }
+            if (FUSED) zsum += static_cast<double>(zt);
+            // the tile is out of TMEM: give the buffer back, then publish the slot
+            tc_fence_before();
+            mbar_arrive(tempty);
+            fence_proxy_async_global();
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t rb = smem_u32(&gready[crank * G_SLOTS + g]);
+                for (int q = 0; q < c; ++q) mbar_arrive_remote(mapa_shared(rb, q));
+            }
+            ++m_all;
+            return true;
+        };
+        // Units in order.  The next unit's first own tile is formed before this
+        // unit's accumulator is stored: its logits are ready earlier (the MMA
+        // issues them before this unit's last accumulates), and the MMA can
+        // then start the next logit tile while the store runs.
+        int u = cluster;
+        BwdUnit w;
+        float4 P = P0;
+        double zsum = 0.0;
+        int m0 = 0;                                   // own tiles of unit w already formed
+        if (u < n_units) {
+            w = bwd_unit(a, u);
+            P = params_of(w);
+        }
+        bool ok = true;
+        for (int k = 0; u < n_units && ok; ++k) {
+            const int n_own = n_own_of(w);
+            for (int m = m0; m < n_own && ok; ++m) ok = tile(w, m, P, zsum);
             if (!ok) break;
-            if (FUSED && w.dg == 0) {
-                // every d-group recomputes the same logits; the first one reports the sums
-                const int split = u / (a.n_fixed * a.n_dg);
-                if (fixrow < a.n_tok)
-                    a.zpart[(static_cast<int64_t>(split) * c + crank) * a.zpart_stride + fixrow] =
-                        static_cast<float>(zsum);
+            const int u2 = u + n_clusters;
+            BwdUnit w2;
+            float4 P2 = P0;
+            double zsum2 = 0.0;
+            int m02 = 0;
+            if (u2 < n_units) {
+                w2 = bwd_unit(a, u2);
+                P2 = params_of(w2);
+                if (n_own_of(w2) > 0) {
+                    ok = tile(w2, 0, P2, zsum2);
+                    if (!ok) break;
+                    m02 = 1;
+                }
             }
+            const int fixrow = w.fixed * 128 + r;
+            const int split = u / (a.n_fixed * a.n_dg);
+            if (FUSED && w.dg == 0 && fixrow < a.n_tok)
+                // every d-group recomputes the same logits; the first one reports the sums
+                a.zpart[(static_cast<int64_t>(split) * c + crank) * a.zpart_stride + fixrow] =
+                    static_cast<float>(zsum);
             // the unit's accumulator: store this CTA's rows of its d-slice
             ok = mbar_wait(accfull, k & 1, err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int slice0 = (w.dg * c + crank) * TC_SLICE;
             const int n_rows = ROWS ? a.n_tok : a.vocab;
-            const int split = u / (a.n_fixed * a.n_dg);
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(fixrow) * a.d;
             // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
@@ -512,6 +567,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             }
             tc_fence_before();
             mbar_arrive(accempty);
+            u = u2;
+            w = w2;
+            P = P2;
+            zsum = zsum2;
+            m0 = m02;
         }
         tc_fence_before();
     }

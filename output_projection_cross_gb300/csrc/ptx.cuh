@@ -384,6 +384,12 @@ __device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *w)
                  : "memory");
 }
 
+// Fetch the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---- math -------------------------------------------------------------------------
 
 __device__ __forceinline__ float ex2_approx(float x)

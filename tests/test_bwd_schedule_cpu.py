@@ -129,17 +129,31 @@ def _cta_agents(j, c, nys, nk, B):
                     B[j]["accfull"].arrive()
 
     def epilogue():
+        # Units in order; the next unit's first own tile is formed before this
+        # unit's accumulator is stored (as in the kernel).
         m_all = 0
+
+        def tile():
+            nonlocal m_all
+            g, u = m_all % G_SLOTS, m_all // G_SLOTS
+            yield from _wait(B[j]["gfree"][g], u - 1)
+            yield from _wait(B[j]["tfull"], m_all)
+            B[j]["tempty"].arrive()
+            for q in range(c):
+                B[q]["gready"][j][g].arrive()
+            m_all += 1
+
+        def n_own(ny):
+            return (ny - j + c - 1) // c if j < ny else 0
+
+        m0 = 0
         for k, ny in enumerate(nys):
-            n_own = (ny - j + c - 1) // c if j < ny else 0
-            for _ in range(n_own):
-                g, u = m_all % G_SLOTS, m_all // G_SLOTS
-                yield from _wait(B[j]["gfree"][g], u - 1)
-                yield from _wait(B[j]["tfull"], m_all)
-                B[j]["tempty"].arrive()
-                for q in range(c):
-                    B[q]["gready"][j][g].arrive()
-                m_all += 1
+            for _ in range(m0, n_own(ny)):
+                yield from tile()
+            m0 = 0
+            if k + 1 < len(nys) and n_own(nys[k + 1]) > 0:
+                yield from tile()
+                m0 = 1
             yield from _wait(B[j]["accfull"], k)
             B[j]["accempty"].arrive()
 
