@@ -40,7 +40,7 @@ WORKLOAD = "qwen3_0p6b_head"
 ALGO_FLOPS_NDV = {"tc_stats": 2.0, "tc_rows": 4.0, "tc_cols": 4.0, "tc_fused": 4.0,
                   "fp_stats": 2.0, "fp_rows": 4.0, "fp_cols": 4.0}
 HBM_KERNELS = {"from_logits", "validate", "merge_ce", "merge_distill", "reduce", "tokp_ce",
-               "sum_splits", "tgt_logit", "merge_fused", "combine_dh"}
+               "sum_splits", "tgt_logit", "merge_fused", "combine_dh", "teacher_stats"}
 
 
 def peaks():
@@ -160,7 +160,7 @@ class Clocks:
 
 def kernel_src_sha():
     h = hashlib.sha256()
-    for f in ("k_fwd2.cu", "k_bwd.cu", "k_tc.cu", "lossk_abi.cu", "ptx.cuh", "lossk_internal.h"):
+    for f in ("k_fwd2.cu", "k_bwd.cu", "k_simt.cu", "lossk_abi.cu", "ptx.cuh", "lossk_internal.h"):
         h.update(open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -389,10 +389,19 @@ def extra_paths(L, dev, pk):
         L.lossk_profile_enable(False)
         prof = L.lossk_profile_read(reset=True)
         fl = 6.0 * w.n_tok * w.d_model * w.vocab
+        kms = {k: v[0] / v[1] for k, v in prof.items()}
+        # the teacher stream on its own (the teacher statistics kernel reads
+        # every teacher logit once): its HBM roofline
+        tbytes = w.n_tok * w.vocab * 2
+        tk = kms.get("teacher_stats")
         res[f"distill_{direction}"] = {
             "workload": w.name, "ms": ms, "tokens_per_s": w.n_tok / (ms / 1e3),
             "tensor_frac_6ndV": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
-            "kernels_ms": {k: v[0] / v[1] for k, v in prof.items()}}
+            "kernels_ms": kms,
+            "teacher_stream": None if tk is None else {
+                "kernel": "teacher_stats", "algorithmic_bytes": tbytes, "kernel_ms": tk,
+                "achieved_gbs": tbytes / (tk / 1e3) / 1e9,
+                "frac_hbm": tbytes / (tk / 1e3) / 1e9 / pk["hbm_gbs"]}}
     del H, W, T, bufs
     torch.cuda.empty_cache()
     # CE from materialised logits (HBM-bound): read 622 MB bf16, write 622 MB grad

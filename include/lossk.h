@@ -278,7 +278,7 @@ int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype,
  * events, adds their durations per kind into total_ms[kind] and
  * launches[kind] (host arrays of `cap` entries), and clears them if `reset`.
  * Returns the number of kinds written, or -1 on a CUDA error. */
-#define LOSSK_N_KERNELS 17
+#define LOSSK_N_KERNELS 18
 const char *lossk_kernel_name(int32_t kind);
 int64_t lossk_launch_count(void);
 int32_t lossk_profile_enable(int32_t on);

@@ -1,7 +1,7 @@
 // k_fwd2.cu -- forward statistics of the label cross-entropy on CTA pairs.
 //
 // The forward reduces each logit tile S = H_tile . W_tile^T to per-token
-// (running max, sum of exp) pairs and the target logit -- the online
+// (running max, sum of exp) pairs (the target logit comes from tgt_logit) -- the online
 // log-sum-exp of "Loss functions and resident-context kernels" (lossk: a
 // chunk's logits are reduced as soon as they exist).  Here two CTAs of a
 // cluster act as one tcgen05 unit (cta_group::2): a 256-token x 256-vocabulary
@@ -9,6 +9,14 @@
 // rows) of the vocabulary operand B.  Per K step each SM then reads 8 KB of
 // operands for 1 MFLOP instead of 12 KB (one CTA, N = 256), which is what
 // bounds this contraction: shared-memory bytes per FLOP.
+//
+// The distillation forward (DISTILL) runs the same tiles on the student's
+// logits a = s log2(e) / T and reads the teacher's row segment of each tile
+// from global memory (16-byte loads, the next tile's segment prefetched into
+// L2).  With the teacher's log-sum-exp already known per token (teacher_stats),
+// each tile reports the student's (max, sum) and one cross term: sum p a with
+// the teacher's probabilities exact (CE, forward KL), or sum 2^(a - max)(a - b)
+// (reverse KL).
 //
 // Roles (192 threads per CTA): warp 0 of both CTAs loads its own halves with
 // TMA, counting the bytes on the even CTA's stage barrier; warp 1 of both
@@ -39,6 +47,7 @@ __device__ __forceinline__ void f2_wait_drain(uint64_t *bar, uint32_t parity)
 
 } // namespace
 
+template <bool DISTILL>
 __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -143,55 +152,90 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        const float L2E = static_cast<float>(LOG2E);
+        const float kS = DISTILL ? a.inv_t_l2e : static_cast<float>(LOG2E);
         const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
         bool ok = true;
         for (int j = 0; j < n_it && ok; ++j) {
             int tok0, voc0, vt;
             coords(j, tok0, voc0, vt);
             const int b = j & 1;
+            const int t = tok0 + r;
+            const bool row_ok = t < a.n_tok;
+            const int ncols = min(F2_BN, a.vocab - voc0);
+            const uint16_t *trow_g = nullptr;
+            float lt2 = 0.f;
+            if (DISTILL) {
+                trow_g = a.teacher + static_cast<int64_t>(row_ok ? t : 0) * a.vocab + voc0;
+                lt2 = row_ok ? static_cast<float>(a.tstat[t].x) : 0.f;
+                if (j + 1 < n_it) {
+                    // the next tile's teacher row segment (512 bytes) into L2
+                    int tk1, vc1, vt1;
+                    coords(j + 1, tk1, vc1, vt1);
+                    if (tk1 + r < a.n_tok) {
+                        const uint16_t *p = a.teacher + static_cast<int64_t>(tk1 + r) * a.vocab + vc1;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (vc1 + i * 64 < a.vocab) prefetch_l2(p + i * 64);
+                    }
+                }
+            }
             ok = mbar_wait(&tfull[b], (j >> 1) & 1, err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const int ncols = min(F2_BN, a.vocab - voc0);
-            const int t = tok0 + r;
-            const bool row_ok = t < a.n_tok;
-            const int rel = row_ok ? static_cast<int>(a.targets[t] - voc0) : -1;
             const uint32_t tbuf = trow + b * F2_BN;
-            float m2 = -INFINITY, z = 0.f;
+            float m2 = -INFINITY, z = 0.f, x = 0.f;
 #pragma unroll 1
             for (int q = 0; q < F2_BN / 32; ++q) {
                 if (q * 32 >= ncols) break;
                 uint32_t v[32];
                 tmem_ld32(tbuf + q * 32, v);
+                float bt[32];
+                if (DISTILL) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(trow_g + q * 32);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint4 w4 = (row_ok && q * 32 + c4 * 8 < ncols) ? __ldg(src + c4) : make_uint4(0, 0, 0, 0);
+                        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            bt[c4 * 8 + 2 * e] = __uint_as_float(ww[e] << 16) * kS;
+                            bt[c4 * 8 + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u) * kS;
+                        }
+                    }
+                }
                 tmem_ld_wait();
                 float f[32];
                 float cm = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    f[i] = (q * 32 + i < ncols) ? __uint_as_float(v[i]) * L2E : -INFINITY;
+                    f[i] = (q * 32 + i < ncols) ? __uint_as_float(v[i]) * kS : -INFINITY;
                     cm = fmaxf(cm, f[i]);
                 }
                 if (cm > m2) {
-                    z *= ex2_approx(m2 - cm);
+                    const float sc = ex2_approx(m2 - cm);
+                    z *= sc;
+                    if (DISTILL && a.direction == DIR_RKL) x *= sc;
                     m2 = cm;
                 }
-                float acc = 0.f;
+                float acc = 0.f, xa = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc += ex2_approx(f[i] - m2);
-                z += acc;
-                if (rel >= q * 32 && rel < q * 32 + 32) {
-                    float tv = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (rel - q * 32 == i) tv = __uint_as_float(v[i]);
-                    a.tgt[t] = tv;
+                for (int i = 0; i < 32; ++i) {
+                    const float e = ex2_approx(f[i] - m2);
+                    acc += e;
+                    if (DISTILL) {
+                        const bool in = q * 32 + i < ncols;
+                        if (a.direction == DIR_RKL) xa = fmaf(e, in ? f[i] - bt[i] : 0.f, xa);
+                        else xa = fmaf(in ? ex2_approx(bt[i] - lt2) : 0.f, in ? f[i] : 0.f, xa);
+                    }
                 }
+                z += acc;
+                x += xa;
             }
             if (row_ok) {
                 const int64_t o = static_cast<int64_t>(vt) * a.part_stride + t;
                 a.part[o] = m2;
                 a.part[a.part_plane + o] = z;
+                if (DISTILL) a.part[2 * a.part_plane + o] = x;
             }
             tc_fence_before();
             __syncwarp();
@@ -211,9 +255,10 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
     }
 }
 
-cudaError_t launch_fwd2(const TcArgs &a, int grid, cudaStream_t st)
+template <bool DISTILL> static cudaError_t launch_fwd2_one(const TcArgs &a, int grid, cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(fwd2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F2_SMEM);
+    auto k = fwd2_kernel<DISTILL>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F2_SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -227,7 +272,12 @@ cudaError_t launch_fwd2(const TcArgs &a, int grid, cudaStream_t st)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd2_kernel, a);
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+cudaError_t launch_fwd2(const TcArgs &a, bool distill, int grid, cudaStream_t st)
+{
+    return distill ? launch_fwd2_one<true>(a, grid, st) : launch_fwd2_one<false>(a, grid, st);
 }
 
 } // namespace lossk

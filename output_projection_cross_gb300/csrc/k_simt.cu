@@ -5,8 +5,10 @@
 //   merge_ce       per token: combine the per-tile (max, sum-exp) partials in
 //                  tile order into lse, then ce = lse - target logit and
 //                  z = lse^2 ("Fuse distillation + z-loss ...", "What it does")
-//   merge_distill  the same for the student/teacher pair and the three
-//                  distillation objectives, plus the backward parameters
+//   teacher_stats  per token, the teacher's log-sum-exp and sum p*logit over its
+//                  whole row: an HBM stream over the teacher logits
+//   merge_distill  the student's partials with the teacher's statistics, for
+//                  the three distillation objectives, plus the backward parameters
 //   reduce         fixed-shape double-precision tree over tokens -> the means
 //   tokp_ce        per-token backward parameters of the label loss
 //   sum_splits     d_hidden partials of the vocabulary splits, in split order
@@ -132,50 +134,169 @@ cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *
 }
 
 // ---------------------------------------------------------------------------
+// The teacher's own statistics (teacher_stats, one block per token row, an
+// HBM stream): in log2 units of b = teacher * log2(e) / T,
+//   lse_t2 = log2 sum_v 2^b   and   Eb = sum_v p_v b_v,  p = 2^(b - lse_t2),
+// so that sum p log p = ln2 (Eb - lse_t2).  Each thread keeps an online
+// (max, sum, weighted sum) over 16-byte groups of its row; the threads are then
+// merged by a fixed tree.  The sums are fp32 per thread for bf16 teachers and
+// fp64 for fp32 teachers (whose tolerance is 1e-6).
+template <typename T> struct TeachAcc { using type = float; };
+template <> struct TeachAcc<float> { using type = double; };
+
+template <typename T>
+__device__ __forceinline__ float teach_exp2(float x)
+{
+    if constexpr (sizeof(T) == 2) return ex2_approx(x);
+    else return exp2f(x);
+}
+
+// One warp per token row, all rows at once (no block-level merge and no
+// partial last wave of blocks): 8 x 16 bytes in flight per lane.
+template <typename T>
+__global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict__ teach, int64_t n, int64_t V,
+                                                           float kT, double2 *__restrict__ out)
+{
+    using A = typename TeachAcc<T>::type;
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int UNR = 8;
+    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= n) return;
+    const T *row = teach + t * V;
+    // Raw logits x, b = x kT.  M is the running maximum of b; E accumulates
+    // 2^(b - M) x (scaled by kT at the end), so each element costs one FFMA
+    // into the exponent, one exp2, one add and one FFMA.
+    float M = -INFINITY;
+    A Z = 0, E = 0;
+    auto absorb = [&](const float (&x)[VEC], int nv) {
+        float cm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i)
+            if (i < nv) cm = fmaxf(cm, x[i]);
+        cm *= kT;                                   // kT > 0: the maximum commutes with the scale
+        if (cm > M) {
+            const A f = static_cast<A>(teach_exp2<T>(M - cm));
+            Z *= f;
+            E *= f;
+            M = cm;
+        }
+#pragma unroll
+        for (int i = 0; i < VEC; ++i)
+            if (i < nv) {
+                const A e = static_cast<A>(teach_exp2<T>(fmaf(x[i], kT, -M)));
+                Z += e;
+                E += e * static_cast<A>(x[i]);
+            }
+    };
+    if constexpr (sizeof(T) == 2) {
+        // bf16: V % 8 == 0, so every row starts 16-byte aligned
+        const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+        const int64_t nvec = V / VEC;
+        for (int64_t v0 = lane; v0 < nvec; v0 += UNR * 32) {
+            uint4 w[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int64_t v = v0 + u * 32;
+                w[u] = v < nvec ? __ldg(r4 + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                if (v0 + u * 32 >= nvec) break;
+                const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                float x[VEC];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[2 * i] = __uint_as_float(q[i] << 16);
+                    x[2 * i + 1] = __uint_as_float(q[i] & 0xFFFF0000u);
+                }
+                absorb(x, VEC);
+            }
+        }
+    } else {
+        for (int64_t v0 = lane * VEC; v0 < V; v0 += 32 * VEC) {
+            float x[VEC];
+            const int nv = V - v0 < VEC ? static_cast<int>(V - v0) : VEC;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) x[i] = i < nv ? static_cast<float>(row[v0 + i]) : 0.f;
+            absorb(x, nv);
+        }
+    }
+    E *= static_cast<A>(kT);
+    // fixed xor tree over the lanes, in the accumulation type (fp64 is slow on
+    // this part, so bf16 rows merge in fp32)
+    for (int o = 16; o > 0; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const A zo = __shfl_xor_sync(0xffffffffu, Z, o), eo = __shfl_xor_sync(0xffffffffu, E, o);
+        const float Mn = fmaxf(M, Mo);
+        const A f1 = M == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(M - Mn));
+        const A f2 = Mo == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(Mo - Mn));
+        Z = Z * f1 + zo * f2;
+        E = E * f1 + eo * f2;
+        M = Mn;
+    }
+    if (lane == 0) {
+        const double Zd = static_cast<double>(Z);
+        out[t] = make_double2(static_cast<double>(M) + log2(Zd), static_cast<double>(E) / Zd);
+    }
+}
+
+cudaError_t launch_teacher_stats(int dtype_bf16, const void *teach, int64_t n, int64_t V, double temperature,
+                                 double2 *out, cudaStream_t st)
+{
+    const float kT = static_cast<float>(LOG2E / temperature);
+    const unsigned grid = static_cast<unsigned>((n + 7) / 8);
+    if (dtype_bf16)
+        teacher_stats_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(teach), n, V, kT, out);
+    else
+        teacher_stats_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(teach), n, V, kT, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Distillation merge.  Per (token, vocabulary tile) the forward wrote the
+// student's (m_c, z_c) in log2 units of a = s log2(e) / T and one cross term
+// x_c: CE and forward KL sum p a (the teacher's p exact); reverse KL sums
+// 2^(a - m_c) (a - b).  With lse_s2 = M + log2 sum z_c 2^(m_c - M) and the
+// teacher's (lse_t2, Eb), in natural units:
+//   CE   L = ln2 (lse_s2 - sum_c x_c)
+//   fKL  L = ln2 (Eb - lse_t2 - sum_c x_c + lse_s2)
+//   rKL  L = ln2 (sum_c x_c 2^(m_c - M) / Z_s - lse_s2 + lse_t2)
+// (the three definitions of "Fuse distillation + z-loss ...", "What it does",
+// with q = softmax(a), p = softmax(b)).  Tiles are combined in tile order, as
+// in merge_ce.
 __global__ void __launch_bounds__(32 * MG) merge_distill_kernel(
-    const float *__restrict__ part, const uint8_t *__restrict__ mask, int64_t n, int64_t n_ct,
-    int64_t n_pad, int direction, double wz, float *__restrict__ lse_out,
+    const float *__restrict__ part, const double2 *__restrict__ tstat, const uint8_t *__restrict__ mask,
+    int64_t n, int64_t n_ct, int64_t n_pad, int direction, double wz, float *__restrict__ lse_out,
     float *__restrict__ per_token, double *__restrict__ tokacc, float4 *__restrict__ tokp,
     double alpha, double temperature)
 {
-    __shared__ float smax[2][MG][32];
-    __shared__ double ssum[3][MG][32];
+    __shared__ float smax[MG][32];
+    __shared__ double ssum[2][MG][32];
     const int tx = threadIdx.x, g = threadIdx.y;
     const int64_t t = blockIdx.x * 32 + tx;
     const bool live = t < n;         // the grid covers exactly n_pad tokens
     const int64_t pl = n_ct * n_pad;
-    const float *ms = part, *zs = part + pl, *mt = part + 2 * pl, *zt = part + 3 * pl,
-                *xx = part + 4 * pl;
+    const float *ms = part, *zs = part + pl, *xx = part + 2 * pl;
     int64_t c0, c1;
     tile_range(n_ct, g, c0, c1);
-    float Ms = -INFINITY, Mt = -INFINITY;
+    float Ms = -INFINITY;
     if (live)
-        for (int64_t c = c0; c < c1; ++c) {
-            Ms = fmaxf(Ms, ms[c * n_pad + t]);
-            Mt = fmaxf(Mt, mt[c * n_pad + t]);
-        }
-    smax[0][g][tx] = Ms;
-    smax[1][g][tx] = Mt;
+        for (int64_t c = c0; c < c1; ++c) Ms = fmaxf(Ms, ms[c * n_pad + t]);
+    smax[g][tx] = Ms;
     __syncthreads();
-    Ms = smax[0][0][tx];
-    Mt = smax[1][0][tx];
-    for (int k = 1; k < MG; ++k) {
-        Ms = fmaxf(Ms, smax[0][k][tx]);
-        Mt = fmaxf(Mt, smax[1][k][tx]);
-    }
-    double Zs = 0.0, Zt = 0.0, X = 0.0;
+    Ms = smax[0][tx];
+    for (int k = 1; k < MG; ++k) Ms = fmaxf(Ms, smax[k][tx]);
+    double Zs = 0.0, X = 0.0;
     if (live)
         for (int64_t c = c0; c < c1; ++c) {
             const int64_t o = c * n_pad + t;
             const float fs = ex2_approx(ms[o] - Ms);
-            const float ft = ex2_approx(mt[o] - Mt);
             Zs += static_cast<double>(zs[o] * fs);
-            Zt += static_cast<double>(zt[o] * ft);
-            X += static_cast<double>(xx[o] * (direction == DIR_RKL ? fs : ft));
+            X += static_cast<double>(direction == DIR_RKL ? xx[o] * fs : xx[o]);
         }
     ssum[0][g][tx] = Zs;
-    ssum[1][g][tx] = Zt;
-    ssum[2][g][tx] = X;
+    ssum[1][g][tx] = X;
     __syncthreads();
     if (g != 0) return;
     if (!live) {
@@ -183,20 +304,19 @@ __global__ void __launch_bounds__(32 * MG) merge_distill_kernel(
         return;
     }
     Zs = ssum[0][0][tx];
-    Zt = ssum[1][0][tx];
-    X = ssum[2][0][tx];
+    X = ssum[1][0][tx];
     for (int k = 1; k < MG; ++k) {
         Zs += ssum[0][k][tx];
-        Zt += ssum[1][k][tx];
-        X += ssum[2][k][tx];
+        X += ssum[1][k][tx];
     }
-    const double lse_s = (static_cast<double>(Ms) + log2(Zs)) * LN2;
-    const double lse_t = (static_cast<double>(Mt) + log2(Zt)) * LN2;
-    const double E = LN2 * X / (direction == DIR_RKL ? Zs : Zt);
-    double L;
-    if (direction == DIR_CE) L = lse_s - E;
-    else if (direction == DIR_FKL) L = E + lse_s - lse_t;
-    else L = E - lse_s + lse_t;
+    const double lse_s2 = static_cast<double>(Ms) + log2(Zs);
+    const double2 ts = tstat[t];
+    const double lse_t2 = ts.x;
+    double L2;
+    if (direction == DIR_CE) L2 = lse_s2 - X;
+    else if (direction == DIR_FKL) L2 = ts.y - lse_t2 - X + lse_s2;
+    else L2 = X / Zs - lse_s2 + lse_t2;
+    const double L = L2 * LN2, lse_s = lse_s2 * LN2, lse_t = lse_t2 * LN2;
     const bool on = mask ? (mask[t] != 0) : true;
     const double Lm = on ? L : 0.0;
     const double z2 = on ? lse_s * lse_s : 0.0;
@@ -207,8 +327,8 @@ __global__ void __launch_bounds__(32 * MG) merge_distill_kernel(
     tokacc[2 * n_pad + t] = z2;
     const double at = on ? alpha / temperature : 0.0;
     float4 P;
-    P.x = static_cast<float>(lse_s * LOG2E);
-    P.y = static_cast<float>(lse_t * LOG2E);
+    P.x = static_cast<float>(lse_s2);
+    P.y = static_cast<float>(lse_t2);
     if (direction == DIR_RKL) {
         P.z = static_cast<float>(at);
         P.w = static_cast<float>(lse_t - lse_s - L + 2.0 * wz * lse_s);
@@ -219,13 +339,13 @@ __global__ void __launch_bounds__(32 * MG) merge_distill_kernel(
     tokp[t] = P;
 }
 
-cudaError_t launch_merge_distill(const float *part, const uint8_t *mask, int64_t n, int64_t n_ct,
-                                 int64_t n_pad, int direction, double wz, float *lse_out,
+cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const uint8_t *mask, int64_t n,
+                                 int64_t n_ct, int64_t n_pad, int direction, double wz, float *lse_out,
                                  float *per_token, double *tokacc, float4 *tokp, double alpha,
                                  double temperature, cudaStream_t st)
 {
     merge_distill_kernel<<<static_cast<unsigned>((n_pad + 31) / 32), dim3(32, MG), 0, st>>>(
-        part, mask, n, n_ct, n_pad, direction, wz, lse_out, per_token, tokacc, tokp, alpha,
+        part, tstat, mask, n, n_ct, n_pad, direction, wz, lse_out, per_token, tokacc, tokp, alpha,
         temperature);
     return cudaGetLastError();
 }
@@ -657,6 +777,7 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
                                                  int direction, float inv_t,
                                                  const int64_t *__restrict__ targets,
                                                  const float4 *__restrict__ tokp,
+                                                 const double2 *__restrict__ tstat,
                                                  float *__restrict__ part, float *__restrict__ tgt,
                                                  int64_t part_stride, int64_t part_plane,
                                                  float *__restrict__ out, int64_t out_split_stride)
@@ -747,41 +868,36 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
                             if (rel == jx) tgt[t] = s[i][jx];
                     }
                 } else {
-                    float a2[4], b2[4], ms = -INFINITY, mt = -INFINITY;
+                    // student (max, sum) of this tile and the direction's cross term:
+                    // CE / forward KL: sum p a with the teacher's p exact (its lse from
+                    // teacher_stats); reverse KL: sum 2^(a - max) (a - b)
+                    const float lt2 = t < n_tok ? static_cast<float>(tstat[t].x) : 0.f;
+                    float a2[4], b2[4], ms = -INFINITY;
 #pragma unroll
                     for (int jx = 0; jx < 4; ++jx) {
                         a2[jx] = vs[jx] * inv_t * L2E;
                         b2[jx] = vt[jx] * inv_t * L2E;
                         ms = fmaxf(ms, a2[jx]);
-                        mt = fmaxf(mt, b2[jx]);
                     }
-                    for (int o = 1; o < 16; o <<= 1) {
-                        ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
-                        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-                    }
-                    float zs = 0.f, zt = 0.f, xx = 0.f;
+                    for (int o = 1; o < 16; o <<= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+                    float zs = 0.f, xx = 0.f;
 #pragma unroll
                     for (int jx = 0; jx < 4; ++jx) {
                         if (vs[jx] == -INFINITY) continue;
-                        const float es = exp2f(a2[jx] - ms), et = exp2f(b2[jx] - mt);
+                        const float es = exp2f(a2[jx] - ms);
                         zs += es;
-                        zt += et;
-                        if (direction == DIR_CE) xx = fmaf(et, a2[jx], xx);
-                        else if (direction == DIR_FKL) xx = fmaf(et, b2[jx] - a2[jx], xx);
-                        else xx = fmaf(es, a2[jx] - b2[jx], xx);
+                        if (direction == DIR_RKL) xx = fmaf(es, a2[jx] - b2[jx], xx);
+                        else xx = fmaf(exp2f(b2[jx] - lt2), a2[jx], xx);
                     }
                     for (int o = 1; o < 16; o <<= 1) {
                         zs += __shfl_xor_sync(0xffffffffu, zs, o);
-                        zt += __shfl_xor_sync(0xffffffffu, zt, o);
                         xx += __shfl_xor_sync(0xffffffffu, xx, o);
                     }
                     if (t < n_tok && tx == 0) {
                         const int64_t o = static_cast<int64_t>(yt) * part_stride + t;
                         part[o] = ms;
                         part[part_plane + o] = zs;
-                        part[2 * part_plane + o] = mt;
-                        part[3 * part_plane + o] = zt;
-                        part[4 * part_plane + o] = xx;
+                        part[2 * part_plane + o] = xx;
                     }
                 }
             }
@@ -853,7 +969,8 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
 
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
-                      float inv_t, const int64_t *targets, const float4 *tokp, float *part,
+                      float inv_t, const int64_t *targets, const float4 *tokp, const double2 *tstat,
+                      float *part,
                       float *tgt, int64_t part_stride, int64_t part_plane, float *out,
                       int64_t out_split_stride, cudaStream_t st)
 {
@@ -865,7 +982,7 @@ cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, cons
     const float *x = static_cast<const float *>(X), *y = static_cast<const float *>(Y);
 #define LOSSK_FP(M, D)                                                                             \
     fp_kernel<M, D><<<grid, 256, 0, st>>>(x, y, teach, n_x, n_y, d, n_tok, vocab, n_split,       \
-                                          direction, inv_t, targets, tokp, part, tgt, part_stride, \
+                                          direction, inv_t, targets, tokp, tstat, part, tgt, part_stride, \
                                           part_plane, out, out_split_stride)
     if (mode == TC_STATS) {
         if (distill) LOSSK_FP(TC_STATS, true); else LOSSK_FP(TC_STATS, false);

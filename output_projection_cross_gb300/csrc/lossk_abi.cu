@@ -219,6 +219,12 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
     const WsLayout &L = w.L;
     cudaError_t e;
     if (dtype == LOSSK_BF16) {
+        {
+            Launch k(KK_TGT_LOGIT, st);
+            e = launch_tgt_logit(static_cast<const uint16_t *>(H), static_cast<const uint16_t *>(W), targets, n,
+                                 d, L.n_pad, w.tgt(), w.tokp(), st);
+        }
+        if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
         // CTA pairs: 256 tokens x 256 vocabulary per MMA, each CTA loading its
         // own 128 token rows and half (128 rows) of each vocabulary tile.
         TcArgs a;
@@ -241,12 +247,12 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
         a.err = &w.hdr()->err;
         const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
         Launch k(KK_TC_STATS, st);
-        e = launch_fwd2(a, 2 * pairs, st);
+        e = launch_fwd2(a, false, 2 * pairs, st);
     } else {
         Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, false, H, W, nullptr, static_cast<int>(n), static_cast<int>(V),
                       static_cast<int>(d), static_cast<int>(n), static_cast<int>(V), 1, 0, 1.f,
-                      targets, nullptr, w.part(), w.tgt(), L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
+                      targets, nullptr, nullptr, w.part(), w.tgt(), L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
@@ -305,7 +311,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
                 e = launch_fp(rows ? TC_ROWS : TC_COLS, distill, X, Y, static_cast<const float *>(teacher),
                           static_cast<int>(nx), static_cast<int>(ny), static_cast<int>(d),
                           static_cast<int>(n), static_cast<int>(V), static_cast<int>(nsplit),
-                          direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, 0, 0, out, n * d, st);
+                          direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, nullptr, 0, 0, out, n * d, st);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && nsplit > 1) {
@@ -440,7 +446,7 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     const bool tc = dtype == LOSSK_BF16;
     L->n_pad = cdiv(n, TC_BM) * TC_BM;
     const bool distill = kind == LOSSK_KIND_DISTILL;
-    L->bn = tc ? (distill ? TC_BN_ACC : TC_BN_FWD) : FP_BN;
+    L->bn = tc ? TC_BN_FWD : FP_BN;
     L->n_ct = cdiv(V, L->bn);
     L->nstat = distill ? NSTAT_DISTILL : NSTAT_CE;
     const bool fwd = kind == LOSSK_KIND_CE_FWD || kind == LOSSK_KIND_CE_FWD_BWD || distill;
@@ -466,6 +472,8 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (fused) off = align256(off + sizeof(float2) * L->n_pad);
     L->off_gring = off;
     if (bwd && tc) off = align256(off + sizeof(uint16_t) * 128 * static_cast<size_t>(G_RING_ROWS));
+    L->off_tstat = off;
+    if (distill) off = align256(off + sizeof(double2) * L->n_pad);
     L->off_red = off;
     off = align256(off + 64);
     L->total = off;
@@ -704,11 +712,18 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
     if (s != LOSSK_OK) return s;
     const WsLayout &L = w.L;
     cudaError_t e;
+    double2 *tstat = reinterpret_cast<double2 *>(w.base + L.off_tstat);
+    {
+        // the teacher's own statistics: one HBM stream over the teacher logits
+        Launch k(KK_TEACHER_STATS, st);
+        e = launch_teacher_stats(dtype == LOSSK_BF16, teacher, n, V, temperature, tstat, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     if (dtype == LOSSK_BF16) {
+        // CTA pairs, 256 tokens x 256 vocabulary per MMA, the teacher read in the epilogue
         TcArgs a;
         std::memset(&a, 0, sizeof(a));
-        if (!make_map(&a.map_x, hidden, d, n, 64, TC_BM) || !make_map(&a.map_y, weight, d, V, 64, TC_BN_ACC) ||
-            !make_map(&a.map_teach, teacher, V, n, 64, TC_BM))
+        if (!make_map(&a.map_x, hidden, d, n, 64, TC_BM) || !make_map(&a.map_y, weight, d, V, 64, 128))
             return LOSSK_DEVICE_ERROR;
         a.n_x = static_cast<int>(n);
         a.n_y = static_cast<int>(V);
@@ -717,28 +732,30 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
         a.vocab = static_cast<int>(V);
         a.n_xt = static_cast<int>(cdiv(n, TC_BM));
         a.n_yt = static_cast<int>(L.n_ct);
-        a.n_items = a.n_xt * a.n_yt;
+        a.n_items = static_cast<int>(cdiv(a.n_xt, 2)) * a.n_yt;
         a.direction = direction;
         a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
+        a.teacher = static_cast<const uint16_t *>(teacher);
+        a.tstat = tstat;
         a.part = w.part();
         a.part_stride = L.n_pad;
         a.part_plane = L.n_ct * L.n_pad;
         a.err = &w.hdr()->err;
-        const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+        const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
         Launch k(KK_TC_STATS, st);
-        e = launch_tc(TC_STATS, true, a, grid, st);
+        e = launch_fwd2(a, true, 2 * pairs, st);
     } else {
         Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, true, hidden, weight, static_cast<const float *>(teacher),
                       static_cast<int>(n), static_cast<int>(V), static_cast<int>(d), static_cast<int>(n),
                       static_cast<int>(V), 1, direction, static_cast<float>(1.0 / temperature), nullptr,
-                      nullptr, w.part(), nullptr, L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
+                      nullptr, tstat, w.part(), nullptr, L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
     {
         Launch k(KK_MERGE_DISTILL, st);
-        e = launch_merge_distill(w.part(), loss_mask, n, L.n_ct, L.n_pad, direction, z_weight,
+        e = launch_merge_distill(w.part(), tstat, loss_mask, n, L.n_ct, L.n_pad, direction, z_weight,
                                  lse_out, per_token_out, w.tokacc(), w.tokp(), alpha, temperature, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
@@ -773,7 +790,7 @@ const char *lossk_kernel_name(int32_t kind)
                                       "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
                                       "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
                                       "from_logits",  "tc_fused",      "tgt_logit",   "merge_fused",
-                                      "combine_dh"};
+                                      "combine_dh",   "teacher_stats"};
     return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
 }
 

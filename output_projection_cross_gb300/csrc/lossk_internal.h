@@ -14,7 +14,7 @@ constexpr double LOG2E = 1.44269504088896340736;
 // Tile geometry of the tensor-core path.
 constexpr int TC_BM = 128;         // rows of X per tile (MMA M, TMEM lanes)
 constexpr int TC_BN_FWD = 256;     // logit tile width of the label-CE forward
-constexpr int TC_BN_ACC = 128;     // logit tile width of the backward and distillation
+constexpr int TC_BN_ACC = 128;     // vocabulary tile width the d_hidden splits are counted in
 constexpr int TC_BK = 64;          // K per pipeline stage (one 128-byte swizzle row)
 constexpr int TC_SLICE = 256;      // d_model columns one backward CTA accumulates
 // Tile geometry of the fp32 FFMA path.
@@ -32,10 +32,10 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Per-(token, logit tile) partial statistics written by the forward pass
 // (structure of arrays, each [n_ct][n_pad]).  Label CE: m2 (running max of
-// logit*log2e) and z (sum of 2^(logit*log2e - m2)).  Distillation adds the
-// teacher's pair and one direction-dependent weighted sum.
+// logit*log2e) and z (sum of 2^(logit*log2e - m2)).  Distillation: the same
+// pair for logit/T and one direction-dependent cross term with the teacher.
 constexpr int NSTAT_CE = 2;
-constexpr int NSTAT_DISTILL = 5;
+constexpr int NSTAT_DISTILL = 3;
 
 struct WsLayout {
     int64_t n_pad = 0;       // n_tok rounded up to 128
@@ -51,6 +51,7 @@ struct WsLayout {
     size_t off_zpart = 0;    // float  [nsplit * 8][n_pad] fused pass: sums of G' per (split, CTA)
     size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
     size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the cluster passes
+    size_t off_tstat = 0;    // double2 [n_pad] distillation: teacher (lse_t2, Eb) per token
     size_t off_red = 0;      // double [8] reduction output scratch
     size_t total = 0;
 };
@@ -67,7 +68,6 @@ struct TcArgs {
     CUtensorMap map_x;     // X operand (K-major), box {64, 128}
     CUtensorMap map_y;     // Y operand (K-major), box {64, BN}
     CUtensorMap map_ys;    // Y rows x d-slice as the MN-major B operand, box {64, 64}
-    CUtensorMap map_teach; // teacher logits [n_tok][vocab], box {64, 128}
     int n_x;               // rows of X (n_tok in STATS/ROWS, vocab in COLS)
     int n_y;               // rows of Y
     int d;                 // contraction length (d_model)
@@ -80,6 +80,8 @@ struct TcArgs {
     int direction;         // distillation objective
     float inv_t_l2e;       // log2(e) / temperature
     const int64_t *targets;
+    const uint16_t *teacher; // distillation forward: teacher logits [n_tok][vocab] (bf16)
+    const double2 *tstat;  // distillation forward: per token (lse_t2, Eb) from teacher_stats
     const float4 *tokp;    // per-token backward parameters
     float *part;           // STATS output (structure of arrays)
     float *tgt;            // STATS (label CE): target logit per token
@@ -155,29 +157,33 @@ enum KernelKind : int {
     KK_TGT_LOGIT,
     KK_MERGE_FUSED,
     KK_COMBINE_DH,
+    KK_TEACHER_STATS,
     KK_N
 };
 
 // ---- launchers (all enqueue on `st`) -----------------------------------------
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);
-cudaError_t launch_tc(int mode, bool distill, const TcArgs &a, int grid, cudaStream_t st);
 // Persistent clusters: at most as many as fit at once, walking `n_units` units.
 cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int n_units, cudaStream_t st);
-cudaError_t launch_fwd2(const TcArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_fwd2(const TcArgs &a, bool distill, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
-                      float inv_t, const int64_t *targets, const float4 *tokp, float *part,
+                      float inv_t, const int64_t *targets, const float4 *tokp, const double2 *tstat,
+                      float *part,
                       float *tgt, int64_t part_stride, int64_t part_plane, float *out,
                       int64_t out_split_stride, cudaStream_t st);
 cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
                             const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
                             double wz, float *lse_out, float *ce_out, double *tokacc,
                             cudaStream_t st);
-cudaError_t launch_merge_distill(const float *part, const uint8_t *mask, int64_t n, int64_t n_ct,
-                                 int64_t n_pad, int direction, double wz, float *lse_out,
+cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const uint8_t *mask, int64_t n,
+                                 int64_t n_ct, int64_t n_pad, int direction, double wz, float *lse_out,
                                  float *per_token, double *tokacc, float4 *tokp, double alpha,
                                  double temperature, cudaStream_t st);
+// Teacher log-sum-exp and sum p*logit per token (one block per token row).
+cudaError_t launch_teacher_stats(int dtype_bf16, const void *teach, int64_t n, int64_t V, double temperature,
+                                 double2 *out, cudaStream_t st);
 cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
                           double wz, double *scalars_out, cudaStream_t st);
 cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,

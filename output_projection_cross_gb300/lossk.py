@@ -77,7 +77,7 @@ EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk
             "lossk_targets_check", "lossk_ce_fwd", "lossk_ce_bwd", "lossk_ce_fwd_bwd",
             "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status",
             "lossk_ce_from_logits_static", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
-N_KERNELS = 17
+N_KERNELS = 18
 
 
 class LosskError(RuntimeError):
