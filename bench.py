@@ -64,6 +64,10 @@ def args_parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--paths-only", action="store_true",
+                    help="time only the other rows of the path (distillation, CE from logits)")
+    ap.add_argument("--path-tokens", type=int, default=None,
+                    help="token count of the distillation workload in --paths-only mode")
     return ap.parse_args()
 
 
@@ -361,15 +365,20 @@ def _time(fn, reps, warm=2):
     return e0.elapsed_time(e1) / reps
 
 
-def extra_paths(L, dev, pk):
+def extra_paths(L, dev, pk, n_tok=None):
     """The other rows of the hot path, timed the same way: distillation at
-    n=4096, d=2048, V=151936 (T=2, 10% masked, z 1e-4) and cross-entropy from
-    materialised bf16 logits at the Qwen3 head shape (HBM stream)."""
+    n=4096, d=2048, V=151936 (T=2, 10% masked, z 1e-4; n_tok overrides the
+    token count) and cross-entropy from materialised bf16 logits at the Qwen3
+    head shape (HBM stream)."""
+    import dataclasses
+
     import torch
 
     import lossk_inputs as li
     res = {}
     w = li.WORKLOADS["distill_z_4096x2048"]
+    if n_tok is not None:
+        w = dataclasses.replace(w, n_tok=n_tok)
     x = li.make(w, seed=0)
     H = torch.from_numpy(x["hidden"]).to(dev).to(torch.bfloat16)
     W = torch.from_numpy(x["weight"]).to(dev).to(torch.bfloat16)
@@ -475,6 +484,14 @@ def main():
             print(json.dumps(res), flush=True)
         return
     rank, world, local = dist_init()
+    if a.paths_only:
+        import torch
+        import output_projection_cross_gb300 as L
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        if rank == 0:
+            print(json.dumps({"paths": extra_paths(L, dev, peaks(), a.path_tokens)}), flush=True)
+        return
     res = run_ours(a, rank, world, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
