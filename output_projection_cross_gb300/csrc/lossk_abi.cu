@@ -333,9 +333,40 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
 // less than the separate forward and d_hidden passes.  A row whose shifted
 // terms left the trusted range raises the workspace's redo word; the caller
 // then recomputes everything on the separate passes.
+// A helper stream per device: the training step's small kernels that nothing
+// after them waits for (the token mean, d_hidden's combine) run on it beside
+// the d_weight pass, on the SMs its clusters leave free; the call joins it back
+// into the caller's stream before it returns.
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ready()
+    {
+        if (s) return true;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            s = nullptr;
+            return false;
+        }
+        return true;
+    }
+};
+
+SideStream *side_stream()
+{
+    static SideStream sides[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    return &sides[dev];
+}
+
 int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
                   const int64_t *targets, const uint8_t *mask, double wz, double alpha,
-                  float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st)
+                  float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st,
+                  cudaStream_t aux, cudaEvent_t fork)
 {
     const WsLayout &L = w.L;
     const uint16_t *Hb = static_cast<const uint16_t *>(H), *Wb = static_cast<const uint16_t *>(W);
@@ -367,13 +398,17 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
                                wz, lse_out, ce_out, w.tokacc(), w.tokp(), w.dhc(), w.hdr(), st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    if (aux != st) {
+        if (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(aux, fork, 0) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
     {
-        Launch k(KK_REDUCE, st);
-        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st);
+        Launch k(KK_REDUCE, aux);
+        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, aux);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    Launch k(KK_COMBINE_DH, st);
-    return status_of(launch_combine_dh(part, L.nsplit, n, d, Wb, targets, w.dhc(), d_hidden, w.hdr(), st));
+    Launch k(KK_COMBINE_DH, aux);
+    return status_of(launch_combine_dh(part, L.nsplit, n, d, Wb, targets, w.dhc(), d_hidden, w.hdr(), aux));
 }
 
 // Checks shared by the fused calls, in the documented order up to 585.
@@ -589,9 +624,20 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     if (s != LOSSK_OK) return s;
     if (do_fwd && do_bwd && dH && dtype == LOSSK_BF16) {
         const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
-        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dH, st);
+        SideStream *sd = side_stream();
+        std::unique_lock<std::mutex> lk;
+        cudaStream_t aux = st;
+        if (sd) {
+            lk = std::unique_lock<std::mutex>(sd->mu);
+            if (sd->ready()) aux = sd->s;
+        }
+        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dH, st, aux,
+                      aux != st ? sd->fork : nullptr);
         if (s == LOSSK_OK && dW)
             s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st);
+        if (aux != st &&
+            (cudaEventRecord(sd->join, aux) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
+            return LOSSK_DEVICE_ERROR;
         if (s != LOSSK_OK) return s;
         // The call's second read-back: a device timeout, or a row the shifted
         // pass could not represent (then every output is recomputed by the
