@@ -38,7 +38,9 @@
  *    validation kernel, to read back the target-range flag and the number of
  *    counted tokens: the call refuses bad targets (586) before the main
  *    kernels run, the way the pages' functions validate first.  After that
- *    point the call returns without waiting for the GPU.
+ *    point the call returns without waiting for the GPU -- except the
+ *    training-step calls on the bf16 path (lossk_ce_fwd_bwd and its _ex
+ *    form), which read back one more flag at their end (see there).
  *  - Check order (the first failing check wins): 581 empty dimension, 583
  *    dimension over 2^24, 584 n_tok*d_model*vocab over 2^46, 587 chunk*vocab
  *    over 2^27, 582 length / NULL pointer / short workspace, 591 alignment,
@@ -86,8 +88,20 @@ enum lossk_status {
     LOSSK_UNKNOWN_OBJECTIVE = 588,
     LOSSK_DEVICE_ERROR = 589,   /* a CUDA call or launch failed */
     LOSSK_DEVICE_TIMEOUT = 590, /* a device-side wait hit its time limit */
-    LOSSK_UNALIGNED = 591       /* pointer or row pitch not 16-byte aligned */
+    LOSSK_UNALIGNED = 591,      /* pointer or row pitch not 16-byte aligned */
+    LOSSK_UNKNOWN_FLAGS = 592   /* a flags argument with a bit this library does not define */
 };
+
+/* Flags of the _ex entry points (bitwise or; 0 = the plain call's behaviour).
+ * LOSSK_ACCUMULATE_GRADS: gradients are added into d_hidden / d_weight /
+ *   grad_logits instead of overwriting them (gradient accumulation across
+ *   micro-batches).
+ * LOSSK_REDUCE_SUM: the reduction is a sum over the counted tokens instead of
+ *   their mean: total = sum_t m_t (loss_t + z_weight z_t), the other two
+ *   scalars are sums too, and a_t = grad_scale m_t (no 1/N_valid).
+ * Both follow the variants the pages list beside masking and scaling in the
+ * parity suite of "Fuse distillation + z-loss ...", "Testing". */
+enum lossk_flags { LOSSK_ACCUMULATE_GRADS = 1, LOSSK_REDUCE_SUM = 2 };
 
 enum lossk_dtype { LOSSK_F32 = 0, LOSSK_BF16 = 1 };
 
@@ -101,14 +115,15 @@ enum lossk_kind {
     LOSSK_KIND_CE_BWD = 1,
     LOSSK_KIND_CE_FWD_BWD = 2,
     LOSSK_KIND_FROM_LOGITS = 3,
-    LOSSK_KIND_DISTILL = 4
+    LOSSK_KIND_DISTILL = 4,
+    LOSSK_KIND_CE_CHUNK_CHECK = 5
 };
 
 /* ---- contract: host arithmetic, no device ------------------------------- */
 
 /* Name of a status code: "ok", "empty_dimension", ... for 580-588,
- * "device_error", "device_timeout", "unaligned" for 589-591, and
- * "unknown_status" for anything else (never a neighbour's name).
+ * "device_error", "device_timeout", "unaligned", "unknown_flags" for
+ * 589-592, and "unknown_status" for anything else (never a neighbour's name).
  * loss_status_name in the pages' function table.  Returns a static string. */
 const char *lossk_status_name(int32_t code);
 
@@ -191,7 +206,17 @@ int32_t lossk_ce_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int32_t dtyp
 
 /* lossk_ce_fwd followed by lossk_ce_bwd on the same inputs, with one
  * validation sync instead of two: the training-step call.  lse_out is
- * required (it is also the backward's input). */
+ * required (it is also the backward's input).
+ *
+ * On the bf16 path with d_hidden requested, the forward is folded into the
+ * d_hidden pass: every logit is exponentiated against a per-token reference
+ * shift r_t = target logit * log2(e) + 64 instead of the (not yet known)
+ * log-sum-exp, which saves one full logit pass.  A row whose maximum logit
+ * lies more than about 110 nats above its target logit would leave the range
+ * the shift covers; the call detects that (and any non-finite d_hidden) on
+ * the device, reads the flag back at its end (a second synchronisation of
+ * `stream`) and then recomputes every output on the separate passes.  The
+ * outputs are the same quantities either way, within the tolerances. */
 int32_t lossk_ce_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
                          int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight,
                          int64_t weight_len, const int64_t *targets, int64_t targets_len,
@@ -234,6 +259,60 @@ int32_t lossk_distill_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int
                               double *scalars_out, float *per_token_out, float *lse_out,
                               float *d_hidden, float *d_weight, void *workspace,
                               int64_t workspace_bytes, lossk_stream_t stream);
+
+/* lossk_ce_fwd_bwd with flags (lossk_flags).  With LOSSK_ACCUMULATE_GRADS
+ * the call adds into d_hidden and d_weight, and touches them only after the
+ * fused pass's range check has passed (so it synchronises `stream` once more
+ * in the middle).  Unknown flag bits give 592 (checked after 585). */
+int32_t lossk_ce_fwd_bwd_ex(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
+                            int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight,
+                            int64_t weight_len, const int64_t *targets, int64_t targets_len,
+                            const uint8_t *loss_mask, double z_weight, double grad_scale,
+                            uint32_t flags, float *lse_out, float *ce_out, double *scalars_out,
+                            float *d_hidden, float *d_weight, void *workspace, int64_t workspace_bytes,
+                            lossk_stream_t stream);
+
+/* lossk_distill_fwd_bwd with flags (lossk_flags). */
+int32_t lossk_distill_fwd_bwd_ex(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
+                                 int32_t dtype, const void *hidden, int64_t hidden_len,
+                                 const void *weight, int64_t weight_len, const void *teacher_logits,
+                                 int64_t teacher_len, const uint8_t *loss_mask, int32_t direction,
+                                 double temperature, double z_weight, double grad_scale, uint32_t flags,
+                                 double *scalars_out, float *per_token_out, float *lse_out,
+                                 float *d_hidden, float *d_weight, void *workspace,
+                                 int64_t workspace_bytes, lossk_stream_t stream);
+
+/* ce_chunk_invariance_flat ("Loss functions and resident-context kernels",
+ * lossk function table and "Chunk invariance is checked to the last bit"):
+ * runs lossk_ce_fwd at chunk = 1 and at chunk = n_tok and writes to the host
+ * double *max_abs_delta the largest absolute difference between the two
+ * runs over the three reduced scalars and every token's lse and ce (0.0 is
+ * the property).  When n_tok*vocab exceeds the 2^27 logit budget, the second
+ * chunk is the largest the budget allows (this library's reading: the check
+ * would otherwise be refused at every realistic size).  Workspace kind
+ * LOSSK_KIND_CE_CHUNK_CHECK.  Synchronises `stream`. */
+int32_t lossk_ce_chunk_invariance(int64_t n_tok, int64_t d_model, int64_t vocab, int32_t dtype,
+                                  const void *hidden, int64_t hidden_len, const void *weight,
+                                  int64_t weight_len, const int64_t *targets, int64_t targets_len,
+                                  const uint8_t *loss_mask, double z_weight, double *max_abs_delta,
+                                  void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
+/* Distillation from materialised student logits [n_tok][vocab] (the
+ * (loss, z_loss, grad_logits) shape of "Fuse distillation + z-loss ...",
+ * "Changes": the from-distribution forward/backward with its optional z
+ * slot).  Same objectives, temperature, mask, divisor and scalars as
+ * lossk_distill_fwd_bwd, with the student logits given instead of hidden and
+ * weight.  logits and teacher_logits share `dtype`; grad_logits (same dtype,
+ * or NULL to skip) receives grad_scale * d total / d logits.  flags as in
+ * lossk_flags (LOSSK_ACCUMULATE_GRADS adds into grad_logits).  An HBM
+ * stream: one block per token row.  Workspace kind LOSSK_KIND_FROM_LOGITS. */
+int32_t lossk_distill_from_logits(int64_t n_tok, int64_t vocab, int32_t dtype, const void *logits,
+                                  int64_t logits_len, const void *teacher_logits, int64_t teacher_len,
+                                  const uint8_t *loss_mask, int32_t direction, double temperature,
+                                  double z_weight, double grad_scale, uint32_t flags,
+                                  double *scalars_out, float *per_token_out, float *lse_out,
+                                  void *grad_logits, int64_t grad_len, void *workspace,
+                                  int64_t workspace_bytes, lossk_stream_t stream);
 
 /* Synchronises `stream`, then reports and clears the workspace's device
  * error word: 580 (none), 590 (a bounded device wait timed out) or 589. */
@@ -278,7 +357,7 @@ int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype,
  * events, adds their durations per kind into total_ms[kind] and
  * launches[kind] (host arrays of `cap` entries), and clears them if `reset`.
  * Returns the number of kinds written, or -1 on a CUDA error. */
-#define LOSSK_N_KERNELS 18
+#define LOSSK_N_KERNELS 19
 const char *lossk_kernel_name(int32_t kind);
 int64_t lossk_launch_count(void);
 int32_t lossk_profile_enable(int32_t on);

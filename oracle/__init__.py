@@ -68,6 +68,8 @@ def _load():
                                                    vp, vp, i64, vp]
             lib.oracle_distill.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i32, dbl, dbl,
                                            dbl, vp, vp, vp, vp, vp]
+            lib.oracle_distill_from_logits.argtypes = [vp, vp, vp, i64, i64, i32, dbl, dbl, dbl, i32,
+                                                        vp, vp, vp, vp]
             lib.oracle_distill_token_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, dbl,
                                                       dbl, dbl, vp, i64, vp, vp, vp]
             _lib = lib
@@ -228,6 +230,24 @@ def distill(H, W, teacher, direction, temperature=1.0, mask=None, chunk=None, z_
         raise OracleError(st)
     return {"per_token": per, "lse": lse, "total": scal[0], "distill_mean": scal[1],
             "z_mean": scal[2], "dH": dH, "dW": dW}
+
+
+def distill_from_logits(logits, teacher, direction, temperature=1.0, mask=None, z_weight=0.0,
+                        grad_scale=1.0, reduce_sum=False, want_grad=True):
+    """Distillation from given student logits [n][V] (see oracle_distill_from_logits)."""
+    X, Tt = _f32(logits), _f32(teacher)
+    n, V = X.shape
+    m = _mask(mask)
+    dirn = DIRECTIONS[direction] if isinstance(direction, str) else int(direction)
+    per, lse, scal = np.zeros(n), np.zeros(n), np.zeros(3)
+    grad = np.zeros((n, V)) if want_grad else None
+    st = _load().oracle_distill_from_logits(_p(X), _p(Tt), _p(m), n, V, dirn, temperature, z_weight,
+                                            grad_scale, 1 if reduce_sum else 0, _p(per), _p(lse),
+                                            _p(scal), _p(grad))
+    if st != 580:
+        raise OracleError(st)
+    return {"per_token": per, "lse": lse, "total": scal[0], "distill_mean": scal[1],
+            "z_mean": scal[2], "grad": grad}
 
 
 def distill_token_rows(H, W, teacher, direction, rows, temperature=1.0, mask=None,

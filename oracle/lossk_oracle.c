@@ -544,6 +544,70 @@ int oracle_distill(const float *H, const float *W, const float *teacher, const u
     return OR_OK;
 }
 
+/* ---- distillation from given student logits, [P3] "Changes" -------------
+ * The from-distribution forward/backward on materialised student logits
+ * (the (loss, z_loss, grad_logits) shape): per token the same L_t, lse(a)
+ * and gradient as oracle_distill, with s = logits[t] instead of H W^T.
+ * reduce_sum = 0: means over N_valid (as oracle_distill); 1: sums over the
+ * counted tokens, alpha_t = grad_scale m_t (this oracle's reading of the
+ * "sum" reduction the pages' parity suite lists beside masking and scaling).
+ * grad [n][V] may be NULL. */
+int oracle_distill_from_logits(const float *logits, const float *teacher, const uint8_t *mask,
+                               int64_t n, int64_t V, int direction, double T, double wz,
+                               double grad_scale, int reduce_sum, double *per_token,
+                               double *lse_out, double *scal, double *grad)
+{
+    if (n < 1 || V < 1) return OR_EMPTY_DIMENSION;
+    if (n > OR_MAX_DIM || V > OR_MAX_DIM) return OR_DIMENSION_TOO_LARGE;
+    if (!scalar_ok(wz) || wz < 0.0 || !scalar_ok(grad_scale) || !scalar_ok(T) || T <= 0.0)
+        return OR_NON_FINITE_SCALAR;
+    if (direction < 0 || direction > 2) return OR_UNKNOWN_OBJECTIVE;
+    int64_t nvalid = count_valid(mask, n);
+    double *zt = (double *)malloc(sizeof(double) * (size_t)n);
+    #pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)V);
+        double *a = (double *)malloc(sizeof(double) * (size_t)V);
+        double *b = (double *)malloc(sizeof(double) * (size_t)V);
+        double *g = grad ? (double *)malloc(sizeof(double) * (size_t)V) : NULL;
+        #pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            for (int64_t v = 0; v < V; ++v) s[v] = (double)logits[t * V + v];
+            double la;
+            double L = distill_row(s, teacher + t * V, V, direction, T, a, b, &la, g);
+            int on = mask ? (mask[t] != 0) : 1;
+            per_token[t] = on ? L : 0.0;
+            zt[t] = on ? la * la : 0.0;
+            lse_out[t] = la;
+            if (grad) {
+                double alpha = 0.0;
+                if (on) alpha = reduce_sum ? grad_scale : (nvalid > 0 ? grad_scale / (double)nvalid : 0.0);
+                for (int64_t v = 0; v < V; ++v) {
+                    double q = exp(a[v] - la);
+                    grad[t * V + v] = alpha * (g[v] + 2.0 * wz * la * q / T);
+                }
+            }
+        }
+        free(s); free(a); free(b); free(g);
+    }
+    double sum_tok = 0.0, sum_l = 0.0, sum_z = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        sum_tok += per_token[t] + wz * zt[t];
+        sum_l += per_token[t];
+        sum_z += zt[t];
+    }
+    free(zt);
+    double div = reduce_sum ? 1.0 : (double)nvalid;
+    if (!reduce_sum && nvalid == 0) {
+        scal[0] = scal[1] = scal[2] = 0.0;
+    } else {
+        scal[0] = sum_tok / div;
+        scal[1] = sum_l / div;
+        scal[2] = sum_z / div;
+    }
+    return OR_OK;
+}
+
 /* Sampled distillation rows: per listed token, L_t, lse(a) and the dH row. */
 int oracle_distill_token_rows(const float *H, const float *W, const float *teacher,
                               const uint8_t *mask, int64_t n, int64_t d, int64_t V,

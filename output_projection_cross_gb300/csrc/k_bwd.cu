@@ -555,6 +555,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 for (int h = 0; h < 2; ++h) {
                     const int col = slice0 + (q + h) * 32;
                     if (fixrow < n_rows && col < a.d) {
+                        if (a.accumulate) {
+                            // gradient accumulation: out += this unit's accumulator
+                            for (int i = 0; i < 32; ++i)
+                                if (col + i < a.d) v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) + dst[col + i]);
+                        }
                         if (col + 32 <= a.d) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 8) st_global_v8(dst + col + i, &v[h][i]);

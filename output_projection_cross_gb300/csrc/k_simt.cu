@@ -357,7 +357,7 @@ cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const 
 // every chunk, grid and run.
 __global__ void __launch_bounds__(1024) reduce_kernel(const double *__restrict__ tokacc, int64_t n,
                                                       int64_t n_pad, const WsHeader *hdr,
-                                                      double *__restrict__ out)
+                                                      double *__restrict__ out, int sum)
 {
     __shared__ double sh[3][1024];
     const int i = threadIdx.x;
@@ -374,15 +374,15 @@ __global__ void __launch_bounds__(1024) reduce_kernel(const double *__restrict__
     }
     if (i == 0) {
         const int nv = hdr->n_valid;
-        for (int s = 0; s < 3; ++s) out[s] = nv > 0 ? sh[s][0] / nv : 0.0;
+        for (int s = 0; s < 3; ++s) out[s] = sum ? sh[s][0] : (nv > 0 ? sh[s][0] / nv : 0.0);
     }
 }
 
 cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
-                          double wz, double *scalars_out, cudaStream_t st)
+                          double wz, double *scalars_out, cudaStream_t st, bool sum)
 {
     (void)wz;
-    reduce_kernel<<<1, 1024, 0, st>>>(tokacc, n, n_pad, hdr, scalars_out);
+    reduce_kernel<<<1, 1024, 0, st>>>(tokacc, n, n_pad, hdr, scalars_out, sum ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -414,7 +414,7 @@ cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8
 
 // ---------------------------------------------------------------------------
 __global__ void sum_splits_kernel(const float4 *__restrict__ part, int64_t nsplit, int64_t count4,
-                                  float4 *__restrict__ out)
+                                  float4 *__restrict__ out, int accumulate)
 {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -423,18 +423,22 @@ __global__ void sum_splits_kernel(const float4 *__restrict__ part, int64_t nspli
             const float4 v = part[s * count4 + i];
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
+        if (accumulate) {
+            const float4 o = out[i];
+            acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+        }
         out[i] = acc;
     }
 }
 
 cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
-                              cudaStream_t st)
+                              cudaStream_t st, bool accumulate)
 {
     const int64_t c4 = count / 4;  // count is a multiple of 4 (d_model % 8 == 0)
     int64_t grid = (c4 + 255) / 256;
     if (grid > 4096) grid = 4096;
     sum_splits_kernel<<<static_cast<int>(grid), 256, 0, st>>>(
-        reinterpret_cast<const float4 *>(part), nsplit, c4, reinterpret_cast<float4 *>(out));
+        reinterpret_cast<const float4 *>(part), nsplit, c4, reinterpret_cast<float4 *>(out), accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -763,6 +767,200 @@ cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *tar
 }
 
 // ---------------------------------------------------------------------------
+// Distillation from materialised student logits (the from-distribution
+// forward/backward with its z slot, "Fuse distillation + z-loss ...").  One
+// 512-thread block per token row.  Pass 1 streams the student and teacher
+// rows once and keeps, per thread, online (max, sum) pairs for a = s log2e/T
+// and b = t log2e/T plus the direction's cross sums; the threads merge by a
+// fixed tree.  Pass 2 (optional) re-reads both rows (kept in L2 by pass 1's
+// loads) and writes grad_logits.  Sums are fp32 for bf16 rows and fp64 for
+// fp32 rows (whose tolerance is 1e-6).
+template <typename A> struct DlState {
+    float ms, mt;        // running maxima of a and b
+    A zs, zt;            // sum 2^(a - ms), sum 2^(b - mt)
+    A xa, xb;            // CE/fKL: sum 2^(b - mt) a, sum 2^(b - mt) b
+    A xq;                // rKL: sum 2^(a - ms) (a - b)
+};
+
+template <typename T, typename A>
+__device__ __forceinline__ void dl_add(DlState<A> &S, float a, float b, int direction)
+{
+    if (a > S.ms) {
+        const A f = static_cast<A>(teach_exp2<T>(S.ms - a));
+        S.zs *= f;
+        S.xq *= f;
+        S.ms = a;
+    }
+    if (b > S.mt) {
+        const A f = static_cast<A>(teach_exp2<T>(S.mt - b));
+        S.zt *= f;
+        S.xa *= f;
+        S.xb *= f;
+        S.mt = b;
+    }
+    const A es = static_cast<A>(teach_exp2<T>(a - S.ms));
+    const A et = static_cast<A>(teach_exp2<T>(b - S.mt));
+    S.zs += es;
+    S.zt += et;
+    if (direction == DIR_RKL) {
+        S.xq += es * static_cast<A>(a - b);
+    } else {
+        S.xa += et * static_cast<A>(a);
+        S.xb += et * static_cast<A>(b);
+    }
+}
+
+template <typename T, typename A>
+__device__ __forceinline__ void dl_merge(DlState<A> &S, const DlState<A> &O)
+{
+    const float Ms = fmaxf(S.ms, O.ms), Mt = fmaxf(S.mt, O.mt);
+    const A f1 = S.ms == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(S.ms - Ms));
+    const A f2 = O.ms == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(O.ms - Ms));
+    const A g1 = S.mt == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(S.mt - Mt));
+    const A g2 = O.mt == -INFINITY ? A(0) : static_cast<A>(teach_exp2<T>(O.mt - Mt));
+    S.zs = S.zs * f1 + O.zs * f2;
+    S.xq = S.xq * f1 + O.xq * f2;
+    S.zt = S.zt * g1 + O.zt * g2;
+    S.xa = S.xa * g1 + O.xa * g2;
+    S.xb = S.xb * g1 + O.xb * g2;
+    S.ms = Ms;
+    S.mt = Mt;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) distill_logits_kernel(
+    const T *__restrict__ student, const T *__restrict__ teacher, const uint8_t *__restrict__ mask,
+    int64_t V, int direction, float kT, double wz, double at_on, double inv_t, float *__restrict__ lse_out,
+    float *__restrict__ per_token, double *__restrict__ tokacc, int64_t n_pad, T *__restrict__ grad,
+    int accumulate)
+{
+    using A = typename TeachAcc<T>::type;
+    constexpr int NV = Vec<T>::N;
+    const int64_t t = blockIdx.x;
+    const T *xs = student + t * V, *xt = teacher + t * V;
+    const bool vec_ok = ((V * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(student) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(teacher) % 16 == 0);
+    DlState<A> S{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
+    if (vec_ok) {
+        const int64_t nvec = V / NV;
+        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float fs[NV], ft[NV];
+            load_vec<T>(xs + i * NV, fs, grad != nullptr);
+            load_vec<T>(xt + i * NV, ft, grad != nullptr);
+#pragma unroll
+            for (int u = 0; u < NV; ++u) dl_add<T, A>(S, fs[u] * kT, ft[u] * kT, direction);
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < V; i += blockDim.x)
+            dl_add<T, A>(S, to_f(xs[i]) * kT, to_f(xt[i]) * kT, direction);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        DlState<A> O;
+        O.ms = __shfl_xor_sync(0xffffffffu, S.ms, o);
+        O.mt = __shfl_xor_sync(0xffffffffu, S.mt, o);
+        O.zs = __shfl_xor_sync(0xffffffffu, S.zs, o);
+        O.zt = __shfl_xor_sync(0xffffffffu, S.zt, o);
+        O.xa = __shfl_xor_sync(0xffffffffu, S.xa, o);
+        O.xb = __shfl_xor_sync(0xffffffffu, S.xb, o);
+        O.xq = __shfl_xor_sync(0xffffffffu, S.xq, o);
+        dl_merge<T, A>(S, O);
+    }
+    __shared__ DlState<A> sw[16];
+    __shared__ float sP[4];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) sw[w] = S;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        DlState<A> R = sw[0];
+        for (int k = 1; k < 16; ++k) dl_merge<T, A>(R, sw[k]);
+        const double lse_s2 = static_cast<double>(R.ms) + log2(static_cast<double>(R.zs));
+        const double lse_t2 = static_cast<double>(R.mt) + log2(static_cast<double>(R.zt));
+        const double pa = static_cast<double>(R.xa) / static_cast<double>(R.zt);
+        const double pb = static_cast<double>(R.xb) / static_cast<double>(R.zt);
+        const double qx = static_cast<double>(R.xq) / static_cast<double>(R.zs);
+        double L2;
+        if (direction == DIR_CE) L2 = lse_s2 - pa;
+        else if (direction == DIR_FKL) L2 = pb - lse_t2 - pa + lse_s2;
+        else L2 = qx - lse_s2 + lse_t2;
+        const double L = L2 * LN2, lse_s = lse_s2 * LN2, lse_t = lse_t2 * LN2;
+        const bool on = mask ? (mask[t] != 0) : true;
+        const double Lm = on ? L : 0.0, z2 = on ? lse_s * lse_s : 0.0;
+        if (lse_out) lse_out[t] = static_cast<float>(lse_s);
+        if (per_token) per_token[t] = static_cast<float>(Lm);
+        tokacc[t] = Lm + wz * z2;
+        tokacc[n_pad + t] = Lm;
+        tokacc[2 * n_pad + t] = z2;
+        const double at = on ? at_on * inv_t : 0.0;
+        sP[0] = static_cast<float>(lse_s2);
+        sP[1] = static_cast<float>(lse_t2);
+        if (direction == DIR_RKL) {
+            sP[2] = static_cast<float>(at);
+            sP[3] = static_cast<float>(lse_t - lse_s - L + 2.0 * wz * lse_s);
+        } else {
+            sP[2] = static_cast<float>(at * (1.0 + 2.0 * wz * lse_s));
+            sP[3] = static_cast<float>(at);
+        }
+    }
+    if (!grad) return;
+    __syncthreads();
+    const float ls2 = sP[0], lt2 = sP[1], pz = sP[2], pw = sP[3];
+    const float ln2f = static_cast<float>(LN2);
+    auto gval = [&](float a, float b) {
+        const float qv = teach_exp2<T>(a - ls2);
+        return direction == DIR_RKL ? pz * qv * fmaf(a - b, ln2f, pw)
+                                    : pz * qv - pw * teach_exp2<T>(b - lt2);
+    };
+    T *g = grad + t * V;
+    if (vec_ok) {
+        const int64_t nvec = V / NV;
+        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float fs[NV], ft[NV], gv[NV];
+            load_vec<T>(xs + i * NV, fs, false);
+            load_vec<T>(xt + i * NV, ft, false);
+            if (accumulate) load_vec<T>(g + i * NV, gv, false);
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const float v = gval(fs[u] * kT, ft[u] * kT);
+                gv[u] = accumulate ? gv[u] + v : v;
+            }
+            store_vec(g + i * NV, gv);
+        }
+        return;
+    }
+    for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
+        float v = gval(to_f(xs[i]) * kT, to_f(xt[i]) * kT);
+        if (accumulate) v += to_f(g[i]);
+        if constexpr (sizeof(T) == 4) {
+            g[i] = v;
+        } else {
+            const uint32_t u = pack_bf16x2(v, 0.f);
+            g[i] = static_cast<uint16_t>(u & 0xFFFFu);
+        }
+    }
+}
+
+cudaError_t launch_distill_logits(int dtype_bf16, const void *student, const void *teacher, const uint8_t *mask,
+                                  int64_t n, int64_t V, int direction, double temperature, double wz,
+                                  double at_on, float *lse_out, float *per_token, double *tokacc,
+                                  int64_t n_pad, void *grad, bool accumulate, cudaStream_t st)
+{
+    const float kT = static_cast<float>(LOG2E / temperature);
+    if (dtype_bf16)
+        distill_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const uint16_t *>(student), static_cast<const uint16_t *>(teacher), mask, V, direction,
+            kT, wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<uint16_t *>(grad),
+            accumulate ? 1 : 0);
+    else
+        distill_logits_kernel<float><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const float *>(student), static_cast<const float *>(teacher), mask, V, direction, kT,
+            wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<float *>(grad),
+            accumulate ? 1 : 0);
+    return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------
 // fp32 FFMA path.  256 threads (16 x 16), 64 x 64 logit tiles, 4 x 4 per
 // thread; the contraction over d_model is staged through shared memory in
 // steps of 16 and summed in ascending k.  Modes mirror the tensor-core
@@ -780,7 +978,8 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
                                                  const double2 *__restrict__ tstat,
                                                  float *__restrict__ part, float *__restrict__ tgt,
                                                  int64_t part_stride, int64_t part_plane,
-                                                 float *__restrict__ out, int64_t out_split_stride)
+                                                 float *__restrict__ out, int64_t out_split_stride,
+                                                 int accumulate)
 {
     __shared__ float xs[FP_BK][FP_BM + 4];
     __shared__ float ys[FP_BK][FP_BN + 4];
@@ -961,7 +1160,10 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
 #pragma unroll
             for (int jx = 0; jx < 4; ++jx) {
                 const int c = slice * FP_SLICE + tx * 4 + jx;
-                if (c < d) o[static_cast<int64_t>(xr) * d + c] = acc[i][jx];
+                if (c < d) {
+                    float *p = o + static_cast<int64_t>(xr) * d + c;
+                    *p = accumulate ? *p + acc[i][jx] : acc[i][jx];
+                }
             }
         }
     }
@@ -972,7 +1174,7 @@ cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, cons
                       float inv_t, const int64_t *targets, const float4 *tokp, const double2 *tstat,
                       float *part,
                       float *tgt, int64_t part_stride, int64_t part_plane, float *out,
-                      int64_t out_split_stride, cudaStream_t st)
+                      int64_t out_split_stride, cudaStream_t st, bool accumulate)
 {
     const int n_xt = (n_x + FP_BM - 1) / FP_BM, n_yt = (n_y + FP_BN - 1) / FP_BN;
     const int n_sl = (d + FP_SLICE - 1) / FP_SLICE;
@@ -983,7 +1185,7 @@ cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, cons
 #define LOSSK_FP(M, D)                                                                             \
     fp_kernel<M, D><<<grid, 256, 0, st>>>(x, y, teach, n_x, n_y, d, n_tok, vocab, n_split,       \
                                           direction, inv_t, targets, tokp, tstat, part, tgt, part_stride, \
-                                          part_plane, out, out_split_stride)
+                                          part_plane, out, out_split_stride, accumulate ? 1 : 0)
     if (mode == TC_STATS) {
         if (distill) LOSSK_FP(TC_STATS, true); else LOSSK_FP(TC_STATS, false);
     } else if (mode == TC_ROWS) {

@@ -181,6 +181,7 @@ struct Ws {
     float *zpart() const { return reinterpret_cast<float *>(base + L.off_zpart); }
     float2 *dhc() const { return reinterpret_cast<float2 *>(base + L.off_dhc); }
     uint16_t *gring() const { return reinterpret_cast<uint16_t *>(base + L.off_gring); }
+    float *dhacc() const { return reinterpret_cast<float *>(base + L.off_dhacc); }
 };
 
 // Tensor maps and shape fields of a cluster pass.  rows: d_hidden / fused
@@ -214,7 +215,7 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
 // ---- the forward statistics pass + merge + reduction (label CE) ------------
 int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
                    const void *W, const int64_t *targets, const uint8_t *mask, double wz,
-                   float *lse_out, float *ce_out, double *scalars, cudaStream_t st)
+                   float *lse_out, float *ce_out, double *scalars, cudaStream_t st, bool sum = false)
 {
     const WsLayout &L = w.L;
     cudaError_t e;
@@ -262,13 +263,13 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     Launch k(KK_REDUCE, st);
-    return status_of(launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st));
+    return status_of(launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, st, sum));
 }
 
 // ---- the two accumulate passes (d_hidden, d_weight), label CE or distill ----
 int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
                 const void *W, const void *teacher, bool distill, int direction, double temperature,
-                float *d_hidden, float *d_weight, cudaStream_t st)
+                float *d_hidden, float *d_weight, cudaStream_t st, bool accumulate = false)
 {
     const WsLayout &L = w.L;
     cudaError_t e = cudaSuccess;
@@ -285,6 +286,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.direction = direction;
             a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
+            a.accumulate = (accumulate && a.out == dst) ? 1 : 0;
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
@@ -293,7 +295,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {
                 Launch k(KK_SUM_SPLITS, st);
-                e = launch_sum_splits(w.dhpart(), L.nsplit, n * d, d_hidden, st);
+                e = launch_sum_splits(w.dhpart(), L.nsplit, n * d, d_hidden, st, accumulate);
                 if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             }
         }
@@ -311,12 +313,13 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
                 e = launch_fp(rows ? TC_ROWS : TC_COLS, distill, X, Y, static_cast<const float *>(teacher),
                           static_cast<int>(nx), static_cast<int>(ny), static_cast<int>(d),
                           static_cast<int>(n), static_cast<int>(V), static_cast<int>(nsplit),
-                          direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, nullptr, 0, 0, out, n * d, st);
+                          direction, inv_t, nullptr, w.tokp(), nullptr, nullptr, nullptr, 0, 0, out, n * d, st,
+                          accumulate && out == dst);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && nsplit > 1) {
                 Launch k(KK_SUM_SPLITS, st);
-                e = launch_sum_splits(w.dhpart(), nsplit, n * d, d_hidden, st);
+                e = launch_sum_splits(w.dhpart(), nsplit, n * d, d_hidden, st, accumulate);
                 if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             }
         }
@@ -366,7 +369,7 @@ SideStream *side_stream()
 int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
                   const int64_t *targets, const uint8_t *mask, double wz, double alpha,
                   float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st,
-                  cudaStream_t aux, cudaEvent_t fork)
+                  cudaStream_t aux, cudaEvent_t fork, bool sum)
 {
     const WsLayout &L = w.L;
     const uint16_t *Hb = static_cast<const uint16_t *>(H), *Wb = static_cast<const uint16_t *>(W);
@@ -404,7 +407,7 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     }
     {
         Launch k(KK_REDUCE, aux);
-        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, aux);
+        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), wz, scalars, aux, sum);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     Launch k(KK_COMBINE_DH, aux);
@@ -481,10 +484,11 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     const bool tc = dtype == LOSSK_BF16;
     L->n_pad = cdiv(n, TC_BM) * TC_BM;
     const bool distill = kind == LOSSK_KIND_DISTILL;
+    const bool chk = kind == LOSSK_KIND_CE_CHUNK_CHECK;   // a forward's layout, then the two runs' outputs
     L->bn = tc ? TC_BN_FWD : FP_BN;
     L->n_ct = cdiv(V, L->bn);
     L->nstat = distill ? NSTAT_DISTILL : NSTAT_CE;
-    const bool fwd = kind == LOSSK_KIND_CE_FWD || kind == LOSSK_KIND_CE_FWD_BWD || distill;
+    const bool fwd = kind == LOSSK_KIND_CE_FWD || kind == LOSSK_KIND_CE_FWD_BWD || distill || chk;
     const bool bwd = kind == LOSSK_KIND_CE_BWD || kind == LOSSK_KIND_CE_FWD_BWD || distill;
     L->nsplit = bwd ? dh_splits(n, d, V, dtype) : 1;
     size_t off = 256;
@@ -509,8 +513,12 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (bwd && tc) off = align256(off + sizeof(uint16_t) * 128 * static_cast<size_t>(G_RING_ROWS));
     L->off_tstat = off;
     if (distill) off = align256(off + sizeof(double2) * L->n_pad);
+    L->off_dhacc = off;
+    if (fused) off = align256(off + sizeof(float) * static_cast<size_t>(n) * static_cast<size_t>(d));
     L->off_red = off;
     off = align256(off + 64);
+    L->off_chk = off;      // = the total of a forward's layout
+    if (chk) off = align256(off + sizeof(float) * 4 * L->n_pad + sizeof(double) * 8);
     L->total = off;
     return true;
 }
@@ -535,6 +543,7 @@ const char *lossk_status_name(int32_t code)
     case 589: return "device_error";
     case 590: return "device_timeout";
     case 591: return "unaligned";
+    case 592: return "unknown_flags";
     default: return "unknown_status";
     }
 }
@@ -608,7 +617,7 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
                          int64_t wl, const int64_t *targets, int64_t tl, const uint8_t *mask,
                          double wz, double gs, float *lse_io, int64_t lse_len, float *ce_out,
                          double *scalars, float *dH, float *dW, void *workspace, int64_t wsb,
-                         lossk_stream_t stream)
+                         lossk_stream_t stream, uint32_t flags = 0)
 {
     const int kind = do_fwd && do_bwd ? LOSSK_KIND_CE_FWD_BWD : (do_fwd ? LOSSK_KIND_CE_FWD : LOSSK_KIND_CE_BWD);
     Ws w;
@@ -617,23 +626,30 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     if (!targets || tl < n || !lse_io || lse_len < n) return LOSSK_LENGTH_MISMATCH;
     if (do_fwd && !scalars) return LOSSK_LENGTH_MISMATCH;
     if (!scalars_ok(wz, gs)) return LOSSK_NON_FINITE_SCALAR;
+    if (flags & ~static_cast<uint32_t>(LOSSK_ACCUMULATE_GRADS | LOSSK_REDUCE_SUM)) return LOSSK_UNKNOWN_FLAGS;
+    const bool acc = (flags & LOSSK_ACCUMULATE_GRADS) != 0, sum = (flags & LOSSK_REDUCE_SUM) != 0;
     w.base = static_cast<uint8_t *>(workspace);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Hdr h;
     s = validate(targets, mask, n, V, w.hdr(), st, &h);
     if (s != LOSSK_OK) return s;
+    // gradient of grad_scale * total: a_t = grad_scale m_t / N_valid (mean) or grad_scale m_t (sum)
+    const double alpha = sum ? gs : (h.n_valid > 0 ? gs / h.n_valid : 0.0);
     if (do_fwd && do_bwd && dH && dtype == LOSSK_BF16) {
-        const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
-        SideStream *sd = side_stream();
+        // With accumulation, d_hidden is formed in the workspace and the
+        // caller's gradients are touched only once the fused pass's range
+        // check has come back clean.
+        float *dh_fused = acc ? w.dhacc() : dH;
+        SideStream *sd = acc ? nullptr : side_stream();
         std::unique_lock<std::mutex> lk;
         cudaStream_t aux = st;
         if (sd) {
             lk = std::unique_lock<std::mutex>(sd->mu);
             if (sd->ready()) aux = sd->s;
         }
-        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dH, st, aux,
-                      aux != st ? sd->fork : nullptr);
-        if (s == LOSSK_OK && dW)
+        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dh_fused, st, aux,
+                      aux != st ? sd->fork : nullptr, sum);
+        if (s == LOSSK_OK && dW && !acc)
             s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st);
         if (aux != st &&
             (cudaEventRecord(sd->join, aux) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
@@ -642,25 +658,32 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
         // The call's second read-back: a device timeout, or a row the shifted
         // pass could not represent (then every output is recomputed by the
         // separate passes below, which need no shift).
-        int flags[4] = {0, 0, 0, 0};
-        if (cudaMemcpyAsync(flags, w.hdr(), sizeof(flags), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        int flags_d[4] = {0, 0, 0, 0};
+        if (cudaMemcpyAsync(flags_d, w.hdr(), sizeof(flags_d), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
             cudaStreamSynchronize(st) != cudaSuccess)
             return LOSSK_DEVICE_ERROR;
-        if (flags[0]) return LOSSK_DEVICE_TIMEOUT;
-        if (!flags[3]) return LOSSK_OK;
+        if (flags_d[0]) return LOSSK_DEVICE_TIMEOUT;
+        if (!flags_d[3]) {
+            if (!acc) return LOSSK_OK;
+            {
+                Launch k(KK_SUM_SPLITS, st);
+                if (launch_sum_splits(w.dhacc(), 1, n * d, dH, st, true) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+            }
+            if (dW) return run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st, true);
+            return LOSSK_OK;
+        }
     }
     if (do_fwd) {
-        s = run_ce_fwd(w, n, d, V, dtype, H, W, targets, mask, wz, lse_io, ce_out, scalars, st);
+        s = run_ce_fwd(w, n, d, V, dtype, H, W, targets, mask, wz, lse_io, ce_out, scalars, st, sum);
         if (s != LOSSK_OK) return s;
     }
     if (do_bwd && (dH || dW)) {
-        const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
         {
             Launch k(KK_TOKP, st);
             if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, alpha, wz, w.tokp(), st) != cudaSuccess)
                 return LOSSK_DEVICE_ERROR;
         }
-        s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st);
+        s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st, acc);
     }
     return s;
 }
@@ -699,6 +722,18 @@ int32_t lossk_ce_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t
                      scalars_out, d_hidden, d_weight, workspace, workspace_bytes, stream);
 }
 
+int32_t lossk_ce_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
+                            const void *hidden, int64_t hidden_len, const void *weight, int64_t weight_len,
+                            const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                            double z_weight, double grad_scale, uint32_t flags, float *lse_out, float *ce_out,
+                            double *scalars_out, float *d_hidden, float *d_weight, void *workspace,
+                            int64_t workspace_bytes, lossk_stream_t stream)
+{
+    return ce_common(true, true, n, d, V, chunk, true, dtype, hidden, hidden_len, weight, weight_len,
+                     targets, targets_len, loss_mask, z_weight, grad_scale, lse_out, n, ce_out,
+                     scalars_out, d_hidden, d_weight, workspace, workspace_bytes, stream, flags);
+}
+
 int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, int64_t logits_len,
                              const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
                              double z_weight, double grad_scale, float *lse_out, float *ce_out,
@@ -734,13 +769,13 @@ int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *lo
     return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st));
 }
 
-int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
-                              const void *hidden, int64_t hidden_len, const void *weight,
-                              int64_t weight_len, const void *teacher, int64_t teacher_len,
-                              const uint8_t *loss_mask, int32_t direction, double temperature,
-                              double z_weight, double grad_scale, double *scalars_out,
-                              float *per_token_out, float *lse_out, float *d_hidden, float *d_weight,
-                              void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
+                                 const void *hidden, int64_t hidden_len, const void *weight,
+                                 int64_t weight_len, const void *teacher, int64_t teacher_len,
+                                 const uint8_t *loss_mask, int32_t direction, double temperature,
+                                 double z_weight, double grad_scale, uint32_t flags, double *scalars_out,
+                                 float *per_token_out, float *lse_out, float *d_hidden, float *d_weight,
+                                 void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
 {
     Ws w;
     int32_t s = check_fused(n, d, V, chunk, true, dtype, hidden, hidden_len, weight, weight_len,
@@ -751,6 +786,8 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
     if (!scalars_ok(z_weight, grad_scale) || !is_finite(temperature) || temperature <= 0.0)
         return LOSSK_NON_FINITE_SCALAR;
     if (direction < LOSSK_DISTILL_CE || direction > LOSSK_DISTILL_REV_KL) return LOSSK_UNKNOWN_OBJECTIVE;
+    if (flags & ~static_cast<uint32_t>(LOSSK_ACCUMULATE_GRADS | LOSSK_REDUCE_SUM)) return LOSSK_UNKNOWN_FLAGS;
+    const bool acc = (flags & LOSSK_ACCUMULATE_GRADS) != 0, sum = (flags & LOSSK_REDUCE_SUM) != 0;
     w.base = static_cast<uint8_t *>(workspace);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Hdr h;
@@ -798,7 +835,7 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
                       nullptr, tstat, w.part(), nullptr, L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
+    const double alpha = sum ? grad_scale : (h.n_valid > 0 ? grad_scale / h.n_valid : 0.0);
     {
         Launch k(KK_MERGE_DISTILL, st);
         e = launch_merge_distill(w.part(), tstat, loss_mask, n, L.n_ct, L.n_pad, direction, z_weight,
@@ -807,12 +844,111 @@ int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, in
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
         Launch k(KK_REDUCE, st);
-        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), z_weight, scalars_out, st);
+        e = launch_reduce(w.tokacc(), n, L.n_pad, w.hdr(), z_weight, scalars_out, st, sum);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     if (!d_hidden && !d_weight) return LOSSK_OK;
     return run_acc(w, n, d, V, dtype, hidden, weight, teacher, true, direction, temperature, d_hidden,
-                   d_weight, st);
+                   d_weight, st, acc);
+}
+
+int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
+                              const void *hidden, int64_t hidden_len, const void *weight,
+                              int64_t weight_len, const void *teacher, int64_t teacher_len,
+                              const uint8_t *loss_mask, int32_t direction, double temperature,
+                              double z_weight, double grad_scale, double *scalars_out,
+                              float *per_token_out, float *lse_out, float *d_hidden, float *d_weight,
+                              void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    return lossk_distill_fwd_bwd_ex(n, d, V, chunk, dtype, hidden, hidden_len, weight, weight_len, teacher,
+                                    teacher_len, loss_mask, direction, temperature, z_weight, grad_scale, 0,
+                                    scalars_out, per_token_out, lse_out, d_hidden, d_weight, workspace,
+                                    workspace_bytes, stream);
+}
+
+int32_t lossk_distill_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, int64_t logits_len,
+                                  const void *teacher, int64_t teacher_len, const uint8_t *loss_mask,
+                                  int32_t direction, double temperature, double z_weight, double grad_scale,
+                                  uint32_t flags, double *scalars_out, float *per_token_out, float *lse_out,
+                                  void *grad_logits, int64_t grad_len, void *workspace, int64_t workspace_bytes,
+                                  lossk_stream_t stream)
+{
+    int32_t s = lossk_dims_check(n, 1, V);
+    if (s != LOSSK_OK) return s;
+    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (!logits || !teacher || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
+    if (logits_len < n * V || teacher_len < n * V || (grad_logits && grad_len < n * V))
+        return LOSSK_LENGTH_MISMATCH;
+    Ws w;
+    if (!ws_layout(LOSSK_KIND_FROM_LOGITS, n, 1, V, dtype, &w.L) || workspace_bytes < static_cast<int64_t>(w.L.total))
+        return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(logits) || !aligned16(teacher) || (grad_logits && !aligned16(grad_logits)) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return LOSSK_UNALIGNED;
+    if (!scalars_ok(z_weight, grad_scale) || !is_finite(temperature) || temperature <= 0.0)
+        return LOSSK_NON_FINITE_SCALAR;
+    if (direction < LOSSK_DISTILL_CE || direction > LOSSK_DISTILL_REV_KL) return LOSSK_UNKNOWN_OBJECTIVE;
+    if (flags & ~static_cast<uint32_t>(LOSSK_ACCUMULATE_GRADS | LOSSK_REDUCE_SUM)) return LOSSK_UNKNOWN_FLAGS;
+    const bool acc = (flags & LOSSK_ACCUMULATE_GRADS) != 0, sum = (flags & LOSSK_REDUCE_SUM) != 0;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    s = validate(nullptr, loss_mask, n, V, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    const double at_on = sum ? grad_scale : (h.n_valid > 0 ? grad_scale / h.n_valid : 0.0);
+    cudaError_t e;
+    {
+        Launch k(KK_DISTILL_LOGITS, st);
+        e = launch_distill_logits(dtype == LOSSK_BF16, logits, teacher, loss_mask, n, V, direction, temperature,
+                                  z_weight, at_on, lse_out, per_token_out, w.tokacc(), w.L.n_pad, grad_logits,
+                                  acc, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    Launch k(KK_REDUCE, st);
+    return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st, sum));
+}
+
+int32_t lossk_ce_chunk_invariance(int64_t n, int64_t d, int64_t V, int32_t dtype, const void *hidden,
+                                  int64_t hidden_len, const void *weight, int64_t weight_len,
+                                  const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                                  double z_weight, double *max_abs_delta, void *workspace,
+                                  int64_t workspace_bytes, lossk_stream_t stream)
+{
+    int32_t s = lossk_dims_check(n, d, V);
+    if (s != LOSSK_OK) return s;
+    if (!max_abs_delta) return LOSSK_LENGTH_MISMATCH;
+    WsLayout L;
+    if (!ws_layout(LOSSK_KIND_CE_CHUNK_CHECK, n, d, V, dtype, &L) || workspace_bytes < static_cast<int64_t>(L.total) ||
+        !workspace)
+        return LOSSK_LENGTH_MISMATCH;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LOSSK_UNALIGNED;
+    // chunk = 1 and chunk = n_tok, or the largest chunk the logit budget allows
+    const int64_t c_max = MAX_LOGIT_CELLS / V;
+    const int64_t chunks[2] = {1, n < c_max ? n : c_max};
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    float *runs = reinterpret_cast<float *>(base + L.off_chk);             // lse_a, ce_a, lse_b, ce_b
+    double *scal = reinterpret_cast<double *>(base + L.off_chk + sizeof(float) * 4 * L.n_pad);   // 2 x 3
+    for (int r = 0; r < 2; ++r) {
+        s = lossk_ce_fwd(n, d, V, chunks[r], dtype, hidden, hidden_len, weight, weight_len, targets, targets_len,
+                         loss_mask, z_weight, runs + (2 * r) * L.n_pad, runs + (2 * r + 1) * L.n_pad, scal + 3 * r,
+                         workspace, static_cast<int64_t>(L.off_chk), stream);
+        if (s != LOSSK_OK) return s;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    std::vector<float> hr(static_cast<size_t>(4 * L.n_pad));
+    double hs[6];
+    if (cudaMemcpyAsync(hr.data(), runs, sizeof(float) * hr.size(), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(hs, scal, sizeof(hs), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    double m = 0.0;
+    for (int i = 0; i < 3; ++i) m = std::fmax(m, std::fabs(hs[i] - hs[3 + i]));
+    for (int64_t t = 0; t < n; ++t)
+        for (int q = 0; q < 2; ++q)
+            m = std::fmax(m, std::fabs(static_cast<double>(hr[q * L.n_pad + t]) -
+                                       static_cast<double>(hr[(2 + q) * L.n_pad + t])));
+    *max_abs_delta = m;
+    return LOSSK_OK;
 }
 
 int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
@@ -836,7 +972,7 @@ const char *lossk_kernel_name(int32_t kind)
                                       "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
                                       "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
                                       "from_logits",  "tc_fused",      "tgt_logit",   "merge_fused",
-                                      "combine_dh",   "teacher_stats"};
+                                      "combine_dh",   "teacher_stats", "distill_logits"};
     return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
 }
 

@@ -52,6 +52,8 @@ struct WsLayout {
     size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
     size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the cluster passes
     size_t off_tstat = 0;    // double2 [n_pad] distillation: teacher (lse_t2, Eb) per token
+    size_t off_dhacc = 0;    // float [n_tok][d_model] training step with accumulation: d_hidden before it is added
+    size_t off_chk = 0;      // chunk self-check: two runs' lse and ce, float [4][n_pad], + double [8]
     size_t off_red = 0;      // double [8] reduction output scratch
     size_t total = 0;
 };
@@ -128,6 +130,7 @@ struct BwdArgs {
     int64_t out_split_stride;
     float *zpart;          // BWD_FUSED: sums of G' [n_split * n_cl][zpart_stride]
     int64_t zpart_stride;
+    int accumulate;        // add the accumulator into `out` instead of overwriting it
     int *err;
 };
 
@@ -158,6 +161,7 @@ enum KernelKind : int {
     KK_MERGE_FUSED,
     KK_COMBINE_DH,
     KK_TEACHER_STATS,
+    KK_DISTILL_LOGITS,
     KK_N
 };
 
@@ -172,7 +176,7 @@ cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, cons
                       float inv_t, const int64_t *targets, const float4 *tokp, const double2 *tstat,
                       float *part,
                       float *tgt, int64_t part_stride, int64_t part_plane, float *out,
-                      int64_t out_split_stride, cudaStream_t st);
+                      int64_t out_split_stride, cudaStream_t st, bool accumulate = false);
 cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
                             const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
                             double wz, float *lse_out, float *ce_out, double *tokacc,
@@ -184,13 +188,15 @@ cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const 
 // Teacher log-sum-exp and sum p*logit per token (one block per token row).
 cudaError_t launch_teacher_stats(int dtype_bf16, const void *teach, int64_t n, int64_t V, double temperature,
                                  double2 *out, cudaStream_t st);
+// sum: the three scalars are sums over the tokens instead of means over N_valid.
 cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
-                          double wz, double *scalars_out, cudaStream_t st);
+                          double wz, double *scalars_out, cudaStream_t st, bool sum = false);
 cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,
                            int64_t n, int64_t n_pad, double alpha, double wz, float4 *tokp,
                            cudaStream_t st);
+// accumulate: out += the sum instead of out = the sum.
 cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
-                              cudaStream_t st);
+                              cudaStream_t st, bool accumulate = false);
 // The fused forward + d_hidden path (label CE, bf16): target logit and
 // reference shift per token; merge of the fused pass's sums into lse, ce, z
 // and the backward parameters; d_hidden from the split partials.
@@ -203,6 +209,13 @@ cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt,
 cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int64_t d,
                               const uint16_t *W, const int64_t *targets, const float2 *dhc,
                               float *out, WsHeader *hdr, cudaStream_t st);
+// Distillation from given student logits: per token row the losses, lse and
+// backward parameters, and grad_logits (or nothing when grad is NULL).
+// at_on: the gradient scale of a counted token before the 1/T factor.
+cudaError_t launch_distill_logits(int dtype_bf16, const void *student, const void *teacher, const uint8_t *mask,
+                                  int64_t n, int64_t V, int direction, double temperature, double wz,
+                                  double at_on, float *lse_out, float *per_token, double *tokacc,
+                                  int64_t n_pad, void *grad, bool accumulate, cudaStream_t st);
 cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *targets,
                                const uint8_t *mask, int64_t n, int64_t V, double wz,
                                double alpha, float *lse_out, float *ce_out, double *tokacc,

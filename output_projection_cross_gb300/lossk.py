@@ -16,10 +16,11 @@ import torch
 
 from . import build as _build
 
-_i64, _i32, _dbl, _vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
+_i64, _i32, _dbl, _vp, _u32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, ctypes.c_uint32
 
 F32, BF16 = 0, 1
-KIND_CE_FWD, KIND_CE_BWD, KIND_CE_FWD_BWD, KIND_FROM_LOGITS, KIND_DISTILL = 0, 1, 2, 3, 4
+KIND_CE_FWD, KIND_CE_BWD, KIND_CE_FWD_BWD, KIND_FROM_LOGITS, KIND_DISTILL, KIND_CE_CHUNK_CHECK = 0, 1, 2, 3, 4, 5
+ACCUMULATE_GRADS, REDUCE_SUM = 1, 2
 DIRECTIONS = {"ce": 0, "fkl": 1, "rkl": 2}
 OK = 580
 
@@ -56,6 +57,16 @@ def _load():
         "lossk_distill_fwd_bwd": (_i32, [_i64, _i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp,
                                          _i64, _vp, _i32, _dbl, _dbl, _dbl, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _i64, _vp]),
+        "lossk_ce_fwd_bwd_ex": (_i32, [_i64, _i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _i64,
+                                       _vp, _dbl, _dbl, _u32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+        "lossk_distill_fwd_bwd_ex": (_i32, [_i64, _i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp,
+                                            _i64, _vp, _i32, _dbl, _dbl, _dbl, _u32, _vp, _vp, _vp, _vp,
+                                            _vp, _vp, _i64, _vp]),
+        "lossk_ce_chunk_invariance": (_i32, [_i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _i64,
+                                             _vp, _dbl, ctypes.POINTER(_dbl), _vp, _i64, _vp]),
+        "lossk_distill_from_logits": (_i32, [_i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _i32, _dbl,
+                                             _dbl, _dbl, _u32, _vp, _vp, _vp, _vp, _i64, _vp, _i64,
+                                             _vp]),
         "lossk_device_status": (_i32, [_vp, _i64, _vp]),
         "lossk_ce_from_logits_static": (_i32, [_i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _dbl,
                                                _dbl, _vp, _vp, _vp, _vp, _i64, _vp]),
@@ -76,8 +87,10 @@ EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk
             "lossk_work_fits", "lossk_peak_logit_cells", "lossk_workspace_bytes",
             "lossk_targets_check", "lossk_ce_fwd", "lossk_ce_bwd", "lossk_ce_fwd_bwd",
             "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status",
+            "lossk_ce_fwd_bwd_ex", "lossk_distill_fwd_bwd_ex", "lossk_ce_chunk_invariance",
+            "lossk_distill_from_logits",
             "lossk_ce_from_logits_static", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
-N_KERNELS = 18
+N_KERNELS = 19
 
 
 class LosskError(RuntimeError):
@@ -218,6 +231,17 @@ def lossk_ce_bwd(hidden, weight, targets, lse, loss_mask=None, z_weight=0.0, gra
 def lossk_ce_fwd_bwd(hidden, weight, targets, loss_mask=None, chunk=None, z_weight=0.0,
                      grad_scale=1.0, lse_out=None, ce_out=None, scalars_out=None, d_hidden=None,
                      d_weight=None, want_d_hidden=True, want_d_weight=True, ws=None, stream=None):
+    return lossk_ce_fwd_bwd_ex(hidden, weight, targets, loss_mask, chunk, z_weight, grad_scale, 0,
+                               lse_out, ce_out, scalars_out, d_hidden, d_weight, want_d_hidden,
+                               want_d_weight, ws, stream)
+
+
+def lossk_ce_fwd_bwd_ex(hidden, weight, targets, loss_mask=None, chunk=None, z_weight=0.0,
+                        grad_scale=1.0, flags=0, lse_out=None, ce_out=None, scalars_out=None,
+                        d_hidden=None, d_weight=None, want_d_hidden=True, want_d_weight=True,
+                        ws=None, stream=None):
+    """flags: ACCUMULATE_GRADS (add into d_hidden / d_weight; outputs created here start at
+    zero) and/or REDUCE_SUM.  flags == 0 calls the plain C entry point."""
     for t, nm in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (loss_mask, "loss_mask")):
         _contig(t, nm)
     n, d = hidden.shape
@@ -227,17 +251,23 @@ def lossk_ce_fwd_bwd(hidden, weight, targets, loss_mask=None, chunk=None, z_weig
     lse_out = lse_out if lse_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
     ce_out = ce_out if ce_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
     scalars_out = scalars_out if scalars_out is not None else torch.empty(3, dtype=torch.float64, device=dev)
+    alloc = torch.zeros if flags & ACCUMULATE_GRADS else torch.empty
     if want_d_hidden and d_hidden is None:
-        d_hidden = torch.empty(n, d, dtype=torch.float32, device=dev)
+        d_hidden = alloc(n, d, dtype=torch.float32, device=dev)
     if want_d_weight and d_weight is None:
-        d_weight = torch.empty(V, d, dtype=torch.float32, device=dev)
+        d_weight = alloc(V, d, dtype=torch.float32, device=dev)
     ws = _ws(ws, KIND_CE_FWD_BWD, n, d, V, dt, dev)
-    st = lib.lossk_ce_fwd_bwd(n, d, V, n if chunk is None else chunk, dt, _ptr(hidden), _len(hidden),
-                              _ptr(weight), _len(weight), _ptr(targets), _len(targets),
-                              _ptr(loss_mask), z_weight, grad_scale, _ptr(lse_out), _ptr(ce_out),
-                              _ptr(scalars_out), _ptr(d_hidden), _ptr(d_weight), _ptr(ws), ws.numel(),
-                              _stream(stream))
-    _check(st, "lossk_ce_fwd_bwd")
+    args = (_ptr(hidden), _len(hidden), _ptr(weight), _len(weight), _ptr(targets), _len(targets),
+            _ptr(loss_mask), z_weight, grad_scale)
+    outs = (_ptr(lse_out), _ptr(ce_out), _ptr(scalars_out), _ptr(d_hidden), _ptr(d_weight), _ptr(ws),
+            ws.numel(), _stream(stream))
+    c = n if chunk is None else chunk
+    if flags == 0:
+        st = lib.lossk_ce_fwd_bwd(n, d, V, c, dt, *args, *outs)
+        _check(st, "lossk_ce_fwd_bwd")
+    else:
+        st = lib.lossk_ce_fwd_bwd_ex(n, d, V, c, dt, *args, flags, *outs)
+        _check(st, "lossk_ce_fwd_bwd_ex")
     return {"lse": lse_out, "ce": ce_out, "scalars": scalars_out, "d_hidden": d_hidden,
             "d_weight": d_weight}
 
@@ -293,6 +323,17 @@ def lossk_distill_fwd_bwd(hidden, weight, teacher_logits, direction="fkl", tempe
                           scalars_out=None, per_token_out=None, lse_out=None, d_hidden=None,
                           d_weight=None, want_d_hidden=True, want_d_weight=True, ws=None,
                           stream=None):
+    return lossk_distill_fwd_bwd_ex(hidden, weight, teacher_logits, direction, temperature,
+                                    loss_mask, chunk, z_weight, grad_scale, 0, scalars_out,
+                                    per_token_out, lse_out, d_hidden, d_weight, want_d_hidden,
+                                    want_d_weight, ws, stream)
+
+
+def lossk_distill_fwd_bwd_ex(hidden, weight, teacher_logits, direction="fkl", temperature=1.0,
+                             loss_mask=None, chunk=None, z_weight=0.0, grad_scale=1.0, flags=0,
+                             scalars_out=None, per_token_out=None, lse_out=None, d_hidden=None,
+                             d_weight=None, want_d_hidden=True, want_d_weight=True, ws=None,
+                             stream=None):
     for t, nm in ((hidden, "hidden"), (weight, "weight"), (teacher_logits, "teacher_logits"),
                   (loss_mask, "loss_mask")):
         _contig(t, nm)
@@ -304,20 +345,68 @@ def lossk_distill_fwd_bwd(hidden, weight, teacher_logits, direction="fkl", tempe
     scalars_out = scalars_out if scalars_out is not None else torch.empty(3, dtype=torch.float64, device=dev)
     per_token_out = per_token_out if per_token_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
     lse_out = lse_out if lse_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    alloc = torch.zeros if flags & ACCUMULATE_GRADS else torch.empty
     if want_d_hidden and d_hidden is None:
-        d_hidden = torch.empty(n, d, dtype=torch.float32, device=dev)
+        d_hidden = alloc(n, d, dtype=torch.float32, device=dev)
     if want_d_weight and d_weight is None:
-        d_weight = torch.empty(V, d, dtype=torch.float32, device=dev)
+        d_weight = alloc(V, d, dtype=torch.float32, device=dev)
     ws = _ws(ws, KIND_DISTILL, n, d, V, dt, dev)
-    st = lib.lossk_distill_fwd_bwd(n, d, V, n if chunk is None else chunk, dt, _ptr(hidden),
-                                   _len(hidden), _ptr(weight), _len(weight), _ptr(teacher_logits),
-                                   _len(teacher_logits), _ptr(loss_mask), dirn, temperature,
-                                   z_weight, grad_scale, _ptr(scalars_out), _ptr(per_token_out),
-                                   _ptr(lse_out), _ptr(d_hidden), _ptr(d_weight), _ptr(ws),
-                                   ws.numel(), _stream(stream))
-    _check(st, "lossk_distill_fwd_bwd")
+    head = (n, d, V, n if chunk is None else chunk, dt, _ptr(hidden), _len(hidden), _ptr(weight),
+            _len(weight), _ptr(teacher_logits), _len(teacher_logits), _ptr(loss_mask), dirn,
+            temperature, z_weight, grad_scale)
+    tail = (_ptr(scalars_out), _ptr(per_token_out), _ptr(lse_out), _ptr(d_hidden), _ptr(d_weight),
+            _ptr(ws), ws.numel(), _stream(stream))
+    if flags == 0:
+        _check(lib.lossk_distill_fwd_bwd(*head, *tail), "lossk_distill_fwd_bwd")
+    else:
+        _check(lib.lossk_distill_fwd_bwd_ex(*head, flags, *tail), "lossk_distill_fwd_bwd_ex")
     return {"scalars": scalars_out, "per_token": per_token_out, "lse": lse_out,
             "d_hidden": d_hidden, "d_weight": d_weight}
+
+
+def lossk_ce_chunk_invariance(hidden, weight, targets, loss_mask=None, z_weight=0.0, ws=None,
+                              stream=None) -> float:
+    """Max |difference| between lossk_ce_fwd at chunk 1 and at chunk n_tok (or the largest
+    chunk the logit budget allows) over the scalars and every token's lse and ce."""
+    for t, nm in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (loss_mask, "loss_mask")):
+        _contig(t, nm)
+    n, d = hidden.shape
+    V = weight.shape[0]
+    dt = _dtype_code(hidden)
+    ws = _ws(ws, KIND_CE_CHUNK_CHECK, n, d, V, dt, hidden.device)
+    out = _dbl(-1.0)
+    st = lib.lossk_ce_chunk_invariance(n, d, V, dt, _ptr(hidden), _len(hidden), _ptr(weight),
+                                       _len(weight), _ptr(targets), _len(targets), _ptr(loss_mask),
+                                       z_weight, ctypes.byref(out), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "lossk_ce_chunk_invariance")
+    return out.value
+
+
+def lossk_distill_from_logits(logits, teacher_logits, direction="fkl", temperature=1.0,
+                              loss_mask=None, z_weight=0.0, grad_scale=1.0, flags=0, want_grad=True,
+                              scalars_out=None, per_token_out=None, lse_out=None, grad_logits=None,
+                              ws=None, stream=None):
+    for t, nm in ((logits, "logits"), (teacher_logits, "teacher_logits"), (loss_mask, "loss_mask")):
+        _contig(t, nm)
+    n, V = logits.shape
+    dt = _dtype_code(logits)
+    dev = logits.device
+    dirn = DIRECTIONS[direction] if isinstance(direction, str) else int(direction)
+    scalars_out = scalars_out if scalars_out is not None else torch.empty(3, dtype=torch.float64, device=dev)
+    per_token_out = per_token_out if per_token_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    lse_out = lse_out if lse_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    if want_grad and grad_logits is None:
+        grad_logits = torch.zeros_like(logits) if flags & ACCUMULATE_GRADS else torch.empty_like(logits)
+    ws = _ws(ws, KIND_FROM_LOGITS, n, 1, V, dt, dev)
+    st = lib.lossk_distill_from_logits(n, V, dt, _ptr(logits), _len(logits), _ptr(teacher_logits),
+                                       _len(teacher_logits), _ptr(loss_mask), dirn, temperature,
+                                       z_weight, grad_scale, flags, _ptr(scalars_out),
+                                       _ptr(per_token_out), _ptr(lse_out), _ptr(grad_logits),
+                                       _len(grad_logits), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "lossk_distill_from_logits")
+    return {"scalars": scalars_out, "per_token": per_token_out, "lse": lse_out,
+            "grad_logits": grad_logits}
 
 
 def lossk_device_status(ws, stream=None) -> int:

@@ -40,9 +40,9 @@ def test_status_names_match_oracle(L):
     for code in range(570, 612):
         o = oracle.status_name(code)
         g = L.lossk_status_name(code)
-        if code in (589, 590, 591):
+        if code in (589, 590, 591, 592):
             assert o == "unknown_status"
-            assert g in ("device_error", "device_timeout", "unaligned")
+            assert g in ("device_error", "device_timeout", "unaligned", "unknown_flags")
         else:
             assert g == o, code
 

@@ -508,3 +508,146 @@ def test_device_status_clean_after_calls(L):
     y = torch.randint(0, V, (n,), device="cuda")
     L.lossk_ce_fwd_bwd(H, W, y, ws=ws)
     assert L.lossk_device_status(ws) == 580
+
+
+# ---------------------------------------------------------------------------
+# Gradient accumulation, sum reduction, the chunk self-check, distillation from
+# given logits.
+
+@pytest.mark.parametrize("dtype,shape", [("bf16", (300, 256, 2000)), ("bf16", (257, 520, 3000)),
+                                         ("fp32", (130, 72, 300))])
+def test_ce_accumulate_and_sum_flags(L, dtype, shape):
+    n, d, V = shape
+    x = _inputs("ce_512x1024x32000", seed=50, n_tok=n, d_model=d, vocab=V)
+    if dtype == "fp32":
+        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
+        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    mask = li.mask(3, n, 0.2)
+    nv = int(mask.sum())
+    wz, gs = 1e-3, 0.75
+    H, W, y, m = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], ""), _dev(mask, "")
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz, grad_scale=gs)
+    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    # starting gradients of the same order as the ones added, so that fp32 keeps the sum exact enough
+    h0 = torch.randn(n, d, device="cuda", generator=g) * 1e-4
+    w0 = torch.randn(V, d, device="cuda", generator=g) * 1e-3
+    for flags in (L.lossk.ACCUMULATE_GRADS, L.lossk.REDUCE_SUM, L.lossk.ACCUMULATE_GRADS | L.lossk.REDUCE_SUM):
+        acc, sm = bool(flags & L.lossk.ACCUMULATE_GRADS), bool(flags & L.lossk.REDUCE_SUM)
+        dh, dw = h0.clone(), w0.clone()
+        o = L.lossk_ce_fwd_bwd_ex(H, W, y, loss_mask=m, chunk=64, z_weight=wz, grad_scale=gs,
+                                  flags=flags, d_hidden=dh, d_weight=dw)
+        torch.cuda.synchronize()
+        k = nv if sm else 1
+        close_loss(_np(o["scalars"]), [ref["total"] * k, ref["ce_mean"] * k, ref["z_mean"] * k], lt)
+        close_loss(_np(o["lse"]), ref["lse"], lt)
+        base_h = _np(h0) if acc else 0.0
+        base_w = _np(w0) if acc else 0.0
+        assert rel_l2(_np(dh) - base_h, dH * k) <= gt, flags
+        assert rel_l2(_np(dw) - base_w, dW * k) <= gt, flags
+
+
+def test_ce_accumulate_through_the_recompute_fallback(L):
+    """A 160-nat row sends the training step to the separate passes; with
+    accumulation the caller's gradients must still receive the sum once."""
+    n, d, V = 130, 64, 1000
+    x = _inputs("ce_512x1024x32000", seed=9, n_tok=n, d_model=d, vocab=V)
+    Hn, Wn, yn = x["hidden"].copy(), x["weight"].copy(), x["targets"].copy()
+    Hn[7, :] = 1.0
+    Wn[3, :] = 2.5
+    Wn[5, :] = 0.0
+    yn[7] = 5
+    Hn, Wn = li.to_bf16_values(Hn), li.to_bf16_values(Wn)
+    H, W, y = _dev(Hn, "bf16"), _dev(Wn, "bf16"), _dev(yn, "")
+    h0 = torch.full((n, d), 0.25, device="cuda")
+    w0 = torch.full((V, d), -0.5, device="cuda")
+    dh, dw = h0.clone(), w0.clone()
+    L.lossk_ce_fwd_bwd_ex(H, W, y, z_weight=1e-4, flags=L.lossk.ACCUMULATE_GRADS, d_hidden=dh, d_weight=dw)
+    torch.cuda.synchronize()
+    dH, dW = oracle.ce_bwd(Hn, Wn, yn, z_weight=1e-4)
+    assert rel_l2(_np(dh) - 0.25, dH) <= BF16_GRAD
+    assert rel_l2(_np(dw) + 0.5, dW) <= BF16_GRAD
+
+
+@pytest.mark.parametrize("direction", ["ce", "rkl"])
+def test_distill_accumulate_and_sum_flags(L, direction):
+    n, d, V = 200, 256, 1024
+    x = _inputs("distill_z_4096x2048", seed=51, n_tok=n, d_model=d, vocab=V)
+    mask = li.mask(6, n, 0.1)
+    nv = int(mask.sum())
+    r = oracle.distill(x["hidden"], x["weight"], x["teacher"], direction, temperature=2.0, mask=mask,
+                       z_weight=1e-3)
+    h0 = torch.ones(n, d, device="cuda") * 0.1
+    w0 = torch.ones(V, d, device="cuda") * -0.2
+    flags = L.lossk.ACCUMULATE_GRADS | L.lossk.REDUCE_SUM
+    dh, dw = h0.clone(), w0.clone()
+    o = L.lossk_distill_fwd_bwd_ex(_dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"),
+                                   _dev(x["teacher"], "bf16"), direction, temperature=2.0,
+                                   loss_mask=_dev(mask, ""), z_weight=1e-3, flags=flags,
+                                   d_hidden=dh, d_weight=dw)
+    torch.cuda.synchronize()
+    close_loss(_np(o["scalars"]), [r["total"] * nv, r["distill_mean"] * nv, r["z_mean"] * nv], BF16_LOSS)
+    assert rel_l2(_np(dh) - 0.1, r["dH"] * nv) <= BF16_GRAD
+    assert rel_l2(_np(dw) + 0.2, r["dW"] * nv) <= BF16_GRAD
+
+
+def test_unknown_flag_bits_are_refused(L):
+    n, d, V = 64, 64, 512
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = torch.randn(V, d, device="cuda").to(torch.bfloat16)
+    y = torch.randint(0, V, (n,), device="cuda")
+    dh = torch.full((n, d), 3.0, device="cuda")
+    with pytest.raises(L.LosskError) as e:
+        L.lossk_ce_fwd_bwd_ex(H, W, y, flags=4, d_hidden=dh)
+    assert e.value.status == 592
+    assert torch.all(dh == 3.0)
+
+
+@pytest.mark.parametrize("dtype,shape", [("bf16", (300, 256, 2000)), ("fp32", (64, 64, 1000)),
+                                         ("bf16", (2048, 1024, 151936))])
+def test_chunk_invariance_self_check(L, dtype, shape):
+    n, d, V = shape
+    x = _inputs("ce_512x1024x32000", seed=52, n_tok=n, d_model=d, vocab=V)
+    if dtype == "fp32":
+        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
+        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    delta = L.lossk_ce_chunk_invariance(_dev(x["hidden"], dtype), _dev(x["weight"], dtype),
+                                        _dev(x["targets"], ""), loss_mask=_dev(li.mask(2, n, 0.1), ""),
+                                        z_weight=1e-3)
+    assert delta == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+@pytest.mark.parametrize("V", [3000, 1003])
+def test_distill_from_logits(L, dtype, direction, V):
+    n = 67
+    g = np.random.default_rng(V + len(direction))
+    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
+    Tt = (g.standard_normal((n, V)) * 3).astype(np.float32)
+    if dtype == "bf16":
+        X, Tt = li.to_bf16_values(X), li.to_bf16_values(Tt)
+    mask = li.mask(7, n, 0.15)
+    for sm in (False, True):
+        r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, mask=mask, z_weight=1e-3,
+                                       grad_scale=0.9, reduce_sum=sm)
+        flags = L.lossk.REDUCE_SUM if sm else 0
+        o = L.lossk_distill_from_logits(_dev(X, dtype), _dev(Tt, dtype), direction, temperature=1.5,
+                                        loss_mask=_dev(mask, ""), z_weight=1e-3, grad_scale=0.9,
+                                        flags=flags)
+        torch.cuda.synchronize()
+        lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+        close_loss(_np(o["per_token"]), r["per_token"], lt)
+        close_loss(_np(o["lse"]), r["lse"], lt)
+        close_loss(_np(o["scalars"]), [r["total"], r["distill_mean"], r["z_mean"]], lt)
+        assert rel_l2(_np(o["grad_logits"]), r["grad"]) <= gt
+    # accumulation: two calls into a zeroed gradient give twice the gradient
+    gl = torch.zeros(n, V, device="cuda", dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    for _ in range(2):
+        L.lossk_distill_from_logits(_dev(X, dtype), _dev(Tt, dtype), direction, temperature=1.5,
+                                    loss_mask=_dev(mask, ""), z_weight=1e-3, grad_scale=0.9,
+                                    flags=L.lossk.ACCUMULATE_GRADS, grad_logits=gl)
+    torch.cuda.synchronize()
+    r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, mask=mask, z_weight=1e-3, grad_scale=0.9)
+    assert rel_l2(_np(gl), 2 * r["grad"]) <= (BF16_GRAD if dtype == "bf16" else F32_GRAD)

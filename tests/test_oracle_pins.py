@@ -368,6 +368,55 @@ def test_distill_matches_torch_library(direction, T, wz):
     assert np.allclose(r["dW"], Wt.grad.numpy(), rtol=1e-10, atol=1e-14)
 
 
+def _torch_distill_logits(X, Tt, direction, T, mask, wz, reduce_sum):
+    """The three objectives written with torch's own log_softmax / kl_div /
+    logsumexp, on given student logits X (the from-distribution form)."""
+    a = torch.log_softmax(X / T, dim=1)
+    lp = torch.log_softmax(Tt / T, dim=1)
+    if direction == "ce":
+        L = -(lp.exp() * a).sum(1)
+    elif direction == "fkl":
+        L = torch.nn.functional.kl_div(a, lp, reduction="none", log_target=True).sum(1)
+    else:
+        L = torch.nn.functional.kl_div(lp, a, reduction="none", log_target=True).sum(1)
+    lse = torch.logsumexp(X / T, dim=1)
+    m = torch.ones(X.shape[0], dtype=F64) if mask is None else torch.tensor(mask, dtype=F64)
+    s = ((L + wz * lse * lse) * m).sum()
+    return (s if reduce_sum else s / m.sum()), L, lse
+
+
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+@pytest.mark.parametrize("T,wz,reduce_sum", [(1.0, 0.0, False), (2.0, 0.1, False), (0.7, 0.05, True)])
+def test_distill_from_logits_matches_torch_library(direction, T, wz, reduce_sum):
+    g = np.random.default_rng(22)
+    X = g.standard_normal((9, 37)).astype(np.float32) * 2
+    Tt = (g.standard_normal((9, 37)) * 3).astype(np.float32)
+    mask = np.array([1, 0, 1, 1, 1, 1, 0, 1, 1], np.uint8)
+    gs = 0.8
+    r = oracle.distill_from_logits(X, Tt, direction, temperature=T, mask=mask, z_weight=wz,
+                                   grad_scale=gs, reduce_sum=reduce_sum)
+    Xt = torch.tensor(X, dtype=F64, requires_grad=True)
+    tot, L, lse = _torch_distill_logits(Xt, torch.tensor(Tt, dtype=F64), direction, T, mask, wz,
+                                        reduce_sum)
+    assert r["total"] == pytest.approx(tot.item(), rel=1e-12)
+    assert np.allclose(r["per_token"], L.detach().numpy() * mask, rtol=1e-10, atol=1e-13)
+    assert np.allclose(r["lse"], lse.detach().numpy(), rtol=1e-13)
+    (gs * tot).backward()
+    assert np.allclose(r["grad"], Xt.grad.numpy(), rtol=1e-10, atol=1e-14)
+
+
+def test_distill_from_logits_sum_is_mean_times_count():
+    g = np.random.default_rng(23)
+    X = g.standard_normal((7, 20)).astype(np.float32)
+    Tt = g.standard_normal((7, 20)).astype(np.float32)
+    mask = np.array([1, 1, 0, 1, 1, 0, 1], np.uint8)
+    a = oracle.distill_from_logits(X, Tt, "fkl", temperature=1.5, mask=mask, z_weight=0.1)
+    b = oracle.distill_from_logits(X, Tt, "fkl", temperature=1.5, mask=mask, z_weight=0.1,
+                                   reduce_sum=True)
+    assert b["total"] == pytest.approx(a["total"] * 5, rel=1e-14)
+    assert np.allclose(b["grad"], a["grad"] * 5, rtol=1e-13, atol=1e-16)
+
+
 def test_distill_uniform_teacher_zero_weight():
     n, d, V = 5, 4, 17
     H = np.random.default_rng(3).standard_normal((n, d)).astype(np.float32)
