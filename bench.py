@@ -40,7 +40,8 @@ WORKLOAD = "qwen3_0p6b_head"
 ALGO_FLOPS_NDV = {"tc_stats": 2.0, "tc_rows": 4.0, "tc_cols": 4.0, "tc_fused": 4.0,
                   "fp_stats": 2.0, "fp_rows": 4.0, "fp_cols": 4.0}
 HBM_KERNELS = {"from_logits", "validate", "merge_ce", "merge_distill", "reduce", "tokp_ce",
-               "sum_splits", "tgt_logit", "merge_fused", "combine_dh", "teacher_stats"}
+               "sum_splits", "tgt_logit", "merge_fused", "combine_dh", "teacher_stats",
+               "distill_logits"}
 
 
 def peaks():
@@ -433,6 +434,26 @@ def extra_paths(L, dev, pk, n_tok=None):
         res["from_logits" + ("_grad" if want else "")] = {
             "workload": "logits bf16 [2048][151936]", "ms": ms,
             "kernel_ms": kms, "algorithmic_bytes": nbytes,
+            "achieved_gbs": nbytes / (kms / 1e3) / 1e9,
+            "frac_hbm": nbytes / (kms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    # distillation from given student logits (HBM stream): read the student and
+    # teacher logits once, write grad_logits once
+    T = (torch.randn(n, V, device=dev, generator=g) * 3).to(torch.bfloat16)
+    ws = L.workspace(L.lossk.KIND_FROM_LOGITS, n, 1, V, 1, dev)
+    for want in (False, True):
+        def fn():
+            L.lossk_distill_from_logits(X, T, "fkl", temperature=2.0, z_weight=1e-4, want_grad=want,
+                                        grad_logits=grad if want else None, ws=ws)
+        L.lossk_profile_read(reset=True)
+        L.lossk_profile_enable(True)
+        ms = _time(fn, 5)
+        L.lossk_profile_enable(False)
+        prof = L.lossk_profile_read(reset=True)
+        kms = prof["distill_logits"][0] / prof["distill_logits"][1]
+        nbytes = X.numel() * 2 * (3 if want else 2)
+        res["distill_from_logits" + ("_grad" if want else "")] = {
+            "workload": "student and teacher logits bf16 [2048][151936], forward KL, T 2",
+            "ms": ms, "kernel_ms": kms, "algorithmic_bytes": nbytes,
             "achieved_gbs": nbytes / (kms / 1e3) / 1e9,
             "frac_hbm": nbytes / (kms / 1e3) / 1e9 / pk["hbm_gbs"]}
     return res
