@@ -58,7 +58,7 @@ def peaks():
 def args_parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the extra path measurements")
@@ -111,7 +111,10 @@ def aggregate(n_tok_per_rank, world, max_ms):
 # ---- clocks -------------------------------------------------------------------
 
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms.  mark() brackets the timed region on the
+    host clock; stop() keeps the samples taken inside it (all loaded samples if
+    the region was shorter than the sampling interval, said in `window`)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -119,6 +122,15 @@ class Clocks:
         self.uuid = gpu_uuid
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
+
+    def mark(self, begin):
+        import datetime
+        now = datetime.datetime.now()
+        if begin:
+            self.t0 = now
+        else:
+            self.t1 = now
 
     def start(self):
         try:
@@ -141,24 +153,32 @@ class Clocks:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        import datetime
         rows = []
         for line in open(self.path):
             f = [c.strip() for c in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9], ts))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return None
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[4] <= self.t1]
+        window = "timed region"
+        if not inside:
+            # the timed region was shorter than the sampling interval: the samples
+            # of the loaded window around it (untimed steps before and after)
+            inside = [r for r in rows if r[2] > 0.3 * max(x[2] for x in rows)] or rows
+            window = "loaded window around the timed region"
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        loaded = [r for r in rows if r[2] > 0.3 * max(x[2] for x in rows)] or rows
-        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in inside),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+                "samples": len(inside), "window": window, "power_w_max": max(r[2] for r in inside)}
 
 
 # ---- traffic from the committed ncu summary -----------------------------------
@@ -199,12 +219,16 @@ def cpu_cores():
 
 
 def cpu_baseline(x, chunk, seconds):
-    """Oracle fwd+bwd on the first k tokens of the batch; k sized to ~`seconds`."""
+    """Oracle fwd+bwd on the first k tokens of the batch; k sized to ~`seconds`
+    from a calibration run on 2 tokens per core (the oracle splits tokens
+    across its threads, so fewer tokens would leave cores idle and overstate
+    the time per token)."""
     os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+    k0 = min(len(x["targets"]), 2 * cpu_cores())
     t0 = time.perf_counter()
-    oracle_step(x, 2, chunk)
-    t2 = time.perf_counter() - t0
-    k = int(max(2, min(len(x["targets"]), 2 * seconds / max(t2, 1e-3))))
+    oracle_step(x, k0, chunk)
+    tk = time.perf_counter() - t0
+    k = int(max(k0, min(len(x["targets"]), k0 * seconds / max(tk, 1e-3))))
     t0 = time.perf_counter()
     oracle_step(x, k, chunk)
     dt = time.perf_counter() - t0
@@ -214,6 +238,11 @@ def cpu_baseline(x, chunk, seconds):
 
 
 # ---- our implementation -----------------------------------------------------------------
+
+def WORKLOAD_OBJ():
+    import lossk_inputs as li
+    return li.WORKLOADS[WORKLOAD]
+
 
 def run_ours(a, rank, world, local):
     import numpy as np
@@ -250,23 +279,35 @@ def run_ours(a, rank, world, local):
     except Exception:
         uuid = None
     clocks = Clocks(uuid)
+    # the sampler needs a moment to start: keep the GPU loaded with untimed
+    # steps for ~0.4 s before the timed region and ~0.2 s after it
+    clocks.start()
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 0.4:
+        step()
+        torch.cuda.synchronize()
     L.lossk_profile_read(reset=True)
     L.lossk_profile_enable(True)
-    launches0 = L.lossk_launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
+    launches0 = L.lossk_launch_count()
+    clocks.mark(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(a.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    ck = clocks.stop()
+    clocks.mark(False)
     launches = L.lossk_launch_count() - launches0
     L.lossk_profile_enable(False)
     prof = L.lossk_profile_read(reset=True)
+    barrier(world)
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 0.2:
+        step()
+        torch.cuda.synchronize()
+    ck = clocks.stop()
     ms = e0.elapsed_time(e1) / a.steps
     ms_max = max_over_ranks(ms, world)
     assert L.lossk_device_status(ws) == 580
@@ -315,41 +356,83 @@ def run_ours(a, rank, world, local):
 
 
 def e2e(a, x, H, W, y, out, step, stream, n, world):
-    """The same step through the C ABI with host buffers: each step copies its
-    inputs from pinned host memory and its outputs back, inside the timed region."""
+    """The same step through the public call with host buffers.  Every timed
+    step copies its inputs (hidden, weight, targets) from pinned host memory to
+    the device and its outputs (lse, ce, scalars, d_hidden, d_weight) back to
+    pinned host memory.  The copies are pipelined the way a training loop feeds
+    a device: step i+1's inputs travel on a copy stream while step i computes,
+    and step i's gradients travel back on another while step i+1 computes.
+    Device buffers are doubled for that; the timed region runs from the first
+    input copy to the last output copy."""
     import numpy as np
     import torch
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    import output_projection_cross_gb300 as L
+
+    w = WORKLOAD_OBJ()
+    dev = H.device
     hH = torch.from_numpy(x["hidden"]).to(torch.bfloat16).pin_memory()
     hW = torch.from_numpy(x["weight"]).to(torch.bfloat16).pin_memory()
     hy = torch.from_numpy(x["targets"]).pin_memory()
-    o_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
     bi = hH.numel() * 2 + hW.numel() * 2 + hy.numel() * 8
-    bo = sum(v.numel() * v.element_size() for v in o_h.values())
+    ins = [(H, W, y), (torch.empty_like(H), torch.empty_like(W), torch.empty_like(y))]
+    outs = [out, {k: torch.empty_like(v) for k, v in out.items()}]
+    o_h = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()} for _ in range(2)]
+    bo = sum(v.numel() * v.element_size() for v in o_h[0].values())
+    ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, H.shape[1], W.shape[0], L.lossk.BF16, dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def e2e_step():
-        H.copy_(hH, non_blocking=True)
-        W.copy_(hW, non_blocking=True)
-        y.copy_(hy, non_blocking=True)
-        step()
-        for k, v in out.items():
-            o_h[k].copy_(v, non_blocking=True)
+    def run(k_steps, timed):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for e in comp_done + out_done:
+            e.record(stream)
+        with torch.cuda.stream(s_in):
+            if timed:
+                e0.record(s_in)
+            hb, wb, yb = ins[0]
+            hb.copy_(hH, non_blocking=True)
+            wb.copy_(hW, non_blocking=True)
+            yb.copy_(hy, non_blocking=True)
+            in_done[0].record(s_in)
+        for i in range(k_steps):
+            b = i % 2
+            if i + 1 < k_steps:
+                nb = (i + 1) % 2
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(comp_done[nb])          # step i-1 no longer reads buffer nb
+                    hb, wb, yb = ins[nb]
+                    hb.copy_(hH, non_blocking=True)
+                    wb.copy_(hW, non_blocking=True)
+                    yb.copy_(hy, non_blocking=True)
+                    in_done[nb].record(s_in)
+            stream.wait_event(in_done[b])
+            stream.wait_event(out_done[b])                  # step i-2's outputs have left buffer b
+            hb, wb, yb = ins[b]
+            L.lossk_ce_fwd_bwd(hb, wb, yb, chunk=w.chunk, z_weight=w.z_weight, ws=ws, **outs[b])
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                for k, v in outs[b].items():
+                    o_h[b][k].copy_(v, non_blocking=True)
+                out_done[b].record(s_out)
+        stream.wait_event(out_done[(k_steps - 1) % 2])
+        if timed:
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0, e1
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
+    run(2, False)
     barrier(world)
-    k_e2e = max(3, min(a.steps, 10))
-    e0.record(stream)
-    for _ in range(k_e2e):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    k_e2e = max(3, min(a.steps, 20))
+    e0, e1 = run(k_e2e, True)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / k_e2e, world)
-    # the results of the last e2e step match the device-resident ones
-    assert np.array_equal(o_h["scalars_out"].numpy(), out["scalars_out"].cpu().numpy())
+    # the results that came back match the device-resident step's
+    assert np.array_equal(o_h[(k_e2e - 1) % 2]["scalars_out"].numpy(), out["scalars_out"].cpu().numpy())
     return {"value": aggregate(n, world, e2e_ms), "unit": "tokens/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+            "overlap": "next step's inputs and previous step's outputs copied during the current step"}
 
 
 def _time(fn, reps, warm=2):
