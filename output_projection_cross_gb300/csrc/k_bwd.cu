@@ -69,9 +69,17 @@ constexpr int B_NST = 4;                          // operand ring stages
 constexpr int B_STAGE = 49152;                    // 48 KB: an A part and a B part
 constexpr int B_APART = 16384;                    // 128 rows x 64 K (bf16, 128-byte swizzle)
 constexpr int B_MAXC = 8;                         // CTAs per cluster at most
-constexpr int B_NBARS = 2 * B_NST + 4 + B_MAXC * G_SLOTS + G_SLOTS + 1;
-constexpr int B_SMEM = 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + B_NBARS * 8 + 16;
-static_assert(B_SMEM <= 232448, "fits the 227 KB per-CTA shared memory limit");
+constexpr int B_NBARS = 2 * B_NST + 4 + B_MAXC * G_SLOTS + G_SLOTS + 1 + 8;
+// The distillation d_weight pass reads its teacher block through TMA: per
+// epilogue warp two 32-token x 32-vocabulary bf16 buffers (2 KB each).
+constexpr int B_TBLK = 32 * 32 * 2;
+constexpr int B_TEACH = 4 * 2 * B_TBLK;
+template <int MODE, bool DISTILL> constexpr int bwd_smem()
+{
+    return 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + ((MODE == BWD_COLS && DISTILL) ? B_TEACH : 0) +
+           B_NBARS * 8 + 16;
+}
+static_assert(bwd_smem<BWD_COLS, true>() <= 232448, "fits the 227 KB per-CTA shared memory limit");
 static_assert(BWD_BN == 256 && TC_SLICE == 256, "one 256-column logit buffer + one 256-column accumulator");
 
 __device__ __forceinline__ float bw_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -139,7 +147,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint8_t *ring = smem;
     // d_weight: per-token parameters of a supertile's columns, one copy per epilogue warp
     float4 *sPall = reinterpret_cast<float4 *>(ring + B_NST * B_STAGE);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sPall + 4 * BWD_BN);
+    constexpr bool TTMA = MODE == BWD_COLS && DISTILL;     // teacher blocks through TMA
+    uint8_t *tblk = reinterpret_cast<uint8_t *>(sPall + 4 * BWD_BN);   // [4 warps][2][32][32] bf16
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tblk + (TTMA ? B_TEACH : 0));
     uint64_t *full = bars;                 // [B_NST]
     uint64_t *empty = full + B_NST;        // [B_NST]
     uint64_t *tfull = empty + B_NST;       // logit tile ready in TMEM
@@ -149,7 +159,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint64_t *gready = accempty + 1;       // [B_MAXC][G_SLOTS] a writer's tile is in its slot (4 warps)
     uint64_t *gfree = gready + B_MAXC * G_SLOTS;   // [G_SLOTS] own slot loaded by every CTA (c)
     uint64_t *drain = gfree + G_SLOTS;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *tbar = drain + 1;            // [4 warps][2] teacher block landed (TTMA)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tbar + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int *err = a.err;
@@ -187,6 +198,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         for (int i = 0; i < B_MAXC * G_SLOTS; ++i) mbar_init(&gready[i], 4);
         for (int g = 0; g < G_SLOTS; ++g) mbar_init(&gfree[g], c);
         mbar_init(drain, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&tbar[i], 1);
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(tslot, 512);
@@ -343,6 +355,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int quad = warp & 3;
         const int r = quad * 32 + lane;               // logit-tile row of this thread
         float4 *sP = sPall + quad * BWD_BN;           // this warp's copy
+        uint8_t *tw_s = tblk + quad * 2 * B_TBLK;     // TTMA: this warp's two teacher buffers
+        uint64_t *tw_b = tbar + quad * 2;
+        // TTMA: issued and waited fills of each buffer.  Chunk q always uses buffer
+        // q & 1 and a supertile has an even number of chunks, so one count of
+        // each kind serves both buffers: buffer b's k-th fill is the (2k+b)-th.
+        int tiss_all = 0, tuse_all = 0;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float L2E = static_cast<float>(LOG2E);
         const float kT = a.inv_t_l2e;
@@ -410,7 +428,33 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                                             : static_cast<int64_t>(loop0) * a.vocab + (t_ok ? fixrow : 0))
                         : nullptr;
             uint32_t tw[16];                          // a chunk's 32 teacher values (bf16 pairs)
+            // TTMA: warp-local TMA of the teacher block [32 tokens][this warp's 32
+            // vocabulary rows] of chunk q into buffer q & 1 (lane 0 issues; the
+            // lanes' earlier reads of that buffer are ordered before it).
+            auto tissue = [&](int q) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                ++tiss_all;
+                if (lane == 0) {
+                    uint64_t *bar = &tw_b[q & 1];
+                    mbar_arrive_expect_tx(bar, B_TBLK);
+                    tma_load_2d(tw_s + (q & 1) * B_TBLK, &a.map_teach, bar, w.fixed * 128 + quad * 32,
+                                loop0 + q * 32);
+                }
+            };
+            bool tok_all = true;
             auto tload = [&](int q) {
+                if (TTMA) {
+                    const int b = q & 1;
+                    const bool okw = mbar_wait(&tw_b[b], (tuse_all >> 1) & 1, err);
+                    tok_all = tok_all && okw;
+                    ++tuse_all;
+                    const uint16_t *src = reinterpret_cast<const uint16_t *>(tw_s + b * B_TBLK) + lane;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        tw[i >> 1] = static_cast<uint32_t>(src[i * 32]) | (static_cast<uint32_t>(src[(i + 1) * 32]) << 16);
+                    return;
+                }
                 if (ROWS) {
                     // one contiguous 64-byte row segment: four 16-byte loads
                     const uint4 *src = reinterpret_cast<const uint4 *>(tbase + q * 32);
@@ -434,7 +478,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     }
                 }
             };
+            if (TTMA) {
+                tissue(0);
+                tissue(1);
+            }
             if (DISTILL) tload(0);
+            if (TTMA) tissue(2);
             uint16_t *gdst = a.gscr + static_cast<int64_t>(((blockIdx.x * G_SLOTS + g) * 2) * 128 + r) * 128;
             float zt = 0.f;
 #pragma unroll 1
@@ -445,7 +494,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 if (DISTILL) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) tcur[i] = tw[i];
-                    if (q + 1 < BWD_BN / 32) tload(q + 1);
+                    if (q + 1 < BWD_BN / 32) {
+                        tload(q + 1);
+                        if (TTMA && q + 3 < BWD_BN / 32) tissue(q + 3);
+                    }
                 }
                 tmem_ld_wait();
                 uint32_t pk[16];
@@ -483,6 +535,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 st_global_v8(dst + 16, pk + 8);
             }
             if (FUSED) zsum += static_cast<double>(zt);
+            if (TTMA && !__all_sync(0xffffffffu, tok_all)) return false;
             // the tile is out of TMEM: give the buffer back, then publish the slot
             tc_fence_before();
             mbar_arrive(tempty);
@@ -578,6 +631,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             zsum = zsum2;
             m0 = m02;
         }
+        if (TTMA)
+            for (int k = tuse_all; k < tiss_all; ++k) bw_wait_drain(&tw_b[k & 1], (k >> 1) & 1);
         tc_fence_before();
     }
     __syncthreads();
@@ -594,11 +649,12 @@ template <int MODE, bool DISTILL>
 static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st)
 {
     auto k = bwd_kernel<MODE, DISTILL>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM);
+    constexpr int SMEM = bwd_smem<MODE, DISTILL>();
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = B_SMEM;
+    cfg.dynamicSmemBytes = SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

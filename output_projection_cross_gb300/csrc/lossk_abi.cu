@@ -62,6 +62,22 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// A 2-D bf16 tensor [outer][inner] read in boxes of {box_inner, box_outer}
+// without swizzle (row-major in shared memory); out-of-range elements read as zero.
+bool make_map_plain(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, uint32_t box_inner,
+                    uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A 2-D bf16 tensor [outer][inner] (row pitch inner*2 bytes) read in boxes of
 // {box_inner, box_outer} with the 128-byte swizzle; out-of-range elements
 // read as zero.
@@ -282,6 +298,8 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             BwdArgs a;
             if (!bwd_args(w, rows, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
             a.teacher = distill ? static_cast<const uint16_t *>(teacher) : nullptr;
+            if (distill && !rows && !make_map_plain(&a.map_teach, teacher, V, n, 32, 32))
+                return LOSSK_DEVICE_ERROR;
             a.n_split = rows ? static_cast<int>(L.nsplit) : 1;
             a.direction = direction;
             a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
