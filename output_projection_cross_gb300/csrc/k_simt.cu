@@ -12,8 +12,10 @@
 //   reduce         fixed-shape double-precision tree over tokens -> the means
 //   tokp_ce        per-token backward parameters of the label loss
 //   sum_splits     d_hidden partials of the vocabulary splits, in split order
-//   tgt_logit      fused path: the target logit s[t][y_t] per token and the
-//                  reference shift r_t the fused pass exponentiates against
+//   tgt_logit      the target logit s[t][y_t] per token and the reference
+//                  shift r_t the fused pass exponentiates against
+//   validate_tgt   the training step's first launch: validate and tgt_logit
+//                  in one pass
 //   merge_fused    fused path: per token, the pass's sums of 2^(s log2e - r_t)
 //                  -> lse, ce, z and the backward parameters; flags a row
 //                  whose sum left the range the shift covers
@@ -486,6 +488,73 @@ __global__ void __launch_bounds__(256) tgt_logit_kernel(const uint16_t *__restri
         tgt[t] = acc;
         tokp[t] = make_float4(fmaf(acc, static_cast<float>(LOG2E), FUSED_SHIFT), 0.f, 0.f, 0.f);
     }
+}
+
+// The training step's first kernel: validation (target range, counted
+// tokens) and the target logit with its reference shift in one pass, one
+// warp per token.  An out-of-range target is counted and its weight row never
+// read (the call then refuses with 586 before anything else runs).
+__global__ void __launch_bounds__(256) validate_tgt_kernel(const uint16_t *__restrict__ H,
+                                                           const uint16_t *__restrict__ W,
+                                                           const int64_t *__restrict__ targets,
+                                                           const uint8_t *__restrict__ mask, int64_t n,
+                                                           int64_t d, int64_t V, int64_t n_pad,
+                                                           WsHeader *hdr, float *__restrict__ tgt,
+                                                           float4 *__restrict__ tokp)
+{
+    __shared__ int sbad, svalid;
+    if (threadIdx.x == 0) { sbad = 0; svalid = 0; }
+    __syncthreads();
+    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t < n_pad) {
+        float acc = 0.f;
+        bool in = false;
+        if (t < n) {
+            const int64_t y = targets[t];
+            in = y >= 0 && y < V;
+            if (lane == 0) {
+                if (!in) atomicAdd(&sbad, 1);
+                if (mask ? (mask[t] != 0) : true) atomicAdd(&svalid, 1);
+            }
+            if (in) {
+                const uint4 *h = reinterpret_cast<const uint4 *>(H + t * d);
+                const uint4 *w = reinterpret_cast<const uint4 *>(W + y * d);
+                for (int64_t k = lane; k < d / 8; k += 32) {
+                    const uint4 a = h[k], b = w[k];
+                    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
+                    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
+                    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
+                    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
+                    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
+                    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
+                    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
+                    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+                }
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            }
+        }
+        if (lane == 0) {
+            tgt[t] = in ? acc : 0.f;
+            tokp[t] = make_float4(in ? fmaf(acc, static_cast<float>(LOG2E), FUSED_SHIFT) : 0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (sbad) atomicAdd(&hdr->bad_targets, sbad);
+        if (svalid) atomicAdd(&hdr->n_valid, svalid);
+    }
+}
+
+cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int64_t *targets,
+                                const uint8_t *mask, int64_t n, int64_t d, int64_t V, int64_t n_pad,
+                                WsHeader *hdr, float *tgt, float4 *tokp, cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 3 * sizeof(int), st);   // bad, n_valid, redo
+    if (e != cudaSuccess) return e;
+    validate_tgt_kernel<<<static_cast<unsigned>((n_pad + 7) / 8), 256, 0, st>>>(H, W, targets, mask, n, d, V,
+                                                                              n_pad, hdr, tgt, tokp);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,

@@ -164,12 +164,25 @@ struct Hdr {
 int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DEVICE_ERROR; }
 
 // Run the validation kernel and read its result back (the one sync of a call).
+// `fused` (the bf16 training step): the same validation in one launch with the
+// target logits and reference shifts the fused pass needs (written to tgt/tokp).
+struct FusedPre {
+    const void *H, *W;
+    int64_t d, n_pad;
+    float *tgt;
+    float4 *tokp;
+};
+
 int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V, WsHeader *hdr,
-                 cudaStream_t st, Hdr *h)
+                 cudaStream_t st, Hdr *h, const FusedPre *fused = nullptr)
 {
     {
         Launch k(KK_VALIDATE, st);
-        if (launch_validate(targets, mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+        cudaError_t e = fused ? launch_validate_tgt(static_cast<const uint16_t *>(fused->H),
+                                                    static_cast<const uint16_t *>(fused->W), targets, mask, n,
+                                                    fused->d, V, fused->n_pad, hdr, fused->tgt, fused->tokp, st)
+                              : launch_validate(targets, mask, n, V, hdr, st);
+        if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     }
     int buf[3] = {0, 0, 0};
     if (cudaMemcpyAsync(buf, hdr, sizeof(buf), cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -348,7 +361,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
 // ---- forward + d_hidden in one pass (label CE, bf16) ---------------------------
 // The d_hidden schedule of the backward run before any lse exists: every logit
 // is exponentiated against the per-token shift r_t = s[t][y_t] log2e + 64
-// (tgt_logit), the pass accumulates D = G' W and reports the sums of G'
+// (computed with the validation), the pass accumulates D = G' W and reports the sums of G'
 // (BWD_FUSED in k_bwd.cu), merge_fused turns the sums into lse, ce, z and the
 // d_weight parameters, and combine_dh scales D into d_hidden.  One logit pass
 // less than the separate forward and d_hidden passes.  A row whose shifted
@@ -389,14 +402,10 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
                   float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st,
                   cudaStream_t aux, cudaEvent_t fork, bool sum)
 {
+    // the target logits and reference shifts came with the validation launch
     const WsLayout &L = w.L;
-    const uint16_t *Hb = static_cast<const uint16_t *>(H), *Wb = static_cast<const uint16_t *>(W);
+    const uint16_t *Wb = static_cast<const uint16_t *>(W);
     cudaError_t e;
-    {
-        Launch k(KK_TGT_LOGIT, st);
-        e = launch_tgt_logit(Hb, Wb, targets, n, d, L.n_pad, w.tgt(), w.tokp(), st);
-    }
-    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     const BwdGeom g = bwd_geometry(d, false);
     BwdArgs a;
     if (!bwd_args(w, true, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
@@ -649,11 +658,13 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     w.base = static_cast<uint8_t *>(workspace);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Hdr h;
-    s = validate(targets, mask, n, V, w.hdr(), st, &h);
+    const bool fused_path = do_fwd && do_bwd && dH && dtype == LOSSK_BF16;
+    const FusedPre pre{H, W, d, w.L.n_pad, w.tgt(), w.tokp()};
+    s = validate(targets, mask, n, V, w.hdr(), st, &h, fused_path ? &pre : nullptr);
     if (s != LOSSK_OK) return s;
     // gradient of grad_scale * total: a_t = grad_scale m_t / N_valid (mean) or grad_scale m_t (sum)
     const double alpha = sum ? gs : (h.n_valid > 0 ? gs / h.n_valid : 0.0);
-    if (do_fwd && do_bwd && dH && dtype == LOSSK_BF16) {
+    if (fused_path) {
         // With accumulation, d_hidden is formed in the workspace and the
         // caller's gradients are touched only once the fused pass's range
         // check has come back clean.

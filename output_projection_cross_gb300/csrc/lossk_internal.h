@@ -201,6 +201,10 @@ cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, 
 // The fused forward + d_hidden path (label CE, bf16): target logit and
 // reference shift per token; merge of the fused pass's sums into lse, ce, z
 // and the backward parameters; d_hidden from the split partials.
+// Validation and the target logit / reference shift in one launch (the bf16 training step).
+cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int64_t *targets,
+                                const uint8_t *mask, int64_t n, int64_t d, int64_t V, int64_t n_pad,
+                                WsHeader *hdr, float *tgt, float4 *tokp, cudaStream_t st);
 cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
                              int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st);
 cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,

@@ -187,8 +187,9 @@ def test_fused_forward_dhidden_path_is_the_one_that_runs(L):
     x = _inputs("ce_512x1024x32000", seed=8, n_tok=n, d_model=d, vocab=V)
     H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
     k = _kernels_run(L, lambda: L.lossk_ce_fwd_bwd(H, W, y, z_weight=1e-3))
-    assert {"tgt_logit", "tc_fused", "merge_fused", "combine_dh", "tc_cols"} <= set(k)
-    assert "tc_stats" not in k and "tc_rows" not in k
+    assert {"validate", "tc_fused", "merge_fused", "combine_dh", "tc_cols"} <= set(k)
+    # the target logits come with the validation launch on this path
+    assert "tc_stats" not in k and "tc_rows" not in k and "tgt_logit" not in k
     # without d_hidden there is nothing to fold: the separate forward runs
     k = _kernels_run(L, lambda: L.lossk_ce_fwd_bwd(H, W, y, want_d_hidden=False))
     assert "tc_stats" in k and "tc_fused" not in k
