@@ -22,14 +22,19 @@
  *    contiguous row-major array; the library never allocates device memory.
  *    Each tensor comes with its element count (`*_len`); a count shorter than
  *    the shape needs, or a NULL required pointer, gives 582.
- *  - dtype: LOSSK_BF16 (uint16 bf16 bits) or LOSSK_F32 (float) for hidden,
- *    weight, logits and teacher logits.  bf16 inputs are multiplied on the
- *    tcgen05 tensor cores with fp32 accumulation; fp32 inputs use an FFMA
- *    path.  Per-token outputs are float, gradients are float, the three
- *    reduced scalars are double.  The bf16 tensor path loads operands with
- *    TMA, which needs 16-byte row pitches: d_model % 8 == 0 (and, for the
- *    teacher logits, vocab % 8 == 0), else 591.  Every device pointer must be
- *    16-byte aligned, else 591.
+ *  - dtype: LOSSK_BF16 (uint16 bf16 bits), LOSSK_F16 (uint16 IEEE half bits)
+ *    or LOSSK_F32 (float) for hidden, weight, logits and teacher logits.
+ *    16-bit inputs are multiplied on the tcgen05 tensor cores with fp32
+ *    accumulation; fp32 inputs use an FFMA path.  Per-token outputs are
+ *    float, gradients are float (grad_logits take the logits' dtype), the
+ *    three reduced scalars are double.  fp16 grad tiles hold the gradient
+ *    without its common factor grad_scale / N_valid (applied in fp32 when the
+ *    accumulators are stored), so they stay inside fp16's range; the training
+ *    step's single-pass forward + d_hidden needs bf16's exponent range and is
+ *    bf16 only (fp16 runs the separate passes).  The 16-bit tensor path loads
+ *    operands with TMA, which needs 16-byte row pitches: d_model % 8 == 0
+ *    (and, for the teacher logits, vocab % 8 == 0), else 591.  Every device
+ *    pointer must be 16-byte aligned, else 591.
  *  - Scratch: `workspace` is device memory of at least
  *    lossk_workspace_bytes(...) bytes, 256-byte aligned; shorter gives 582.
  *    Calls that share a workspace must not overlap in time.
@@ -103,7 +108,7 @@ enum lossk_status {
  * parity suite of "Fuse distillation + z-loss ...", "Testing". */
 enum lossk_flags { LOSSK_ACCUMULATE_GRADS = 1, LOSSK_REDUCE_SUM = 2 };
 
-enum lossk_dtype { LOSSK_F32 = 0, LOSSK_BF16 = 1 };
+enum lossk_dtype { LOSSK_F32 = 0, LOSSK_BF16 = 1, LOSSK_F16 = 2 };
 
 /* Distillation objective ("Fuse distillation + z-loss ...", "What it
  * does": cross-entropy, forward-KL, reverse-KL).  Any other value -> 588. */

@@ -77,11 +77,25 @@ def to_bf16_values(x: np.ndarray) -> np.ndarray:
         torch.bfloat16).to(torch.float32).numpy()
 
 
+def to_f16_values(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE half (RNE) and return them widened to float32."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """The values a tensor of `dtype` ("bf16", "f16" or "fp32") holds."""
+    if dtype == "bf16":
+        return to_bf16_values(x)
+    if dtype == "f16":
+        return to_f16_values(x)
+    return x
+
+
 def _normal(seed, stream, shape, std, dtype, batch=0):
     x = rng(seed, stream, batch).standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
-    return to_bf16_values(x) if dtype == "bf16" else x
+    return round_to(x, dtype)
 
 
 def hidden(seed, n, d, std=1.0, dtype="bf16", batch=0):
@@ -92,8 +106,8 @@ def weight(seed, V, d, std=0.02, dtype="bf16"):
     return _normal(seed, STREAM_WEIGHT, (V, d), std, dtype)
 
 
-def teacher(seed, n, V, std=3.0, batch=0):
-    return _normal(seed, STREAM_TEACHER, (n, V), std, "bf16", batch)
+def teacher(seed, n, V, std=3.0, batch=0, dtype="bf16"):
+    return _normal(seed, STREAM_TEACHER, (n, V), std, dtype, batch)
 
 
 def targets(seed, n, V, kind="uniform", batch=0):

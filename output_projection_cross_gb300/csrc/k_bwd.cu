@@ -82,8 +82,6 @@ template <int MODE, bool DISTILL> constexpr int bwd_smem()
 static_assert(bwd_smem<BWD_COLS, true>() <= 232448, "fits the 227 KB per-CTA shared memory limit");
 static_assert(BWD_BN == 256 && TC_SLICE == 256, "one 256-column logit buffer + one 256-column accumulator");
 
-__device__ __forceinline__ float bw_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bw_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __device__ __forceinline__ void bw_wait_drain(uint64_t *bar, uint32_t parity)
 {
@@ -135,7 +133,11 @@ __device__ __forceinline__ void cnt_inc(int (&cnt)[B_MAXC], int i)
 
 } // namespace
 
-template <int MODE, bool DISTILL>
+// F16: fp16 operands (hidden, weight, teacher).  The grad tile then holds
+// G / out_scale (every per-token coefficient without the common factor
+// grad_scale / N_valid, so it stays inside fp16's range) and the accumulator
+// is multiplied by out_scale when it is stored.
+template <int MODE, bool DISTILL, bool F16>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
 {
     constexpr bool FUSED = MODE == BWD_FUSED;
@@ -280,8 +282,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             if (issued & (1u << s)) bw_wait_drain(&full[s], (last_ph >> s) & 1);
     } else if (warp == 1 && lane == 0) {
         // ================= MMA issuer =================
-        constexpr uint32_t ID_S = idesc_bf16_f32(128, BWD_BN, 0, 0);
-        constexpr uint32_t ID_ACC = idesc_bf16_f32(128, TC_SLICE, 0, 1);
+        constexpr uint32_t ID_S = idesc_16_f32(128, BWD_BN, 0, 0, F16);
+        constexpr uint32_t ID_ACC = idesc_16_f32(128, TC_SLICE, 0, 1, F16);
         int st = 0;
         uint32_t ph = 0;
         bool ok = true, first_acc = true;
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                             if (ROWS ? (rel == j) : (__float_as_int(Pq.w) == fixrow)) gv -= Pq.z;
                             gg[uu] = gv;
                         } else {
-                            const float tv = uu ? bw_hi(tcur[i >> 1]) : bw_lo(tcur[i >> 1]);
+                            const float tv = uu ? h16_hi<F16>(tcur[i >> 1]) : h16_lo<F16>(tcur[i >> 1]);
                             const float a2 = s * kT, b2 = tv * kT;
                             const float qv = ex2_approx(a2 - Pq.x);
                             if (a.direction == DIR_RKL)
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                                 gg[uu] = Pq.z * qv - Pq.w * ex2_approx(b2 - Pq.y);
                         }
                     }
-                    pk[i >> 1] = pack_bf16x2(gg[0], gg[1]);
+                    pk[i >> 1] = pack_16x2<F16>(gg[0], gg[1]);
                 }
                 // columns q*32 .. q*32+31: sub-tile q/4, 64 bytes at column (q%4)*32
                 uint16_t *dst = gdst + (q >> 2) * (128 * 128) + (q & 3) * 32;
@@ -608,6 +610,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 for (int h = 0; h < 2; ++h) {
                     const int col = slice0 + (q + h) * 32;
                     if (fixrow < n_rows && col < a.d) {
+                        if (F16) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) * a.out_scale);
+                        }
                         if (a.accumulate) {
                             // gradient accumulation: out += this unit's accumulator
                             for (int i = 0; i < 32; ++i)
@@ -645,10 +652,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     }
 }
 
-template <int MODE, bool DISTILL>
+template <int MODE, bool DISTILL, bool F16>
 static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st)
 {
-    auto k = bwd_kernel<MODE, DISTILL>;
+    auto k = bwd_kernel<MODE, DISTILL, F16>;
     constexpr int SMEM = bwd_smem<MODE, DISTILL>();
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
@@ -678,13 +685,22 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int n_units, cudaStream_t st)
+cudaError_t launch_bwd(int mode, bool distill, bool f16, const BwdArgs &a, int n_units, cudaStream_t st)
 {
     if (a.n_cl < 1 || a.n_cl > B_MAXC) return cudaErrorInvalidValue;
-    if (mode == BWD_FUSED) return launch_bwd_one<BWD_FUSED, false>(a, n_units, st);
+    if (mode == BWD_FUSED) return f16 ? cudaErrorInvalidValue : launch_bwd_one<BWD_FUSED, false, false>(a, n_units, st);
+    if (f16) {
+        if (mode == BWD_ROWS)
+            return distill ? launch_bwd_one<BWD_ROWS, true, true>(a, n_units, st)
+                           : launch_bwd_one<BWD_ROWS, false, true>(a, n_units, st);
+        return distill ? launch_bwd_one<BWD_COLS, true, true>(a, n_units, st)
+                       : launch_bwd_one<BWD_COLS, false, true>(a, n_units, st);
+    }
     if (mode == BWD_ROWS)
-        return distill ? launch_bwd_one<BWD_ROWS, true>(a, n_units, st) : launch_bwd_one<BWD_ROWS, false>(a, n_units, st);
-    return distill ? launch_bwd_one<BWD_COLS, true>(a, n_units, st) : launch_bwd_one<BWD_COLS, false>(a, n_units, st);
+        return distill ? launch_bwd_one<BWD_ROWS, true, false>(a, n_units, st)
+                       : launch_bwd_one<BWD_ROWS, false, false>(a, n_units, st);
+    return distill ? launch_bwd_one<BWD_COLS, true, false>(a, n_units, st)
+                   : launch_bwd_one<BWD_COLS, false, false>(a, n_units, st);
 }
 
 } // namespace lossk

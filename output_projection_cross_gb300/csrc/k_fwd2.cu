@@ -1,7 +1,7 @@
 // k_fwd2.cu -- forward statistics of the label cross-entropy on CTA pairs.
 //
 // The forward reduces each logit tile S = H_tile . W_tile^T to per-token
-// (running max, sum of exp) pairs (the target logit comes from tgt_logit) -- the online
+// (running max, sum of exp) pairs (the target logit comes from a separate kernel) -- the online
 // log-sum-exp of "Loss functions and resident-context kernels" (lossk: a
 // chunk's logits are reduced as soon as they exist).  Here two CTAs of a
 // cluster act as one tcgen05 unit (cta_group::2): a 256-token x 256-vocabulary
@@ -47,7 +47,8 @@ __device__ __forceinline__ void f2_wait_drain(uint64_t *bar, uint32_t parity)
 
 } // namespace
 
-template <bool DISTILL>
+// F16: fp16 operands and teacher logits instead of bf16.
+template <bool DISTILL, bool F16>
 __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
         }
     } else if (warp == 1 && lane == 0 && lead) {
         // ================= MMA issuer (even CTA) =================
-        constexpr uint32_t ID = idesc_bf16_f32(256, F2_BN, 0, 0);
+        constexpr uint32_t ID = idesc_16_f32(256, F2_BN, 0, 0, F16);
         int st = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -198,8 +199,8 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
                         const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            bt[c4 * 8 + 2 * e] = __uint_as_float(ww[e] << 16) * kS;
-                            bt[c4 * 8 + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u) * kS;
+                            bt[c4 * 8 + 2 * e] = h16_lo<F16>(ww[e]) * kS;
+                            bt[c4 * 8 + 2 * e + 1] = h16_hi<F16>(ww[e]) * kS;
                         }
                     }
                 }
@@ -255,9 +256,9 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
     }
 }
 
-template <bool DISTILL> static cudaError_t launch_fwd2_one(const TcArgs &a, int grid, cudaStream_t st)
+template <bool DISTILL, bool F16> static cudaError_t launch_fwd2_one(const TcArgs &a, int grid, cudaStream_t st)
 {
-    auto k = fwd2_kernel<DISTILL>;
+    auto k = fwd2_kernel<DISTILL, F16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F2_SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -275,9 +276,10 @@ template <bool DISTILL> static cudaError_t launch_fwd2_one(const TcArgs &a, int 
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-cudaError_t launch_fwd2(const TcArgs &a, bool distill, int grid, cudaStream_t st)
+cudaError_t launch_fwd2(const TcArgs &a, bool distill, bool f16, int grid, cudaStream_t st)
 {
-    return distill ? launch_fwd2_one<true>(a, grid, st) : launch_fwd2_one<false>(a, grid, st);
+    if (f16) return distill ? launch_fwd2_one<true, true>(a, grid, st) : launch_fwd2_one<false, true>(a, grid, st);
+    return distill ? launch_fwd2_one<true, false>(a, grid, st) : launch_fwd2_one<false, false>(a, grid, st);
 }
 
 } // namespace lossk

@@ -143,6 +143,10 @@ cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *
 // (max, sum, weighted sum) over 16-byte groups of its row; the threads are then
 // merged by a fixed tree.  The sums are fp32 per thread for bf16 teachers and
 // fp64 for fp32 teachers (whose tolerance is 1e-6).
+// T: float, uint16_t (bf16 bits) or h16_t (fp16 bits).
+template <typename T> constexpr bool kIsF16 = false;
+template <> constexpr bool kIsF16<h16_t> = true;
+
 template <typename T> struct TeachAcc { using type = float; };
 template <> struct TeachAcc<float> { using type = double; };
 
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
             }
     };
     if constexpr (sizeof(T) == 2) {
-        // bf16: V % 8 == 0, so every row starts 16-byte aligned
+        // 16-bit: V % 8 == 0, so every row starts 16-byte aligned
         const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
         const int64_t nvec = V / VEC;
         for (int64_t v0 = lane; v0 < nvec; v0 += UNR * 32) {
@@ -209,8 +213,8 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
                 float x[VEC];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    x[2 * i] = __uint_as_float(q[i] << 16);
-                    x[2 * i + 1] = __uint_as_float(q[i] & 0xFFFF0000u);
+                    x[2 * i] = h16_lo<kIsF16<T>>(q[i]);
+                    x[2 * i + 1] = h16_hi<kIsF16<T>>(q[i]);
                 }
                 absorb(x, VEC);
             }
@@ -243,13 +247,15 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
     }
 }
 
-cudaError_t launch_teacher_stats(int dtype_bf16, const void *teach, int64_t n, int64_t V, double temperature,
+cudaError_t launch_teacher_stats(int dtype, const void *teach, int64_t n, int64_t V, double temperature,
                                  double2 *out, cudaStream_t st)
 {
     const float kT = static_cast<float>(LOG2E / temperature);
     const unsigned grid = static_cast<unsigned>((n + 7) / 8);
-    if (dtype_bf16)
+    if (dtype == 1)
         teacher_stats_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(teach), n, V, kT, out);
+    else if (dtype == 2)
+        teacher_stats_kernel<h16_t><<<grid, 256, 0, st>>>(static_cast<const h16_t *>(teach), n, V, kT, out);
     else
         teacher_stats_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(teach), n, V, kT, out);
     return cudaGetLastError();
@@ -453,6 +459,7 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 // One warp per token: 16-byte loads of the hidden row and the target's weight
 // row, fp32 products summed per lane in k order, then a fixed xor tree.
+template <bool F16>
 __global__ void __launch_bounds__(256) tgt_logit_kernel(const uint16_t *__restrict__ H,
                                                         const uint16_t *__restrict__ W,
                                                         const int64_t *__restrict__ targets, int64_t n,
@@ -474,14 +481,14 @@ __global__ void __launch_bounds__(256) tgt_logit_kernel(const uint16_t *__restri
     float acc = 0.f;
     for (int64_t k = lane; k < d / 8; k += 32) {
         const uint4 a = h[k], b = w[k];
-        acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
-        acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
-        acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
-        acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
-        acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
-        acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
-        acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
-        acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+        acc = fmaf(h16_lo<F16>(a.x), h16_lo<F16>(b.x), acc);
+        acc = fmaf(h16_hi<F16>(a.x), h16_hi<F16>(b.x), acc);
+        acc = fmaf(h16_lo<F16>(a.y), h16_lo<F16>(b.y), acc);
+        acc = fmaf(h16_hi<F16>(a.y), h16_hi<F16>(b.y), acc);
+        acc = fmaf(h16_lo<F16>(a.z), h16_lo<F16>(b.z), acc);
+        acc = fmaf(h16_hi<F16>(a.z), h16_hi<F16>(b.z), acc);
+        acc = fmaf(h16_lo<F16>(a.w), h16_lo<F16>(b.w), acc);
+        acc = fmaf(h16_hi<F16>(a.w), h16_hi<F16>(b.w), acc);
     }
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
@@ -494,6 +501,7 @@ __global__ void __launch_bounds__(256) tgt_logit_kernel(const uint16_t *__restri
 // tokens) and the target logit with its reference shift in one pass, one
 // warp per token.  An out-of-range target is counted and its weight row never
 // read (the call then refuses with 586 before anything else runs).
+template <bool F16>
 __global__ void __launch_bounds__(256) validate_tgt_kernel(const uint16_t *__restrict__ H,
                                                            const uint16_t *__restrict__ W,
                                                            const int64_t *__restrict__ targets,
@@ -522,14 +530,14 @@ __global__ void __launch_bounds__(256) validate_tgt_kernel(const uint16_t *__res
                 const uint4 *w = reinterpret_cast<const uint4 *>(W + y * d);
                 for (int64_t k = lane; k < d / 8; k += 32) {
                     const uint4 a = h[k], b = w[k];
-                    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
-                    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
-                    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
-                    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
-                    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
-                    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
-                    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
-                    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+                    acc = fmaf(h16_lo<F16>(a.x), h16_lo<F16>(b.x), acc);
+                    acc = fmaf(h16_hi<F16>(a.x), h16_hi<F16>(b.x), acc);
+                    acc = fmaf(h16_lo<F16>(a.y), h16_lo<F16>(b.y), acc);
+                    acc = fmaf(h16_hi<F16>(a.y), h16_hi<F16>(b.y), acc);
+                    acc = fmaf(h16_lo<F16>(a.z), h16_lo<F16>(b.z), acc);
+                    acc = fmaf(h16_hi<F16>(a.z), h16_hi<F16>(b.z), acc);
+                    acc = fmaf(h16_lo<F16>(a.w), h16_lo<F16>(b.w), acc);
+                    acc = fmaf(h16_hi<F16>(a.w), h16_hi<F16>(b.w), acc);
                 }
                 for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             }
@@ -552,16 +560,17 @@ cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int6
 {
     cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 3 * sizeof(int), st);   // bad, n_valid, redo
     if (e != cudaSuccess) return e;
-    validate_tgt_kernel<<<static_cast<unsigned>((n_pad + 7) / 8), 256, 0, st>>>(H, W, targets, mask, n, d, V,
-                                                                              n_pad, hdr, tgt, tokp);
+    validate_tgt_kernel<false><<<static_cast<unsigned>((n_pad + 7) / 8), 256, 0, st>>>(H, W, targets, mask, n, d,
+                                                                                     V, n_pad, hdr, tgt, tokp);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
+cudaError_t launch_tgt_logit(bool f16, const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
                              int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st)
 {
-    tgt_logit_kernel<<<static_cast<unsigned>((n_pad + 7) / 8), 256, 0, st>>>(H, W, targets, n, d, n_pad,
-                                                                          tgt, tokp);
+    const unsigned grid = static_cast<unsigned>((n_pad + 7) / 8);
+    if (f16) tgt_logit_kernel<true><<<grid, 256, 0, st>>>(H, W, targets, n, d, n_pad, tgt, tokp);
+    else tgt_logit_kernel<false><<<grid, 256, 0, st>>>(H, W, targets, n, d, n_pad, tgt, tokp);
     return cudaGetLastError();
 }
 
@@ -668,9 +677,15 @@ cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int6
 template <typename T> struct Vec;
 template <> struct Vec<float> { static constexpr int N = 4; };
 template <> struct Vec<uint16_t> { static constexpr int N = 8; };
+template <> struct Vec<h16_t> { static constexpr int N = 8; };
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+__device__ __forceinline__ float to_f(h16_t x) { return f16_to_f(x.bits); }
+// One gradient value rounded to the element type.
+__device__ __forceinline__ void from_f(float v, float &o) { o = v; }
+__device__ __forceinline__ void from_f(float v, uint16_t &o) { o = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
+__device__ __forceinline__ void from_f(float v, h16_t &o) { o.bits = static_cast<uint16_t>(pack_f16x2(v, 0.f) & 0xFFFFu); }
 
 // 16-byte loads of a logit row.  `keep` leaves the line in L2 (the row is read
 // again for its gradient); otherwise the load streams past L2.
@@ -683,17 +698,27 @@ __device__ __forceinline__ void load_vec<float>(const float *p, float *f, bool k
     const float4 v = keep ? __ldg(q) : __ldcs(q);
     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
 }
-template <>
-__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *p, float *f, bool keep)
+template <bool F16>
+__device__ __forceinline__ void load_vec16(const void *p, float *f, bool keep)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
     const uint4 v = keep ? __ldg(q) : __ldcs(q);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        f[2 * i] = h16_lo<F16>(w[i]);
+        f[2 * i + 1] = h16_hi<F16>(w[i]);
     }
+}
+template <>
+__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *p, float *f, bool keep)
+{
+    load_vec16<false>(p, f, keep);
+}
+template <>
+__device__ __forceinline__ void load_vec<h16_t>(const h16_t *p, float *f, bool keep)
+{
+    load_vec16<true>(p, f, keep);
 }
 
 // 16-byte streaming store of NV gradient values.
@@ -705,6 +730,11 @@ __device__ __forceinline__ void store_vec(uint16_t *p, const float *g)
 {
     __stcs(reinterpret_cast<uint4 *>(p), make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
                                                     pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7])));
+}
+__device__ __forceinline__ void store_vec(h16_t *p, const float *g)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), make_uint4(pack_f16x2(g[0], g[1]), pack_f16x2(g[2], g[3]),
+                                                    pack_f16x2(g[4], g[5]), pack_f16x2(g[6], g[7])));
 }
 
 __device__ __forceinline__ void online_add(float &m, float &z, float x2)
@@ -810,11 +840,7 @@ __global__ void __launch_bounds__(512) from_logits_kernel(const T *__restrict__ 
     for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
         float gv = c * ex2_approx(fmaf(to_f(x[i]), L2E, -lse2));
         if (i == y) gv -= at;
-        if constexpr (sizeof(T) == 4) {
-            g[i] = gv;
-        } else {
-            g[i] = static_cast<uint16_t>(pack_bf16x2(gv, 0.f) & 0xFFFFu);
-        }
+        from_f(gv, g[i]);
     }
 }
 
@@ -828,6 +854,10 @@ cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *tar
         from_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
             static_cast<const uint16_t *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
             tokacc, n_pad, static_cast<uint16_t *>(grad));
+    else if (dtype == 2)
+        from_logits_kernel<h16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const h16_t *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
+            tokacc, n_pad, static_cast<h16_t *>(grad));
     else
         from_logits_kernel<float><<<static_cast<unsigned>(n), 512, 0, st>>>(
             static_cast<const float *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
@@ -1000,22 +1030,22 @@ __global__ void __launch_bounds__(512) distill_logits_kernel(
     for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
         float v = gval(to_f(xs[i]) * kT, to_f(xt[i]) * kT);
         if (accumulate) v += to_f(g[i]);
-        if constexpr (sizeof(T) == 4) {
-            g[i] = v;
-        } else {
-            const uint32_t u = pack_bf16x2(v, 0.f);
-            g[i] = static_cast<uint16_t>(u & 0xFFFFu);
-        }
+        from_f(v, g[i]);
     }
 }
 
-cudaError_t launch_distill_logits(int dtype_bf16, const void *student, const void *teacher, const uint8_t *mask,
+cudaError_t launch_distill_logits(int dtype, const void *student, const void *teacher, const uint8_t *mask,
                                   int64_t n, int64_t V, int direction, double temperature, double wz,
                                   double at_on, float *lse_out, float *per_token, double *tokacc,
                                   int64_t n_pad, void *grad, bool accumulate, cudaStream_t st)
 {
     const float kT = static_cast<float>(LOG2E / temperature);
-    if (dtype_bf16)
+    if (dtype == 2)
+        distill_logits_kernel<h16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
+            static_cast<const h16_t *>(student), static_cast<const h16_t *>(teacher), mask, V, direction,
+            kT, wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<h16_t *>(grad),
+            accumulate ? 1 : 0);
+    else if (dtype == 1)
         distill_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
             static_cast<const uint16_t *>(student), static_cast<const uint16_t *>(teacher), mask, V, direction,
             kT, wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<uint16_t *>(grad),

@@ -198,6 +198,10 @@ int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t
 
 bool is_finite(double x) { return std::isfinite(x); }
 
+// 16-bit inputs (bf16 or fp16): the tensor-core path.
+bool is16(int32_t dtype) { return dtype == LOSSK_BF16 || dtype == LOSSK_F16; }
+bool dtype_ok(int32_t dtype) { return dtype == LOSSK_F32 || is16(dtype); }
+
 struct Ws {
     WsLayout L;
     uint8_t *base;
@@ -248,11 +252,11 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
 {
     const WsLayout &L = w.L;
     cudaError_t e;
-    if (dtype == LOSSK_BF16) {
+    if (is16(dtype)) {
         {
             Launch k(KK_TGT_LOGIT, st);
-            e = launch_tgt_logit(static_cast<const uint16_t *>(H), static_cast<const uint16_t *>(W), targets, n,
-                                 d, L.n_pad, w.tgt(), w.tokp(), st);
+            e = launch_tgt_logit(dtype == LOSSK_F16, static_cast<const uint16_t *>(H),
+                                 static_cast<const uint16_t *>(W), targets, n, d, L.n_pad, w.tgt(), w.tokp(), st);
         }
         if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
         // CTA pairs: 256 tokens x 256 vocabulary per MMA, each CTA loading its
@@ -277,7 +281,7 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
         a.err = &w.hdr()->err;
         const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
         Launch k(KK_TC_STATS, st);
-        e = launch_fwd2(a, false, 2 * pairs, st);
+        e = launch_fwd2(a, false, dtype == LOSSK_F16, 2 * pairs, st);
     } else {
         Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, false, H, W, nullptr, static_cast<int>(n), static_cast<int>(V),
@@ -296,14 +300,17 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
 }
 
 // ---- the two accumulate passes (d_hidden, d_weight), label CE or distill ----
+// out_scale: fp16 grad tiles carry G / out_scale (the per-token parameters were
+// formed without the common factor), which the stored accumulators get back.
 int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
                 const void *W, const void *teacher, bool distill, int direction, double temperature,
-                float *d_hidden, float *d_weight, cudaStream_t st, bool accumulate = false)
+                float *d_hidden, float *d_weight, cudaStream_t st, bool accumulate = false,
+                double out_scale = 1.0)
 {
     const WsLayout &L = w.L;
     cudaError_t e = cudaSuccess;
     const float inv_t = static_cast<float>(1.0 / temperature);
-    if (dtype == LOSSK_BF16) {
+    if (is16(dtype)) {
         for (int pass = 0; pass < 2; ++pass) {
             float *dst = pass == 0 ? d_hidden : d_weight;
             if (!dst) continue;
@@ -318,10 +325,11 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.inv_t_l2e = static_cast<float>(LOG2E / temperature);
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
             a.accumulate = (accumulate && a.out == dst) ? 1 : 0;
+            a.out_scale = static_cast<float>(out_scale);
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
-                e = launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, a, n_units, st);
+                e = launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, dtype == LOSSK_F16, a, n_units, st);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {
@@ -419,7 +427,7 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     a.err = &w.hdr()->err;
     {
         Launch k(KK_TC_FUSED, st);
-        e = launch_bwd(BWD_FUSED, false, a, a.n_fixed * a.n_split * a.n_dg, st);
+        e = launch_bwd(BWD_FUSED, false, false, a, a.n_fixed * a.n_split * a.n_dg, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
@@ -452,14 +460,14 @@ int32_t check_fused(int64_t n, int64_t d, int64_t V, int64_t chunk, bool has_chu
         s = lossk_chunk_check(chunk, V);
         if (s != LOSSK_OK) return s;
     }
-    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (!dtype_ok(dtype)) return LOSSK_LENGTH_MISMATCH;
     if (!H || !W || !workspace) return LOSSK_LENGTH_MISMATCH;
     if (hl < n * d || wl < V * d) return LOSSK_LENGTH_MISMATCH;
     if (!ws_layout(kind, n, d, V, dtype, L) || wsb < static_cast<int64_t>(L->total))
         return LOSSK_LENGTH_MISMATCH;
     if (!aligned16(H) || !aligned16(W) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return LOSSK_UNALIGNED;
-    if (dtype == LOSSK_BF16 && d % 8 != 0) return LOSSK_UNALIGNED;
+    if (is16(dtype) && d % 8 != 0) return LOSSK_UNALIGNED;
     return LOSSK_OK;
 }
 
@@ -487,7 +495,7 @@ int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
     // 144 clusters (four full waves) on the tensor-core path, and for about
     // two CTAs per SM on the FFMA path.  Shape-only, so results never depend
     // on the device.
-    const bool tc = dtype == LOSSK_BF16;
+    const bool tc = is16(dtype);
     const int64_t bm = tc ? TC_BM : FP_BM, bn = tc ? TC_BN_ACC : FP_BN, sl = tc ? TC_SLICE : FP_SLICE;
     const int64_t n_yt = cdiv(V, bn);
     const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
@@ -508,7 +516,7 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
 {
     if (lossk_dims_check(n, d, V) != LOSSK_OK) return false;
     *L = WsLayout();
-    const bool tc = dtype == LOSSK_BF16;
+    const bool tc = is16(dtype);
     L->n_pad = cdiv(n, TC_BM) * TC_BM;
     const bool distill = kind == LOSSK_KIND_DISTILL;
     const bool chk = kind == LOSSK_KIND_CE_CHUNK_CHECK;   // a forward's layout, then the two runs' outputs
@@ -531,7 +539,7 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (bwd && L->nsplit > 1) off = align256(off + sizeof(float) * L->nsplit * n * d);
     // The training-step call on the tensor-core path folds d_hidden into the
     // forward (run_fused); it keeps the separate passes' space for its fallback.
-    const bool fused = kind == LOSSK_KIND_CE_FWD_BWD && tc;
+    const bool fused = kind == LOSSK_KIND_CE_FWD_BWD && dtype == LOSSK_BF16;
     L->off_zpart = off;
     if (fused) off = align256(off + sizeof(float) * L->nsplit * 8 * L->n_pad);
     L->off_dhc = off;
@@ -707,12 +715,16 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
         if (s != LOSSK_OK) return s;
     }
     if (do_bwd && (dH || dW)) {
+        // fp16: the grad tiles leave out the common factor alpha, which the
+        // stored accumulators get back
+        const bool f16 = dtype == LOSSK_F16;
+        const double a_tok = f16 ? (alpha != 0.0 ? 1.0 : 0.0) : alpha;
         {
             Launch k(KK_TOKP, st);
-            if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, alpha, wz, w.tokp(), st) != cudaSuccess)
+            if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, a_tok, wz, w.tokp(), st) != cudaSuccess)
                 return LOSSK_DEVICE_ERROR;
         }
-        s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st, acc);
+        s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st, acc, f16 ? alpha : 1.0);
     }
     return s;
 }
@@ -771,7 +783,7 @@ int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *lo
 {
     if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
     if (n > MAX_DIM || V > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
-    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (!dtype_ok(dtype)) return LOSSK_LENGTH_MISMATCH;
     Ws w;
     if (!ws_layout(LOSSK_KIND_FROM_LOGITS, n, 1, V, dtype, &w.L)) return LOSSK_DIMENSION_TOO_LARGE;
     if (!logits || !targets || !lse_out || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
@@ -811,7 +823,7 @@ int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk,
                             workspace, workspace_bytes, LOSSK_KIND_DISTILL, &w.L);
     if (s != LOSSK_OK) return s;
     if (!teacher || teacher_len < n * V || !scalars_out) return LOSSK_LENGTH_MISMATCH;
-    if (!aligned16(teacher) || (dtype == LOSSK_BF16 && V % 8 != 0)) return LOSSK_UNALIGNED;
+    if (!aligned16(teacher) || (is16(dtype) && V % 8 != 0)) return LOSSK_UNALIGNED;
     if (!scalars_ok(z_weight, grad_scale) || !is_finite(temperature) || temperature <= 0.0)
         return LOSSK_NON_FINITE_SCALAR;
     if (direction < LOSSK_DISTILL_CE || direction > LOSSK_DISTILL_REV_KL) return LOSSK_UNKNOWN_OBJECTIVE;
@@ -828,10 +840,10 @@ int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk,
     {
         // the teacher's own statistics: one HBM stream over the teacher logits
         Launch k(KK_TEACHER_STATS, st);
-        e = launch_teacher_stats(dtype == LOSSK_BF16, teacher, n, V, temperature, tstat, st);
+        e = launch_teacher_stats(dtype, teacher, n, V, temperature, tstat, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    if (dtype == LOSSK_BF16) {
+    if (is16(dtype)) {
         // CTA pairs, 256 tokens x 256 vocabulary per MMA, the teacher read in the epilogue
         TcArgs a;
         std::memset(&a, 0, sizeof(a));
@@ -855,7 +867,7 @@ int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk,
         a.err = &w.hdr()->err;
         const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
         Launch k(KK_TC_STATS, st);
-        e = launch_fwd2(a, true, 2 * pairs, st);
+        e = launch_fwd2(a, true, dtype == LOSSK_F16, 2 * pairs, st);
     } else {
         Launch k(KK_FP_STATS, st);
         e = launch_fp(TC_STATS, true, hidden, weight, static_cast<const float *>(teacher),
@@ -865,10 +877,13 @@ int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk,
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     const double alpha = sum ? grad_scale : (h.n_valid > 0 ? grad_scale / h.n_valid : 0.0);
+    // fp16: the grad tiles leave out the common factor alpha (as in the label loss)
+    const bool f16 = dtype == LOSSK_F16;
+    const double a_tok = f16 ? (alpha != 0.0 ? 1.0 : 0.0) : alpha;
     {
         Launch k(KK_MERGE_DISTILL, st);
         e = launch_merge_distill(w.part(), tstat, loss_mask, n, L.n_ct, L.n_pad, direction, z_weight,
-                                 lse_out, per_token_out, w.tokacc(), w.tokp(), alpha, temperature, st);
+                                 lse_out, per_token_out, w.tokacc(), w.tokp(), a_tok, temperature, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
@@ -878,7 +893,7 @@ int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk,
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     if (!d_hidden && !d_weight) return LOSSK_OK;
     return run_acc(w, n, d, V, dtype, hidden, weight, teacher, true, direction, temperature, d_hidden,
-                   d_weight, st, acc);
+                   d_weight, st, acc, f16 ? alpha : 1.0);
 }
 
 int32_t lossk_distill_fwd_bwd(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
@@ -904,7 +919,7 @@ int32_t lossk_distill_from_logits(int64_t n, int64_t V, int32_t dtype, const voi
 {
     int32_t s = lossk_dims_check(n, 1, V);
     if (s != LOSSK_OK) return s;
-    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (!dtype_ok(dtype)) return LOSSK_LENGTH_MISMATCH;
     if (!logits || !teacher || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
     if (logits_len < n * V || teacher_len < n * V || (grad_logits && grad_len < n * V))
         return LOSSK_LENGTH_MISMATCH;
@@ -928,7 +943,7 @@ int32_t lossk_distill_from_logits(int64_t n, int64_t V, int32_t dtype, const voi
     cudaError_t e;
     {
         Launch k(KK_DISTILL_LOGITS, st);
-        e = launch_distill_logits(dtype == LOSSK_BF16, logits, teacher, loss_mask, n, V, direction, temperature,
+        e = launch_distill_logits(dtype, logits, teacher, loss_mask, n, V, direction, temperature,
                                   z_weight, at_on, lse_out, per_token_out, w.tokacc(), w.L.n_pad, grad_logits,
                                   acc, st);
     }

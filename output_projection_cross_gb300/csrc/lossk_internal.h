@@ -132,6 +132,7 @@ struct BwdArgs {
     float *zpart;          // BWD_FUSED: sums of G' [n_split * n_cl][zpart_stride]
     int64_t zpart_stride;
     int accumulate;        // add the accumulator into `out` instead of overwriting it
+    float out_scale;       // fp16 operands: the factor the stored accumulator is multiplied by
     int *err;
 };
 
@@ -170,8 +171,9 @@ enum KernelKind : int {
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);
 // Persistent clusters: at most as many as fit at once, walking `n_units` units.
-cudaError_t launch_bwd(int mode, bool distill, const BwdArgs &a, int n_units, cudaStream_t st);
-cudaError_t launch_fwd2(const TcArgs &a, bool distill, int grid, cudaStream_t st);
+// f16: fp16 operands (BWD_ROWS / BWD_COLS only); otherwise bf16.
+cudaError_t launch_bwd(int mode, bool distill, bool f16, const BwdArgs &a, int n_units, cudaStream_t st);
+cudaError_t launch_fwd2(const TcArgs &a, bool distill, bool f16, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,
                       int n_x, int n_y, int d, int n_tok, int vocab, int n_split, int direction,
                       float inv_t, const int64_t *targets, const float4 *tokp, const double2 *tstat,
@@ -187,7 +189,8 @@ cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const 
                                  float *per_token, double *tokacc, float4 *tokp, double alpha,
                                  double temperature, cudaStream_t st);
 // Teacher log-sum-exp and sum p*logit per token (one block per token row).
-cudaError_t launch_teacher_stats(int dtype_bf16, const void *teach, int64_t n, int64_t V, double temperature,
+// dtype: lossk_dtype (0 fp32, 1 bf16, 2 fp16) here and in the other row-stream launchers.
+cudaError_t launch_teacher_stats(int dtype, const void *teach, int64_t n, int64_t V, double temperature,
                                  double2 *out, cudaStream_t st);
 // sum: the three scalars are sums over the tokens instead of means over N_valid.
 cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
@@ -205,7 +208,7 @@ cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, 
 cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int64_t *targets,
                                 const uint8_t *mask, int64_t n, int64_t d, int64_t V, int64_t n_pad,
                                 WsHeader *hdr, float *tgt, float4 *tokp, cudaStream_t st);
-cudaError_t launch_tgt_logit(const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
+cudaError_t launch_tgt_logit(bool f16, const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
                              int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st);
 cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,
                                const uint8_t *mask, int64_t n, int64_t n_pad, double alpha, double wz,
@@ -217,7 +220,7 @@ cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int6
 // Distillation from given student logits: per token row the losses, lse and
 // backward parameters, and grad_logits (or nothing when grad is NULL).
 // at_on: the gradient scale of a counted token before the 1/T factor.
-cudaError_t launch_distill_logits(int dtype_bf16, const void *student, const void *teacher, const uint8_t *mask,
+cudaError_t launch_distill_logits(int dtype, const void *student, const void *teacher, const uint8_t *mask,
                                   int64_t n, int64_t V, int direction, double temperature, double wz,
                                   double at_on, float *lse_out, float *per_token, double *tokacc,
                                   int64_t n_pad, void *grad, bool accumulate, cudaStream_t st);

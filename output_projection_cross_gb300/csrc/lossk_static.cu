@@ -65,7 +65,7 @@ extern "C" int32_t lossk_ce_from_logits_static(int64_t n, int64_t V, int32_t dty
 {
     if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
     if (n > STATIC_MAX_TOKENS || V > (int64_t(1) << 24)) return LOSSK_DIMENSION_TOO_LARGE;
-    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16) return LOSSK_LENGTH_MISMATCH;
+    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16 && dtype != LOSSK_F16) return LOSSK_LENGTH_MISMATCH;
     if (!logits || !targets || !lse_out || !scalars_out) return LOSSK_LENGTH_MISMATCH;
     if (logits_len < n * V || targets_len < n || (grad_logits && grad_len < n * V))
         return LOSSK_LENGTH_MISMATCH;

@@ -255,6 +255,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// The same for 16-bit operands of either kind: A and B formats 0 = f16, 1 = bf16
+// (one type for both operands of an MMA).
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, int a_mn, int b_mn, bool f16)
+{
+    return f16 ? (idesc_bf16_f32(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16_f32(M, N, a_mn, b_mn);
+}
+
 // ---- thread-block clusters ------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -404,6 +411,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A 16-bit value (the low or high half of a 32-bit word) widened to float:
+// bf16 by placing its bits in the high half, f16 by the hardware conversion.
+__device__ __forceinline__ float f16_to_f(uint32_t h)
+{
+    float f;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "r"(h));
+    return f;
+}
+// Storage type of an fp16 element (the bits; conversions go through f16_to_f
+// and pack_f16x2), distinct from uint16_t, which holds bf16.
+struct h16_t {
+    uint16_t bits;
+};
+
+template <bool F16> __device__ __forceinline__ float h16_lo(uint32_t w)
+{
+    return F16 ? f16_to_f(w & 0xFFFFu) : __uint_as_float(w << 16);
+}
+template <bool F16> __device__ __forceinline__ float h16_hi(uint32_t w)
+{
+    return F16 ? f16_to_f(w >> 16) : __uint_as_float(w & 0xFFFF0000u);
+}
+template <bool F16> __device__ __forceinline__ uint32_t pack_16x2(float lo, float hi)
+{
+    return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 } // namespace lossk

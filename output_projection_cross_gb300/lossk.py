@@ -18,7 +18,7 @@ from . import build as _build
 
 _i64, _i32, _dbl, _vp, _u32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, ctypes.c_uint32
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 KIND_CE_FWD, KIND_CE_BWD, KIND_CE_FWD_BWD, KIND_FROM_LOGITS, KIND_DISTILL, KIND_CE_CHUNK_CHECK = 0, 1, 2, 3, 4, 5
 ACCUMULATE_GRADS, REDUCE_SUM = 1, 2
 DIRECTIONS = {"ce": 0, "fkl": 1, "rkl": 2}
@@ -121,9 +121,11 @@ def _stream(stream):
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return BF16
+    if t.dtype == torch.float16:
+        return F16
     if t.dtype == torch.float32:
         return F32
-    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16, fp16 or fp32")
 
 
 def _contig(t, name):

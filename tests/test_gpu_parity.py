@@ -37,7 +37,24 @@ def _dev(a, dtype):
     t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
     if dtype == "bf16":
         return t.to(torch.bfloat16)
+    if dtype == "f16":
+        return t.to(torch.float16)
     return t
+
+
+def _tol(dtype):
+    """(loss, gradient) tolerances: the 16-bit bound for bf16 and fp16 inputs."""
+    return (F32_LOSS, F32_GRAD) if dtype == "fp32" else (BF16_LOSS, BF16_GRAD)
+
+
+def _redraw(x, dtype, seed, n, d, V, teacher=False):
+    """Inputs of another dtype (fp32 / fp16) for a parity case: same recipe."""
+    if dtype != "bf16":
+        x["hidden"] = li.hidden(seed, n, d, dtype=dtype)
+        x["weight"] = li.weight(seed, V, d, dtype=dtype)
+        if teacher:
+            x["teacher"] = li.teacher(seed, n, V, dtype=dtype)
+    return x
 
 
 def _np(t):
@@ -88,14 +105,11 @@ SMALL = [  # (n, d, V): several tiles and ragged tails in every dimension
 ]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
 @pytest.mark.parametrize("shape", SMALL)
 def test_ce_small_shapes(L, shape, dtype):
     n, d, V = shape
-    x = _inputs("ce_512x1024x32000", seed=sum(shape), n_tok=n, d_model=d, vocab=V)
-    if dtype == "fp32":
-        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
-        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    x = _redraw(_inputs("ce_512x1024x32000", seed=sum(shape), n_tok=n, d_model=d, vocab=V), dtype, 1, n, d, V)
     mask = li.mask(3, n, 0.2) if n > 4 else None
     wz, gs = 1e-3, 0.75
     H, W, y = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], "")
@@ -104,7 +118,7 @@ def test_ce_small_shapes(L, shape, dtype):
     torch.cuda.synchronize()
     ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, chunk=min(n, 64), z_weight=wz)
     dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz, grad_scale=gs)
-    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    lt, gt = _tol(dtype)
     close_loss(_np(out["lse"]), ref["lse"], lt)
     close_loss(_np(out["ce"]), ref["ce"], lt)
     close_loss(_np(out["scalars"]), [ref["total"], ref["ce_mean"], ref["z_mean"]], lt)
@@ -236,11 +250,14 @@ def test_config_512x1024x32000_full(L):
     assert rel_l2(_np(out["d_weight"]), dW) <= BF16_GRAD
 
 
-def test_qwen3_head_full_size_sampled(L):
-    """n=2048, d=1024, V=151936, Zipf targets: the launch configuration the bench times."""
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_qwen3_head_full_size_sampled(L, dtype):
+    """n=2048, d=1024, V=151936, Zipf targets: the launch configuration the bench
+    times (bf16: the training step's single-pass forward + d_hidden; fp16: the
+    separate passes with the grad tiles' common factor applied at the store)."""
     w = li.WORKLOADS["qwen3_0p6b_head"]
-    x = _inputs(w)
-    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    x = _redraw(_inputs(w), dtype, 0, w.n_tok, w.d_model, w.vocab)
+    H, W, y = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], "")
     out = L.lossk_ce_fwd_bwd(H, W, y, chunk=w.chunk)
     torch.cuda.synchronize()
     rows = np.random.default_rng(7).choice(w.n_tok, 48, replace=False)
@@ -311,7 +328,7 @@ def test_ce_z_mask_full_size_sampled(L):
 
 
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
 @pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
 @pytest.mark.parametrize("T", [1.0, 2.0])
 def test_distill_small(L, dtype, direction, T):
@@ -320,6 +337,8 @@ def test_distill_small(L, dtype, direction, T):
     if dtype == "fp32":
         x["hidden"] = li.hidden(2, n, d, dtype="fp32")
         x["weight"] = li.weight(2, V, d, dtype="fp32")
+    if dtype == "f16":
+        x = _redraw(x, "f16", 2, n, d, V, teacher=True)
     mask = li.mask(1, n, 0.1)
     wz, gs = 1e-3, 1.25
     Tt = x["teacher"]
@@ -330,7 +349,7 @@ def test_distill_small(L, dtype, direction, T):
     torch.cuda.synchronize()
     r = oracle.distill(x["hidden"], x["weight"], Tt, direction, temperature=T, mask=mask, chunk=50,
                        z_weight=wz, grad_scale=gs)
-    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS * 10, F32_GRAD)
+    lt, gt = (F32_LOSS * 10, F32_GRAD) if dtype == "fp32" else (BF16_LOSS, BF16_GRAD)
     close_loss(_np(out["per_token"]), r["per_token"], lt)
     close_loss(_np(out["lse"]), r["lse"], lt)
     close_loss(_np(out["scalars"]), [r["total"], r["distill_mean"], r["z_mean"]], lt)
@@ -388,14 +407,12 @@ def _cached_distill():
 
 
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
 @pytest.mark.parametrize("V", [9, 1000, 4099, 151936])
 def test_from_logits(L, dtype, V):
     n = 37 if V > 10000 else 129
     g = np.random.default_rng(V)
-    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
-    if dtype == "bf16":
-        X = li.to_bf16_values(X)
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
     y = g.integers(0, V, n).astype(np.int64)
     mask = (np.arange(n) % 7 != 3).astype(np.uint8)
     wz, gs = 1e-2, 1.5
@@ -403,7 +420,7 @@ def test_from_logits(L, dtype, V):
                                  grad_scale=gs, want_grad=True)
     torch.cuda.synchronize()
     r = oracle.ce_from_logits(X, y, mask=mask, z_weight=wz, grad_scale=gs, want_grad=True)
-    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    lt, gt = _tol(dtype)
     close_loss(_np(out["lse"]), r["lse"], lt)
     close_loss(_np(out["ce"]), r["ce"], lt)
     close_loss(_np(out["scalars"]), [r["total"], r["ce_mean"], r["z_mean"]], lt)
@@ -516,20 +533,17 @@ def test_device_status_clean_after_calls(L):
 # given logits.
 
 @pytest.mark.parametrize("dtype,shape", [("bf16", (300, 256, 2000)), ("bf16", (257, 520, 3000)),
-                                         ("fp32", (130, 72, 300))])
+                                         ("fp32", (130, 72, 300)), ("f16", (257, 520, 3000))])
 def test_ce_accumulate_and_sum_flags(L, dtype, shape):
     n, d, V = shape
-    x = _inputs("ce_512x1024x32000", seed=50, n_tok=n, d_model=d, vocab=V)
-    if dtype == "fp32":
-        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
-        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    x = _redraw(_inputs("ce_512x1024x32000", seed=50, n_tok=n, d_model=d, vocab=V), dtype, 1, n, d, V)
     mask = li.mask(3, n, 0.2)
     nv = int(mask.sum())
     wz, gs = 1e-3, 0.75
     H, W, y, m = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], ""), _dev(mask, "")
     ref = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz)
     dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=wz, grad_scale=gs)
-    lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+    lt, gt = _tol(dtype)
     g = torch.Generator(device="cuda").manual_seed(3)
     # starting gradients of the same order as the ones added, so that fp32 keeps the sum exact enough
     h0 = torch.randn(n, d, device="cuda", generator=g) * 1e-4
@@ -606,29 +620,24 @@ def test_unknown_flag_bits_are_refused(L):
 
 
 @pytest.mark.parametrize("dtype,shape", [("bf16", (300, 256, 2000)), ("fp32", (64, 64, 1000)),
-                                         ("bf16", (2048, 1024, 151936))])
+                                         ("bf16", (2048, 1024, 151936)), ("f16", (300, 256, 2000))])
 def test_chunk_invariance_self_check(L, dtype, shape):
     n, d, V = shape
-    x = _inputs("ce_512x1024x32000", seed=52, n_tok=n, d_model=d, vocab=V)
-    if dtype == "fp32":
-        x["hidden"] = li.hidden(1, n, d, dtype="fp32")
-        x["weight"] = li.weight(1, V, d, dtype="fp32")
+    x = _redraw(_inputs("ce_512x1024x32000", seed=52, n_tok=n, d_model=d, vocab=V), dtype, 1, n, d, V)
     delta = L.lossk_ce_chunk_invariance(_dev(x["hidden"], dtype), _dev(x["weight"], dtype),
                                         _dev(x["targets"], ""), loss_mask=_dev(li.mask(2, n, 0.1), ""),
                                         z_weight=1e-3)
     assert delta == 0.0
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
 @pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
 @pytest.mark.parametrize("V", [3000, 1003])
 def test_distill_from_logits(L, dtype, direction, V):
     n = 67
     g = np.random.default_rng(V + len(direction))
-    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
-    Tt = (g.standard_normal((n, V)) * 3).astype(np.float32)
-    if dtype == "bf16":
-        X, Tt = li.to_bf16_values(X), li.to_bf16_values(Tt)
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    Tt = li.round_to((g.standard_normal((n, V)) * 3).astype(np.float32), dtype)
     mask = li.mask(7, n, 0.15)
     for sm in (False, True):
         r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, mask=mask, z_weight=1e-3,
@@ -638,17 +647,17 @@ def test_distill_from_logits(L, dtype, direction, V):
                                         loss_mask=_dev(mask, ""), z_weight=1e-3, grad_scale=0.9,
                                         flags=flags)
         torch.cuda.synchronize()
-        lt, gt = (BF16_LOSS, BF16_GRAD) if dtype == "bf16" else (F32_LOSS, F32_GRAD)
+        lt, gt = _tol(dtype)
         close_loss(_np(o["per_token"]), r["per_token"], lt)
         close_loss(_np(o["lse"]), r["lse"], lt)
         close_loss(_np(o["scalars"]), [r["total"], r["distill_mean"], r["z_mean"]], lt)
         assert rel_l2(_np(o["grad_logits"]), r["grad"]) <= gt
     # accumulation: two calls into a zeroed gradient give twice the gradient
-    gl = torch.zeros(n, V, device="cuda", dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    gl = torch.zeros(n, V, device="cuda", dtype={"bf16": torch.bfloat16, "f16": torch.float16}.get(dtype, torch.float32))
     for _ in range(2):
         L.lossk_distill_from_logits(_dev(X, dtype), _dev(Tt, dtype), direction, temperature=1.5,
                                     loss_mask=_dev(mask, ""), z_weight=1e-3, grad_scale=0.9,
                                     flags=L.lossk.ACCUMULATE_GRADS, grad_logits=gl)
     torch.cuda.synchronize()
     r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, mask=mask, z_weight=1e-3, grad_scale=0.9)
-    assert rel_l2(_np(gl), 2 * r["grad"]) <= (BF16_GRAD if dtype == "bf16" else F32_GRAD)
+    assert rel_l2(_np(gl), 2 * r["grad"]) <= _tol(dtype)[1]
