@@ -430,9 +430,32 @@ def e2e(a, x, H, W, y, out, step, stream, n, world):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / k_e2e, world)
     # the results that came back match the device-resident step's
     assert np.array_equal(o_h[(k_e2e - 1) % 2]["scalars_out"].numpy(), out["scalars_out"].cpu().numpy())
+
+    # The host link alone (untimed for the metric): the step's copies in both
+    # directions at once, no compute -- the floor the pipelined step can reach.
+    def copies():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        s_in.wait_event(ev)
+        s_out.wait_event(ev)
+        with torch.cuda.stream(s_in):
+            hb, wb, yb = ins[0]
+            hb.copy_(hH, non_blocking=True)
+            wb.copy_(hW, non_blocking=True)
+            yb.copy_(hy, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for k, v in outs[1].items():
+                o_h[1][k].copy_(v, non_blocking=True)
+        for s in (s_in, s_out):
+            e = torch.cuda.Event()
+            e.record(s)
+            stream.wait_event(e)
+    floor_ms = _time(copies, 3, warm=1)
     return {"value": aggregate(n, world, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
-            "overlap": "next step's inputs and previous step's outputs copied during the current step"}
+            "overlap": "next step's inputs and previous step's outputs copied during the current step",
+            "copy_floor_ms": floor_ms,
+            "copy_floor": "the same copies in both directions at once with no compute (host link bound)"}
 
 
 def _time(fn, reps, warm=2):

@@ -45,7 +45,11 @@
  *    kernels run, the way the pages' functions validate first.  After that
  *    point the call returns without waiting for the GPU -- except the
  *    training-step calls on the bf16 path (lossk_ce_fwd_bwd and its _ex
- *    form), which read back one more flag at their end (see there).
+ *    form), which read back one more flag at their end (see there).  The
+ *    read-backs go through a one-warp kernel writing into mapped pinned host
+ *    memory, not through a copy engine, so large copies other streams have in
+ *    flight do not delay them; the library allocates that memory (64 bytes
+ *    per calling host thread) on a thread's first call and keeps it.
  *  - Check order (the first failing check wins): 581 empty dimension, 583
  *    dimension over 2^24, 584 n_tok*d_model*vocab over 2^46, 587 chunk*vocab
  *    over 2^27, 582 length / NULL pointer / short workspace, 591 alignment,
@@ -362,7 +366,7 @@ int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype,
  * events, adds their durations per kind into total_ms[kind] and
  * launches[kind] (host arrays of `cap` entries), and clears them if `reset`.
  * Returns the number of kinds written, or -1 on a CUDA error. */
-#define LOSSK_N_KERNELS 19
+#define LOSSK_N_KERNELS 20
 const char *lossk_kernel_name(int32_t kind);
 int64_t lossk_launch_count(void);
 int32_t lossk_profile_enable(int32_t on);

@@ -56,6 +56,20 @@ __global__ void validate_kernel(const int64_t *__restrict__ targets, const uint8
     }
 }
 
+// The host's read-back of a call's header words goes through mapped host
+// memory written by this one warp, not through a copy engine (where the
+// 16-byte copy would queue behind other streams' large copies).
+__global__ void __launch_bounds__(32) publish_header_kernel(const WsHeader *__restrict__ hdr, int *__restrict__ dst)
+{
+    if (threadIdx.x < 4) dst[threadIdx.x] = reinterpret_cast<const volatile int *>(hdr)[threadIdx.x];
+}
+
+cudaError_t launch_publish_header(const WsHeader *hdr, int *dst, cudaStream_t st)
+{
+    publish_header_kernel<<<1, 32, 0, st>>>(hdr, dst);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st)
 {

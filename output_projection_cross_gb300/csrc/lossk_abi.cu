@@ -161,6 +161,50 @@ struct Hdr {
     int err, bad, n_valid;
 };
 
+// ---- read-backs ------------------------------------------------------------------
+// A call reads a few words of its workspace header on the host: the validation
+// counts, the device error word, the fused pass's range flag.  A copy engine
+// would queue that 16-byte copy behind the large copies other streams may
+// have in flight (a training loop moving gradients to the host), stalling the
+// call for their whole duration, so a one-warp kernel writes the words into
+// mapped pinned host memory instead: one 64-byte buffer per calling host
+// thread, allocated on first use and kept for the thread's life.
+int *readback_buffer()
+{
+    thread_local int *h = nullptr;
+    if (!h) {
+        void *p = nullptr;
+        if (cudaHostAlloc(&p, 64, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        h = static_cast<int *>(p);
+    }
+    return h;
+}
+
+// The header's first four words (err, bad_targets, n_valid, redo) after all
+// work queued on `st`; synchronises `st`.
+bool read_header(const WsHeader *hdr, cudaStream_t st, int out[4])
+{
+    int *h = readback_buffer();
+    int *dptr = nullptr;
+    if (h && cudaHostGetDevicePointer(reinterpret_cast<void **>(&dptr), h, 0) == cudaSuccess) {
+        {
+            Launch k(KK_READBACK, st);
+            if (launch_publish_header(hdr, dptr, st) != cudaSuccess) return false;
+        }
+        if (cudaStreamSynchronize(st) != cudaSuccess) return false;
+        const volatile int *v = h;
+        for (int i = 0; i < 4; ++i) out[i] = v[i];
+        return true;
+    }
+    (void)cudaGetLastError();
+    // no mapped host memory: a plain copy
+    return cudaMemcpyAsync(out, hdr, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+           cudaStreamSynchronize(st) == cudaSuccess;
+}
+
 int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DEVICE_ERROR; }
 
 // Run the validation kernel and read its result back (the one sync of a call).
@@ -184,10 +228,8 @@ int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t
                               : launch_validate(targets, mask, n, V, hdr, st);
         if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     }
-    int buf[3] = {0, 0, 0};
-    if (cudaMemcpyAsync(buf, hdr, sizeof(buf), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return LOSSK_DEVICE_ERROR;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    int buf[4] = {0, 0, 0, 0};
+    if (!read_header(hdr, st, buf)) return LOSSK_DEVICE_ERROR;
     h->err = buf[0];
     h->bad = buf[1];
     h->n_valid = buf[2];
@@ -696,9 +738,7 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
         // pass could not represent (then every output is recomputed by the
         // separate passes below, which need no shift).
         int flags_d[4] = {0, 0, 0, 0};
-        if (cudaMemcpyAsync(flags_d, w.hdr(), sizeof(flags_d), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-            return LOSSK_DEVICE_ERROR;
+        if (!read_header(w.hdr(), st, flags_d)) return LOSSK_DEVICE_ERROR;
         if (flags_d[0]) return LOSSK_DEVICE_TIMEOUT;
         if (!flags_d[3]) {
             if (!acc) return LOSSK_OK;
@@ -1016,7 +1056,7 @@ const char *lossk_kernel_name(int32_t kind)
                                       "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
                                       "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
                                       "from_logits",  "tc_fused",      "tgt_logit",   "merge_fused",
-                                      "combine_dh",   "teacher_stats", "distill_logits"};
+                                      "combine_dh",   "teacher_stats", "distill_logits", "readback"};
     return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
 }
 

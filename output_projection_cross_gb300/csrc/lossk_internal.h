@@ -164,6 +164,7 @@ enum KernelKind : int {
     KK_COMBINE_DH,
     KK_TEACHER_STATS,
     KK_DISTILL_LOGITS,
+    KK_READBACK,
     KK_N
 };
 
@@ -204,6 +205,9 @@ cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, 
 // The fused forward + d_hidden path (label CE, bf16): target logit and
 // reference shift per token; merge of the fused pass's sums into lse, ce, z
 // and the backward parameters; d_hidden from the split partials.
+// Copies the header's first four words (err, bad_targets, n_valid, redo) to
+// `dst`, a device view of mapped pinned host memory (one warp, no copy engine).
+cudaError_t launch_publish_header(const WsHeader *hdr, int *dst, cudaStream_t st);
 // Validation and the target logit / reference shift in one launch (the bf16 training step).
 cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int64_t *targets,
                                 const uint8_t *mask, int64_t n, int64_t d, int64_t V, int64_t n_pad,

@@ -90,7 +90,7 @@ EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk
             "lossk_ce_fwd_bwd_ex", "lossk_distill_fwd_bwd_ex", "lossk_ce_chunk_invariance",
             "lossk_distill_from_logits",
             "lossk_ce_from_logits_static", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
-N_KERNELS = 19
+N_KERNELS = 20
 
 
 class LosskError(RuntimeError):
