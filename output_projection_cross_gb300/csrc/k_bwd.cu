@@ -68,7 +68,7 @@ namespace {
 constexpr int B_NST = 4;                          // operand ring stages
 constexpr int B_STAGE = 49152;                    // 48 KB: an A part and a B part
 constexpr int B_APART = 16384;                    // 128 rows x 64 K (bf16, 128-byte swizzle)
-constexpr int B_MAXC = 8;                         // CTAs per cluster at most
+constexpr int B_MAXC = BWD_MAX_CL;                // CTAs per cluster at most
 constexpr int B_NBARS = 2 * B_NST + 4 + B_MAXC * G_SLOTS + G_SLOTS + 1 + 8;
 // The distillation d_weight pass reads its teacher block through TMA: per
 // epilogue warp two 32-token x 32-vocabulary bf16 buffers (2 KB each).
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         int st = 0;
         uint32_t ph = 0, issued = 0, last_ph = 0;
         bool ok = true;
-        int cnt[B_MAXC] = {0, 0, 0, 0, 0, 0, 0, 0};   // tiles loaded so far, per writer
+        int cnt[B_MAXC] = {};                  // tiles loaded so far, per writer
         auto acquire = [&]() -> uint8_t * {
             if (!mbar_wait(&empty[st], ph ^ 1, err)) return nullptr;
             mbar_arrive_expect_tx(&full[st], B_STAGE);
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         uint32_t ph = 0;
         bool ok = true, first_acc = true;
         int m_all = 0;                         // own logit tiles issued so far
-        int cnt[B_MAXC] = {0, 0, 0, 0, 0, 0, 0, 0};
+        int cnt[B_MAXC] = {};
         BwdCursor cur, prev;
         cursor_set(cur, cluster, 0);
         bool have_prev = false;
@@ -659,6 +659,11 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
     constexpr int SMEM = bwd_smem<MODE, DISTILL>();
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
+    if (a.n_cl > 8) {
+        // clusters of 9-16 CTAs are beyond the portable size
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = SMEM;

@@ -522,10 +522,29 @@ namespace lossk {
 
 BwdGeom bwd_geometry(int64_t d, bool distill)
 {
+    // Per loop supertile and d-group a cluster of c CTAs spends nk + 4c stages
+    // per CTA (the logit tile over the whole d_model, then c grad tiles in four
+    // quarters), so the pass costs about n_dg (nk + 4c) / (CTAs resident).
+    // Clusters must sit in one GPC: a 152-SM GB300 holds this many clusters of
+    // c CTAs at once (one CTA per SM; measured with the occupancy query).  A
+    // fixed table, so the geometry -- and with it every rounding order -- is a
+    // function of the shape alone.
+    static const int resident[BWD_MAX_CL + 1] = {0, 152, 76, 46, 36, 28, 23, 15, 15,
+                                                 15, 13, 8, 8, 7, 7, 7, 7};
     const int64_t ns = cdiv(d, TC_SLICE);               // 256-column slices
-    BwdGeom g;
-    g.n_dg = static_cast<int>(cdiv(ns, 8));
-    g.n_cl = static_cast<int>(cdiv(ns, g.n_dg));
+    const int64_t nk = cdiv(d, TC_BK);
+    BwdGeom g{0, 0};
+    double best = 0.0;
+    for (int64_t dg = cdiv(ns, BWD_MAX_CL); dg <= ns; ++dg) {
+        const int64_t c = cdiv(ns, dg);
+        if (cdiv(ns, c) != dg) continue;                // the same clusters with idle d-groups
+        const double cost = static_cast<double>(dg * (nk + 4 * c)) / static_cast<double>(c * resident[c]);
+        if (g.n_cl == 0 || cost < best) {
+            best = cost;
+            g.n_cl = static_cast<int>(c);
+            g.n_dg = static_cast<int>(dg);
+        }
+    }
     (void)distill;
     return g;
 }
@@ -543,8 +562,7 @@ int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
     const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
     int64_t s;
     if (tc) {
-        const int64_t ns = cdiv(d, sl);
-        const int64_t clusters = cdiv(n, bm) * cdiv(ns, 8);     // token tiles x d-groups
+        const int64_t clusters = cdiv(n, bm) * bwd_geometry(d, false).n_dg;   // token tiles x d-groups
         s = clusters >= 144 ? 1 : 144 / clusters;
     } else {
         const int64_t base = cdiv(n, bm) * cdiv(d, sl);
@@ -583,7 +601,7 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     // forward (run_fused); it keeps the separate passes' space for its fallback.
     const bool fused = kind == LOSSK_KIND_CE_FWD_BWD && dtype == LOSSK_BF16;
     L->off_zpart = off;
-    if (fused) off = align256(off + sizeof(float) * L->nsplit * 8 * L->n_pad);
+    if (fused) off = align256(off + sizeof(float) * L->nsplit * BWD_MAX_CL * L->n_pad);
     L->off_dhc = off;
     if (fused) off = align256(off + sizeof(float2) * L->n_pad);
     L->off_gring = off;

@@ -48,7 +48,7 @@ struct WsLayout {
     size_t off_tokacc = 0;   // double [3][n_pad] per-token reduction terms
     size_t off_part = 0;     // float  [nstat][n_ct][n_pad]
     size_t off_dhpart = 0;   // float  [nsplit][n_tok][d_model] (nsplit > 1)
-    size_t off_zpart = 0;    // float  [nsplit * 8][n_pad] fused pass: sums of G' per (split, CTA)
+    size_t off_zpart = 0;    // float  [nsplit * BWD_MAX_CL][n_pad] fused pass: sums of G' per (split, CTA)
     size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
     size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the cluster passes
     size_t off_tstat = 0;    // double2 [n_pad] distillation: teacher (lse_t2, Eb) per token
@@ -106,6 +106,7 @@ constexpr float FUSED_SHIFT = 64.f;
 // BWD_BN loop columns.  Grad-tile ring: G_SLOTS slots of one supertile
 // (2 x 128 x 128 bf16) per CTA, for at most G_MAX_CTAS CTAs.
 constexpr int BWD_BN = 256;
+constexpr int BWD_MAX_CL = 16;     // CTAs per cluster at most (above 8: a non-portable size)
 constexpr int G_SLOTS = 2;
 constexpr int G_MAX_CTAS = 160;
 constexpr int64_t G_RING_ROWS = int64_t(G_MAX_CTAS) * G_SLOTS * 2 * 128;   // rows of 128 bf16
@@ -136,8 +137,9 @@ struct BwdArgs {
     int *err;
 };
 
-// Cluster geometry of the backward for a d_model: slices of 256 columns, at
-// most 8 CTAs per cluster, d-groups beyond that.
+// Cluster geometry of the backward for a d_model: slices of 256 columns, one
+// per CTA of a cluster of at most BWD_MAX_CL CTAs, d-groups beyond that (each
+// d-group recomputes the logits); chosen from the shape alone.
 struct BwdGeom {
     int n_cl, n_dg;
 };

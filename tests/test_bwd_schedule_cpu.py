@@ -202,6 +202,12 @@ def test_protocol_finishes_without_phase_overrun(c, nys):
         _run(c, nys, nk=3, seed=seed)
 
 
+@pytest.mark.parametrize("nys", [[20, 17, 3], [16], [40]])
+def test_protocol_clusters_of_16(nys):
+    for seed in range(2):
+        _run(16, nys, nk=2, seed=seed)
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_protocol_long_units(seed):
     # the Qwen3 head shape's d_hidden split (66-67 supertiles per unit) and a

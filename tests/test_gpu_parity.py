@@ -101,7 +101,9 @@ SMALL = [  # (n, d, V): several tiles and ragged tails in every dimension
     (128, 256, 512),
     (300, 768, 1000),     # cluster of 3, fewer token tiles than CTAs in the d_weight pass
     (200, 1280, 1500),    # cluster of 5 (one grad slot)
-    (130, 2304, 600),     # 9 slices: two d-groups of 5
+    (130, 2304, 600),     # 9 slices: a cluster of 9 (beyond the portable cluster size)
+    (200, 4096, 1000),    # 16 slices: a cluster of 16
+    (130, 4352, 600),     # 17 slices: two d-groups of 9
 ]
 
 
