@@ -61,6 +61,8 @@
 #include "lossk_internal.h"
 #include "ptx.cuh"
 
+#include <atomic>
+
 namespace lossk {
 
 namespace {
@@ -657,12 +659,24 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
 {
     auto k = bwd_kernel<MODE, DISTILL, F16>;
     constexpr int SMEM = bwd_smem<MODE, DISTILL>();
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    // The function attributes and the resident-cluster count are set up once
+    // per device and cluster size: the launch of the training step's first
+    // pass waits on the host after the validation read-back, so host work here
+    // is GPU idle time.
+    constexpr int MAX_DEV = 64;
+    static std::atomic<int> attr_done[MAX_DEV];
+    static std::atomic<int> resident[MAX_DEV][BWD_MAX_CL + 1];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (a.n_cl > 8) {
+    const bool cache = dev >= 0 && dev < MAX_DEV;
+    if (!cache || !attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
         // clusters of 9-16 CTAs are beyond the portable size
         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
+        if (cache) attr_done[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(192, 1, 1);
@@ -679,10 +693,14 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
     // for), each walking several units; the results do not depend on the
     // count, only the schedule does.
     cfg.gridDim = dim3(n_units * a.n_cl, 1, 1);
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess || active < 1) {
-        (void)cudaGetLastError();
-        active = n_units;
+    int active = cache ? resident[dev][a.n_cl].load(std::memory_order_relaxed) : 0;
+    if (active < 1) {
+        if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess || active < 1) {
+            (void)cudaGetLastError();
+            active = 0;
+        }
+        if (cache && active > 0) resident[dev][a.n_cl].store(active, std::memory_order_relaxed);
+        if (active < 1) active = n_units;
     }
     int clusters = active < n_units ? active : n_units;
     if (clusters * a.n_cl > G_MAX_CTAS) clusters = G_MAX_CTAS / a.n_cl;

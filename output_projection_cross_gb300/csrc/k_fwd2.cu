@@ -25,6 +25,8 @@
 #include "lossk_internal.h"
 #include "ptx.cuh"
 
+#include <atomic>
+
 namespace lossk {
 
 namespace {
@@ -259,8 +261,16 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
 template <bool DISTILL, bool F16> static cudaError_t launch_fwd2_one(const TcArgs &a, int grid, cudaStream_t st)
 {
     auto k = fwd2_kernel<DISTILL, F16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F2_SMEM);
+    // the shared-memory attribute is set once per device
+    static std::atomic<int> attr_done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F2_SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(1, std::memory_order_release);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(192, 1, 1);

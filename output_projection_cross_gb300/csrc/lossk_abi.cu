@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <vector>
 
@@ -184,25 +185,40 @@ int *readback_buffer()
 }
 
 // The header's first four words (err, bad_targets, n_valid, redo) after all
-// work queued on `st`; synchronises `st`.
-bool read_header(const WsHeader *hdr, cudaStream_t st, int out[4])
-{
-    int *h = readback_buffer();
-    int *dptr = nullptr;
-    if (h && cudaHostGetDevicePointer(reinterpret_cast<void **>(&dptr), h, 0) == cudaSuccess) {
-        {
+// work queued on `st`.  begin() enqueues the read-back; end() synchronises `st`
+// and returns the words (host work placed between the two overlaps the GPU).
+struct HeaderRead {
+    int *h = nullptr;
+    int words[4] = {0, 0, 0, 0};
+    bool begin(const WsHeader *hdr, cudaStream_t st)
+    {
+        h = readback_buffer();
+        int *dptr = nullptr;
+        if (h && cudaHostGetDevicePointer(reinterpret_cast<void **>(&dptr), h, 0) == cudaSuccess) {
             Launch k(KK_READBACK, st);
-            if (launch_publish_header(hdr, dptr, st) != cudaSuccess) return false;
+            return launch_publish_header(hdr, dptr, st) == cudaSuccess;
         }
+        (void)cudaGetLastError();
+        h = nullptr;
+        // no mapped host memory: a plain copy
+        return cudaMemcpyAsync(words, hdr, sizeof(words), cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    }
+    bool end(cudaStream_t st, int out[4])
+    {
         if (cudaStreamSynchronize(st) != cudaSuccess) return false;
-        const volatile int *v = h;
-        for (int i = 0; i < 4; ++i) out[i] = v[i];
+        if (h) {
+            const volatile int *v = h;
+            for (int i = 0; i < 4; ++i) words[i] = v[i];
+        }
+        for (int i = 0; i < 4; ++i) out[i] = words[i];
         return true;
     }
-    (void)cudaGetLastError();
-    // no mapped host memory: a plain copy
-    return cudaMemcpyAsync(out, hdr, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) == cudaSuccess &&
-           cudaStreamSynchronize(st) == cudaSuccess;
+};
+
+bool read_header(const WsHeader *hdr, cudaStream_t st, int out[4])
+{
+    HeaderRead r;
+    return r.begin(hdr, st) && r.end(st, out);
 }
 
 int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DEVICE_ERROR; }
@@ -217,8 +233,11 @@ struct FusedPre {
     float4 *tokp;
 };
 
+// `prep` (optional) runs on the host while the GPU validates: host-side set-up
+// of the passes that follow, which must not depend on the validation result.
 int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V, WsHeader *hdr,
-                 cudaStream_t st, Hdr *h, const FusedPre *fused = nullptr)
+                 cudaStream_t st, Hdr *h, const FusedPre *fused = nullptr,
+                 const std::function<bool()> &prep = nullptr)
 {
     {
         Launch k(KK_VALIDATE, st);
@@ -229,7 +248,11 @@ int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t
         if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     }
     int buf[4] = {0, 0, 0, 0};
-    if (!read_header(hdr, st, buf)) return LOSSK_DEVICE_ERROR;
+    HeaderRead r;
+    if (!r.begin(hdr, st)) return LOSSK_DEVICE_ERROR;
+    const bool prepared = !prep || prep();
+    if (!r.end(st, buf)) return LOSSK_DEVICE_ERROR;
+    if (!prepared) return LOSSK_DEVICE_ERROR;
     h->err = buf[0];
     h->bad = buf[1];
     h->n_valid = buf[2];
@@ -347,7 +370,7 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
 int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, const void *H,
                 const void *W, const void *teacher, bool distill, int direction, double temperature,
                 float *d_hidden, float *d_weight, cudaStream_t st, bool accumulate = false,
-                double out_scale = 1.0)
+                double out_scale = 1.0, const BwdArgs *pre_cols = nullptr)
 {
     const WsLayout &L = w.L;
     cudaError_t e = cudaSuccess;
@@ -358,7 +381,8 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             if (!dst) continue;
             const bool rows = pass == 0;
             BwdArgs a;
-            if (!bwd_args(w, rows, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
+            if (!rows && pre_cols) a = *pre_cols;
+            else if (!bwd_args(w, rows, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
             a.teacher = distill ? static_cast<const uint16_t *>(teacher) : nullptr;
             if (distill && !rows && !make_map_plain(&a.map_teach, teacher, V, n, 32, 32))
                 return LOSSK_DEVICE_ERROR;
@@ -450,7 +474,7 @@ SideStream *side_stream()
 int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
                   const int64_t *targets, const uint8_t *mask, double wz, double alpha,
                   float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st,
-                  cudaStream_t aux, cudaEvent_t fork, bool sum)
+                  cudaStream_t aux, cudaEvent_t fork, bool sum, const BwdArgs *pre = nullptr)
 {
     // the target logits and reference shifts came with the validation launch
     const WsLayout &L = w.L;
@@ -458,7 +482,8 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     cudaError_t e;
     const BwdGeom g = bwd_geometry(d, false);
     BwdArgs a;
-    if (!bwd_args(w, true, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
+    if (pre) a = *pre;
+    else if (!bwd_args(w, true, n, d, V, H, W, &a)) return LOSSK_DEVICE_ERROR;
     a.n_split = static_cast<int>(L.nsplit);
     a.inv_t_l2e = static_cast<float>(LOG2E);
     float *part = L.nsplit > 1 ? w.dhpart() : d_hidden;
@@ -728,7 +753,13 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     Hdr h;
     const bool fused_path = do_fwd && do_bwd && dH && dtype == LOSSK_BF16;
     const FusedPre pre{H, W, d, w.L.n_pad, w.tgt(), w.tokp()};
-    s = validate(targets, mask, n, V, w.hdr(), st, &h, fused_path ? &pre : nullptr);
+    // the training step's tensor maps are encoded while the GPU validates
+    BwdArgs fa, ca;
+    const auto prep = [&]() {
+        return bwd_args(w, true, n, d, V, H, W, &fa) && (!dW || bwd_args(w, false, n, d, V, H, W, &ca));
+    };
+    s = validate(targets, mask, n, V, w.hdr(), st, &h, fused_path ? &pre : nullptr,
+                 fused_path ? std::function<bool()>(prep) : std::function<bool()>());
     if (s != LOSSK_OK) return s;
     // gradient of grad_scale * total: a_t = grad_scale m_t / N_valid (mean) or grad_scale m_t (sum)
     const double alpha = sum ? gs : (h.n_valid > 0 ? gs / h.n_valid : 0.0);
@@ -745,9 +776,9 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
             if (sd->ready()) aux = sd->s;
         }
         s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dh_fused, st, aux,
-                      aux != st ? sd->fork : nullptr, sum);
+                      aux != st ? sd->fork : nullptr, sum, &fa);
         if (s == LOSSK_OK && dW && !acc)
-            s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st);
+            s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st, false, 1.0, &ca);
         if (aux != st &&
             (cudaEventRecord(sd->join, aux) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
             return LOSSK_DEVICE_ERROR;
