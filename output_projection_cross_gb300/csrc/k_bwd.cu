@@ -330,8 +330,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     for (int sidx = 0; sidx < 4; ++sidx) {
                         if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
                         tc_fence_after();
-                        // all four quarters of the writer's tile have landed: its slot may be refilled
-                        if (sidx == 3) mbar_arrive_remote(mapa_shared(smem_u32(&gfree[g]), wr));
+                        // all four quarters of the writer's tile have landed: its slot may be
+                        // refilled (a release of completed reads: CTA scope is enough, and the
+                        // issuer must not stall)
+                        if (sidx == 3) mbar_arrive_remote_cta(mapa_shared(smem_u32(&gfree[g]), wr));
                         const uint32_t sa = smem_u32(ring + st * B_STAGE);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -546,10 +548,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             fence_proxy_async_global();
             __threadfence();
             __syncwarp();
-            if (lane == 0) {
-                const uint32_t rb = smem_u32(&gready[crank * G_SLOTS + g]);
-                for (int q = 0; q < c; ++q) mbar_arrive_remote(mapa_shared(rb, q));
-            }
+            // one lane per CTA of the cluster: the cluster-scope releases run side by side
+            if (lane < c) mbar_arrive_remote(mapa_shared(smem_u32(&gready[crank * G_SLOTS + g]), lane));
             ++m_all;
             return true;
         };

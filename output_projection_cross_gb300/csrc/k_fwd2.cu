@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
             __syncwarp();
             if (lane == 0) {
                 if (lead) mbar_arrive(&tempty[b]);
-                else mbar_arrive_remote(tempty_lead + b * 8);
+                else mbar_arrive_remote_cta(tempty_lead + b * 8);   // a buffer release: no data to publish
             }
         }
         tc_fence_before();

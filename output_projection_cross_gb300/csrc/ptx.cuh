@@ -383,6 +383,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
                  : "memory");
 }
 
+// The same arrive with release at CTA scope only: for a signal that publishes
+// no data of this thread (a buffer's reads are complete).  The cluster-scope
+// release above holds the issuing thread for about a thousand clocks, which
+// on the MMA issuer is a thousand clocks of idle tensor core.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // 256-bit global store of eight 32-bit words (the address is 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *w)
 {
