@@ -83,6 +83,7 @@ template <int MODE, bool DISTILL> constexpr int bwd_smem()
 }
 static_assert(bwd_smem<BWD_COLS, true>() <= 232448, "fits the 227 KB per-CTA shared memory limit");
 static_assert(BWD_BN == 256 && TC_SLICE == 256, "one 256-column logit buffer + one 256-column accumulator");
+static_assert(TC_BK == 64, "a ring stage holds four K steps of 16");
 
 
 __device__ __forceinline__ void bw_wait_drain(uint64_t *bar, uint32_t parity)
@@ -291,6 +292,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         bool ok = true, first_acc = true;
         int m_all = 0;                         // own logit tiles issued so far
         int cnt[B_MAXC] = {};
+        // Shared-memory descriptors of ring stage 0; stage s adds s * B_STAGE / 16 to the start
+        // address field, a K step 32 B / 16 (K-major) or 2 KB / 16 (MN-major).  Every MMA then
+        // costs one add per operand: work between MMAs holds the tensor pipe up.
+        const uint32_t ring0 = smem_u32(ring);
+        const uint64_t dA = sdesc_sw128(ring0, 16, 1024);                 // A: K-major, 128 rows
+        const uint64_t dBs = sdesc_sw128(ring0 + B_APART, 16, 1024);      // logit B: K-major, 256 rows
+        const uint64_t dBa = sdesc_sw128(ring0 + B_APART, 8192, 1024);    // accumulate B: MN-major
+        constexpr uint64_t STEP = B_STAGE >> 4;
         BwdCursor cur, prev;
         cursor_set(cur, cluster, 0);
         bool have_prev = false;
@@ -303,11 +312,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     for (int kb = 0; kb < nk; ++kb) {
                         if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t sa = smem_u32(ring + st * B_STAGE);
-#pragma unroll
-                        for (int k = 0; k < TC_BK / 16; ++k)
-                            tc_mma_bf16(tmem, sdesc_sw128(sa + k * 32, 16, 1024),
-                                        sdesc_sw128(sa + B_APART + k * 32, 16, 1024), ID_S, (kb | k) != 0);
+                        const uint64_t off = st * STEP;
+                        const uint64_t a = dA + off, b = dBs + off;
+                        tc_mma_bf16(tmem, a, b, ID_S, kb != 0);
+                        tc_mma_bf16(tmem, a + 2, b + 2, ID_S, 1u);
+                        tc_mma_bf16(tmem, a + 4, b + 4, ID_S, 1u);
+                        tc_mma_bf16(tmem, a + 6, b + 6, ID_S, 1u);
                         tc_commit(&empty[st]);
                         if (++st == B_NST) { st = 0; ph ^= 1; }
                     }
@@ -334,14 +344,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                         // refilled (a release of completed reads: CTA scope is enough, and the
                         // issuer must not stall)
                         if (sidx == 3) mbar_arrive_remote_cta(mapa_shared(smem_u32(&gfree[g]), wr));
-                        const uint32_t sa = smem_u32(ring + st * B_STAGE);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            tc_mma_bf16(tmem + ACC_COL, sdesc_sw128(sa + k * 32, 16, 1024),
-                                        sdesc_sw128(sa + B_APART + k * 2048, 8192, 1024), ID_ACC,
-                                        first_acc ? 0u : 1u);
-                            first_acc = false;
-                        }
+                        const uint64_t off = st * STEP;
+                        const uint64_t a = dA + off, b = dBa + off;
+                        tc_mma_bf16(tmem + ACC_COL, a, b, ID_ACC, first_acc ? 0u : 1u);
+                        tc_mma_bf16(tmem + ACC_COL, a + 2, b + 128, ID_ACC, 1u);
+                        tc_mma_bf16(tmem + ACC_COL, a + 4, b + 256, ID_ACC, 1u);
+                        tc_mma_bf16(tmem + ACC_COL, a + 6, b + 384, ID_ACC, 1u);
+                        first_acc = false;
                         tc_commit(&empty[st]);
                         if (++st == B_NST) { st = 0; ph ^= 1; }
                     }

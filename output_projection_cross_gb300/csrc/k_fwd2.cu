@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
     } else if (warp == 1 && lane == 0 && lead) {
         // ================= MMA issuer (even CTA) =================
         constexpr uint32_t ID = idesc_16_f32(256, F2_BN, 0, 0, F16);
+        static_assert(TC_BK == 64, "a ring stage holds four K steps of 16");
+        const uint64_t dA = sdesc_sw128(smem_u32(ring), 16, 1024);
+        const uint64_t dB = sdesc_sw128(smem_u32(ring) + F2_A_BYTES, 16, 1024);
         int st = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -137,11 +140,14 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
             for (int kb = 0; kb < nk; ++kb) {
                 if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(ring + st * F2_STAGE);
-#pragma unroll
-                for (int k = 0; k < TC_BK / 16; ++k)
-                    tc_mma_bf16_pair(d, sdesc_sw128(sa + k * 32, 16, 1024),
-                                     sdesc_sw128(sa + F2_A_BYTES + k * 32, 16, 1024), ID, (kb | k) != 0);
+                // descriptors of stage 0 plus the stage and K-step offsets (16-byte units):
+                // one add per operand between MMAs
+                const uint64_t off = st * (F2_STAGE >> 4);
+                const uint64_t da = dA + off, db = dB + off;
+                tc_mma_bf16_pair(d, da, db, ID, kb != 0);
+                tc_mma_bf16_pair(d, da + 2, db + 2, ID, 1u);
+                tc_mma_bf16_pair(d, da + 4, db + 4, ID, 1u);
+                tc_mma_bf16_pair(d, da + 6, db + 6, ID, 1u);
                 tc_commit_pair_multicast(&empty[st], 3);
                 if (++st == F2_STAGES) { st = 0; ph ^= 1; }
             }
