@@ -43,9 +43,13 @@
  *    validation kernel, to read back the target-range flag and the number of
  *    counted tokens: the call refuses bad targets (586) before the main
  *    kernels run, the way the pages' functions validate first.  After that
- *    point the call returns without waiting for the GPU -- except the
- *    training-step calls on the bf16 path (lossk_ce_fwd_bwd and its _ex
- *    form), which read back one more flag at their end (see there).  The
+ *    point the call returns without waiting for the GPU.  The training-step
+ *    calls on the bf16 path (lossk_ce_fwd_bwd and its _ex form) synchronise
+ *    once too, at their end instead: the validation is queued first, every
+ *    kernel after it returns at once on the device when it found a target out
+ *    of range (so a 586 still leaves every output untouched), and the end
+ *    read-back carries the validation result with the range flag of the
+ *    single-pass forward (see there).  The
  *    read-backs go through a one-warp kernel writing into mapped pinned host
  *    memory, not through a copy engine, so large copies other streams have in
  *    flight do not delay them; the library allocates that memory (64 bytes
@@ -223,9 +227,10 @@ int32_t lossk_ce_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int32_t dtyp
  * log-sum-exp, which saves one full logit pass.  A row whose maximum logit
  * lies more than about 110 nats above its target logit would leave the range
  * the shift covers; the call detects that (and any non-finite d_hidden) on
- * the device, reads the flag back at its end (a second synchronisation of
- * `stream`) and then recomputes every output on the separate passes.  The
- * outputs are the same quantities either way, within the tolerances. */
+ * the device, reads the flag back at its end (with the validation result, in
+ * the call's one synchronisation of `stream`) and then recomputes every
+ * output on the separate passes.  The outputs are the same quantities either
+ * way, within the tolerances. */
 int32_t lossk_ce_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
                          int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight,
                          int64_t weight_len, const int64_t *targets, int64_t targets_len,
@@ -271,8 +276,8 @@ int32_t lossk_distill_fwd_bwd(int64_t n_tok, int64_t d_model, int64_t vocab, int
 
 /* lossk_ce_fwd_bwd with flags (lossk_flags).  With LOSSK_ACCUMULATE_GRADS
  * the call adds into d_hidden and d_weight, and touches them only after the
- * fused pass's range check has passed (so it synchronises `stream` once more
- * in the middle).  Unknown flag bits give 592 (checked after 585). */
+ * end read-back has come back clean (the d_weight pass and the addition of
+ * d_hidden then follow it).  Unknown flag bits give 592 (checked after 585). */
 int32_t lossk_ce_fwd_bwd_ex(int64_t n_tok, int64_t d_model, int64_t vocab, int64_t chunk,
                             int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight,
                             int64_t weight_len, const int64_t *targets, int64_t targets_len,

@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     constexpr bool FUSED = MODE == BWD_FUSED;
     constexpr bool ROWS = MODE != BWD_COLS;     // token rows x vocabulary columns
     static_assert(!(FUSED && DISTILL), "the fused pass is label cross-entropy only");
+    // Queued behind a validation that found a target out of range: every CTA
+    // leaves before it touches anything (a refused call writes no output).
+    if (a.refused && *reinterpret_cast<const volatile int *>(a.refused)) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -382,6 +382,9 @@ __global__ void __launch_bounds__(1024) reduce_kernel(const double *__restrict__
                                                       double *__restrict__ out, int sum)
 {
     __shared__ double sh[3][1024];
+    // a refused call (a target out of range, found by the validation queued
+    // before) leaves its outputs untouched
+    if (*reinterpret_cast<const volatile int *>(&hdr->bad_targets)) return;
     const int i = threadIdx.x;
     for (int s = 0; s < 3; ++s) {
         double acc = 0.0;
@@ -594,13 +597,19 @@ cudaError_t launch_tgt_logit(bool f16, const uint16_t *H, const uint16_t *W, con
 // shifted terms are only trusted while the largest stays far from the fp32
 // and bf16 limits.  The flag is raised for masked rows too, since their lse is
 // an output.
-__global__ void merge_fused_kernel(const float *__restrict__ zpart, int64_t nz, const float *__restrict__ tgt,
-                                   const int64_t *__restrict__ targets, const uint8_t *__restrict__ mask,
-                                   int64_t n, int64_t n_pad, double alpha, double wz,
-                                   float *__restrict__ lse_out, float *__restrict__ ce_out,
-                                   double *__restrict__ tokacc, float4 *__restrict__ tokp,
-                                   float2 *__restrict__ dhc, WsHeader *hdr)
+// The counted-token total comes from the validation's header (the call does
+// not wait for it on the host): alpha = grad_scale / N_valid, or grad_scale
+// for the sum.  A refused call returns at once.
+__global__ void __launch_bounds__(64) merge_fused_kernel(const float *__restrict__ zpart, int64_t nz,
+                                                         const float *__restrict__ tgt,
+                                                         const int64_t *__restrict__ targets,
+                                                         const uint8_t *__restrict__ mask, int64_t n,
+                                                         int64_t n_pad, double gs, int sum, double wz,
+                                                         float *__restrict__ lse_out, float *__restrict__ ce_out,
+                                                         double *__restrict__ tokacc, float4 *__restrict__ tokp,
+                                                         float2 *__restrict__ dhc, WsHeader *hdr)
 {
+    if (*reinterpret_cast<const volatile int *>(&hdr->bad_targets)) return;
     const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (t >= n_pad) return;
     if (t >= n) {
@@ -608,8 +617,19 @@ __global__ void merge_fused_kernel(const float *__restrict__ zpart, int64_t nz, 
         dhc[t] = make_float2(0.f, 0.f);
         return;
     }
+    const int nv = hdr->n_valid;
+    const double alpha = sum ? gs : (nv > 0 ? gs / nv : 0.0);
+    // the partials in index order; loaded eight at a time so the loads overlap
     double Z = 0.0;
-    for (int64_t j = 0; j < nz; ++j) Z += static_cast<double>(zpart[j * n_pad + t]);
+    int64_t j = 0;
+    for (; j + 8 <= nz; j += 8) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = zpart[(j + q) * n_pad + t];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) Z += static_cast<double>(v[q]);
+    }
+    for (; j < nz; ++j) Z += static_cast<double>(zpart[j * n_pad + t]);
     if (!(Z >= 0x1p-80 && Z <= 0x1p90)) hdr->redo = 1;
     const double r = static_cast<double>(tokp[t].x);
     const float lse_f = static_cast<float>((r + log2(Z)) * LN2);
@@ -630,12 +650,12 @@ __global__ void merge_fused_kernel(const float *__restrict__ zpart, int64_t nz, 
 }
 
 cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,
-                               const uint8_t *mask, int64_t n, int64_t n_pad, double alpha, double wz,
+                               const uint8_t *mask, int64_t n, int64_t n_pad, double gs, bool sum, double wz,
                                float *lse_out, float *ce_out, double *tokacc, float4 *tokp,
                                float2 *dhc, WsHeader *hdr, cudaStream_t st)
 {
-    merge_fused_kernel<<<static_cast<unsigned>((n_pad + 127) / 128), 128, 0, st>>>(
-        zpart, nz, tgt, targets, mask, n, n_pad, alpha, wz, lse_out, ce_out, tokacc, tokp, dhc, hdr);
+    merge_fused_kernel<<<static_cast<unsigned>((n_pad + 63) / 64), 64, 0, st>>>(
+        zpart, nz, tgt, targets, mask, n, n_pad, gs, sum ? 1 : 0, wz, lse_out, ce_out, tokacc, tokp, dhc, hdr);
     return cudaGetLastError();
 }
 
@@ -648,6 +668,7 @@ __global__ void combine_dh_kernel(const float4 *part, int64_t nsplit, int64_t n,
                                   const uint16_t *__restrict__ W, const int64_t *__restrict__ targets,
                                   const float2 *__restrict__ dhc, float4 *out, WsHeader *hdr)
 {
+    if (*reinterpret_cast<const volatile int *>(&hdr->bad_targets)) return;   // a refused call
     const int64_t count4 = n * d4;
     bool bad = false;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;

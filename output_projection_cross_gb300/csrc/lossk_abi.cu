@@ -8,7 +8,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
-#include <functional>
 #include <mutex>
 #include <vector>
 
@@ -223,36 +222,17 @@ bool read_header(const WsHeader *hdr, cudaStream_t st, int out[4])
 
 int32_t status_of(cudaError_t e) { return e == cudaSuccess ? LOSSK_OK : LOSSK_DEVICE_ERROR; }
 
-// Run the validation kernel and read its result back (the one sync of a call).
-// `fused` (the bf16 training step): the same validation in one launch with the
-// target logits and reference shifts the fused pass needs (written to tgt/tokp).
-struct FusedPre {
-    const void *H, *W;
-    int64_t d, n_pad;
-    float *tgt;
-    float4 *tokp;
-};
-
-// `prep` (optional) runs on the host while the GPU validates: host-side set-up
-// of the passes that follow, which must not depend on the validation result.
+// Run the validation kernel and read its result back (the one sync of a call;
+// the bf16 training step validates without waiting, see ce_common).
 int32_t validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V, WsHeader *hdr,
-                 cudaStream_t st, Hdr *h, const FusedPre *fused = nullptr,
-                 const std::function<bool()> &prep = nullptr)
+                 cudaStream_t st, Hdr *h)
 {
     {
         Launch k(KK_VALIDATE, st);
-        cudaError_t e = fused ? launch_validate_tgt(static_cast<const uint16_t *>(fused->H),
-                                                    static_cast<const uint16_t *>(fused->W), targets, mask, n,
-                                                    fused->d, V, fused->n_pad, hdr, fused->tgt, fused->tokp, st)
-                              : launch_validate(targets, mask, n, V, hdr, st);
-        if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+        if (launch_validate(targets, mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
     }
     int buf[4] = {0, 0, 0, 0};
-    HeaderRead r;
-    if (!r.begin(hdr, st)) return LOSSK_DEVICE_ERROR;
-    const bool prepared = !prep || prep();
-    if (!r.end(st, buf)) return LOSSK_DEVICE_ERROR;
-    if (!prepared) return LOSSK_DEVICE_ERROR;
+    if (!read_header(hdr, st, buf)) return LOSSK_DEVICE_ERROR;
     h->err = buf[0];
     h->bad = buf[1];
     h->n_valid = buf[2];
@@ -307,6 +287,7 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
     a->tokp = w.tokp();
     a->out_split_stride = n * d;
     a->err = &w.hdr()->err;
+    a->refused = &w.hdr()->bad_targets;
     return true;
 }
 
@@ -472,7 +453,7 @@ SideStream *side_stream()
 }
 
 int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
-                  const int64_t *targets, const uint8_t *mask, double wz, double alpha,
+                  const int64_t *targets, const uint8_t *mask, double wz, double gs,
                   float *lse_out, float *ce_out, double *scalars, float *d_hidden, cudaStream_t st,
                   cudaStream_t aux, cudaEvent_t fork, bool sum, const BwdArgs *pre = nullptr)
 {
@@ -499,7 +480,7 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
         Launch k(KK_MERGE_FUSED, st);
-        e = launch_merge_fused(w.zpart(), L.nsplit * g.n_cl, w.tgt(), targets, mask, n, L.n_pad, alpha,
+        e = launch_merge_fused(w.zpart(), L.nsplit * g.n_cl, w.tgt(), targets, mask, n, L.n_pad, gs, sum,
                                wz, lse_out, ce_out, w.tokacc(), w.tokp(), w.dhc(), w.hdr(), st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
@@ -750,23 +731,26 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
     const bool acc = (flags & LOSSK_ACCUMULATE_GRADS) != 0, sum = (flags & LOSSK_REDUCE_SUM) != 0;
     w.base = static_cast<uint8_t *>(workspace);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    Hdr h;
     const bool fused_path = do_fwd && do_bwd && dH && dtype == LOSSK_BF16;
-    const FusedPre pre{H, W, d, w.L.n_pad, w.tgt(), w.tokp()};
-    // the training step's tensor maps are encoded while the GPU validates
-    BwdArgs fa, ca;
-    const auto prep = [&]() {
-        return bwd_args(w, true, n, d, V, H, W, &fa) && (!dW || bwd_args(w, false, n, d, V, H, W, &ca));
-    };
-    s = validate(targets, mask, n, V, w.hdr(), st, &h, fused_path ? &pre : nullptr,
-                 fused_path ? std::function<bool()>(prep) : std::function<bool()>());
-    if (s != LOSSK_OK) return s;
     // gradient of grad_scale * total: a_t = grad_scale m_t / N_valid (mean) or grad_scale m_t (sum)
-    const double alpha = sum ? gs : (h.n_valid > 0 ? gs / h.n_valid : 0.0);
+    double alpha = 0.0;
     if (fused_path) {
-        // With accumulation, d_hidden is formed in the workspace and the
-        // caller's gradients are touched only once the fused pass's range
-        // check has come back clean.
+        // The training step reads the header back once, at its end.  The
+        // validation (with the target logits) is queued first; every kernel
+        // after it returns at once if it found a target out of range, so a
+        // refused call still touches no output, and N_valid reaches the
+        // merge on the device.  With accumulation, d_hidden is formed in the
+        // workspace and the caller's gradients are touched only once the
+        // read-back has come back clean.
+        {
+            Launch k(KK_VALIDATE, st);
+            if (launch_validate_tgt(static_cast<const uint16_t *>(H), static_cast<const uint16_t *>(W), targets,
+                                    mask, n, d, V, w.L.n_pad, w.hdr(), w.tgt(), w.tokp(), st) != cudaSuccess)
+                return LOSSK_DEVICE_ERROR;
+        }
+        BwdArgs fa, ca;
+        if (!bwd_args(w, true, n, d, V, H, W, &fa) || (dW && !bwd_args(w, false, n, d, V, H, W, &ca)))
+            return LOSSK_DEVICE_ERROR;
         float *dh_fused = acc ? w.dhacc() : dH;
         SideStream *sd = acc ? nullptr : side_stream();
         std::unique_lock<std::mutex> lk;
@@ -775,7 +759,7 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
             lk = std::unique_lock<std::mutex>(sd->mu);
             if (sd->ready()) aux = sd->s;
         }
-        s = run_fused(w, n, d, V, H, W, targets, mask, wz, alpha, lse_io, ce_out, scalars, dh_fused, st, aux,
+        s = run_fused(w, n, d, V, H, W, targets, mask, wz, gs, lse_io, ce_out, scalars, dh_fused, st, aux,
                       aux != st ? sd->fork : nullptr, sum, &fa);
         if (s == LOSSK_OK && dW && !acc)
             s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st, false, 1.0, &ca);
@@ -783,12 +767,14 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
             (cudaEventRecord(sd->join, aux) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
             return LOSSK_DEVICE_ERROR;
         if (s != LOSSK_OK) return s;
-        // The call's second read-back: a device timeout, or a row the shifted
-        // pass could not represent (then every output is recomputed by the
-        // separate passes below, which need no shift).
+        // The read-back: a device timeout, a target out of range (nothing was
+        // written), or a row the shifted pass could not represent (then every
+        // output is recomputed by the separate passes below, which need no shift).
         int flags_d[4] = {0, 0, 0, 0};
         if (!read_header(w.hdr(), st, flags_d)) return LOSSK_DEVICE_ERROR;
         if (flags_d[0]) return LOSSK_DEVICE_TIMEOUT;
+        if (flags_d[1]) return LOSSK_TARGET_OUT_OF_RANGE;
+        alpha = sum ? gs : (flags_d[2] > 0 ? gs / flags_d[2] : 0.0);
         if (!flags_d[3]) {
             if (!acc) return LOSSK_OK;
             {
@@ -798,6 +784,11 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
             if (dW) return run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, nullptr, dW, st, true);
             return LOSSK_OK;
         }
+    } else {
+        Hdr h;
+        s = validate(targets, mask, n, V, w.hdr(), st, &h);
+        if (s != LOSSK_OK) return s;
+        alpha = sum ? gs : (h.n_valid > 0 ? gs / h.n_valid : 0.0);
     }
     if (do_fwd) {
         s = run_ce_fwd(w, n, d, V, dtype, H, W, targets, mask, wz, lse_io, ce_out, scalars, st, sum);

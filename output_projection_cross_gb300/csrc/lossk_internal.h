@@ -134,6 +134,7 @@ struct BwdArgs {
     int64_t zpart_stride;
     int accumulate;        // add the accumulator into `out` instead of overwriting it
     float out_scale;       // fp16 operands: the factor the stored accumulator is multiplied by
+    const int *refused;    // nonzero: the validation before found a bad target; return at once
     int *err;
 };
 
@@ -216,8 +217,9 @@ cudaError_t launch_validate_tgt(const uint16_t *H, const uint16_t *W, const int6
                                 WsHeader *hdr, float *tgt, float4 *tokp, cudaStream_t st);
 cudaError_t launch_tgt_logit(bool f16, const uint16_t *H, const uint16_t *W, const int64_t *targets, int64_t n,
                              int64_t d, int64_t n_pad, float *tgt, float4 *tokp, cudaStream_t st);
+// gs, sum: the gradient scale and the reduction; alpha comes from the header's N_valid.
 cudaError_t launch_merge_fused(const float *zpart, int64_t nz, const float *tgt, const int64_t *targets,
-                               const uint8_t *mask, int64_t n, int64_t n_pad, double alpha, double wz,
+                               const uint8_t *mask, int64_t n, int64_t n_pad, double gs, bool sum, double wz,
                                float *lse_out, float *ce_out, double *tokacc, float4 *tokp,
                                float2 *dhc, WsHeader *hdr, cudaStream_t st);
 cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int64_t d,

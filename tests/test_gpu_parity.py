@@ -507,6 +507,39 @@ def test_refusals_leave_outputs_untouched(L):
     assert e.value.status == 591
 
 
+@pytest.mark.parametrize("shape", [(64, 64, 500), (300, 256, 4000)])
+def test_training_step_refusal_touches_no_output(L, shape):
+    """The bf16 training step validates without waiting: its later kernels
+    return at once on the device when a target is out of range.  Every output
+    (including d_hidden, which the fused pass writes directly when there is a
+    single vocabulary split, as at the first shape) must keep its contents, with
+    and without accumulation; a valid call on the same workspace then works."""
+    n, d, V = shape
+    H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(V, d, device="cuda") * 0.05).to(torch.bfloat16)
+    ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, d, V, L.lossk.BF16)
+    for flags in (0, L.lossk.ACCUMULATE_GRADS):
+        for bad in (-3, V):
+            y = torch.randint(0, V, (n,), device="cuda")
+            y[n // 2] = bad
+            outs = dict(lse_out=torch.full((n,), 7.0, device="cuda"), ce_out=torch.full((n,), 8.0, device="cuda"),
+                        scalars_out=torch.full((3,), 9.0, dtype=torch.float64, device="cuda"),
+                        d_hidden=torch.full((n, d), 1.5, device="cuda"), d_weight=torch.full((V, d), 2.5, device="cuda"))
+            with pytest.raises(L.LosskError) as e:
+                L.lossk_ce_fwd_bwd_ex(H, W, y, flags=flags, z_weight=1e-3, ws=ws, **outs)
+            assert e.value.status == 586
+            torch.cuda.synchronize()
+            assert torch.all(outs["lse_out"] == 7.0) and torch.all(outs["ce_out"] == 8.0)
+            assert torch.all(outs["scalars_out"] == 9.0)
+            assert torch.all(outs["d_hidden"] == 1.5) and torch.all(outs["d_weight"] == 2.5)
+    y = torch.randint(0, V, (n,), device="cuda")
+    o = L.lossk_ce_fwd_bwd(H, W, y, z_weight=1e-3, ws=ws)
+    r = L.lossk_ce_fwd_bwd(H, W, y, z_weight=1e-3)
+    torch.cuda.synchronize()
+    assert torch.equal(o["lse"], r["lse"]) and torch.equal(o["d_weight"], r["d_weight"])
+    assert torch.equal(o["d_hidden"], r["d_hidden"]) and torch.equal(o["scalars"], r["scalars"])
+
+
 def test_all_masked_gives_zeros(L):
     n, d, V = 70, 64, 300
     H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
