@@ -242,6 +242,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         cursor_set(cur, cluster, 0);
         bool have_prev = false;
         while (ok && (cur.u < n_units || have_prev)) {
+            if (!ROWS && cur.u < n_units && cur.r == 0 && cur.u + n_clusters < n_units) {
+                // d_weight: the cluster's next unit has a new fixed tile (128 weight rows
+                // over the whole d_model, read from HBM for the first time); bring it into
+                // L2 now, the CTAs splitting its K steps
+                const int fixn = bwd_unit(a, cur.u + n_clusters).fixed * 128;
+                for (int kb = crank; kb < nk; kb += c) tma_prefetch_2d(&a.map_fix, kb * TC_BK, fixn);
+            }
             if (cur.u < n_units) {
                 const int y = cur.r * c + crank;
                 if (y < cur.w.ny) {
