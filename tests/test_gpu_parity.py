@@ -148,12 +148,16 @@ def test_ce_persistent_clusters(L, shape):
 
 
 @pytest.mark.parametrize("direction", ["fkl", "rkl"])
-def test_distill_persistent_clusters(L, direction):
-    n, d, V = 600, 1024, 8192
+@pytest.mark.parametrize("dtype,shape", [("bf16", (600, 1024, 8192)), ("bf16", (300, 4096, 4096)),
+                                         ("f16", (600, 1024, 8192))])
+def test_distill_persistent_clusters(L, direction, dtype, shape):
+    """Several units per cluster; d_model 4096 runs one cluster of 16 CTAs."""
+    n, d, V = shape
     x = _inputs("distill_z_4096x2048", seed=32, n_tok=n, d_model=d, vocab=V)
+    x = _redraw(x, dtype, 3, n, d, V, teacher=True)
     mask = li.mask(6, n, 0.1)
-    out = L.lossk_distill_fwd_bwd(_dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"),
-                                  _dev(x["teacher"], "bf16"), direction, temperature=2.0,
+    out = L.lossk_distill_fwd_bwd(_dev(x["hidden"], dtype), _dev(x["weight"], dtype),
+                                  _dev(x["teacher"], dtype), direction, temperature=2.0,
                                   loss_mask=_dev(mask, ""), z_weight=1e-3)
     torch.cuda.synchronize()
     r = oracle.distill(x["hidden"], x["weight"], x["teacher"], direction, temperature=2.0,
