@@ -542,6 +542,50 @@ def extra_paths(L, dev, pk, n_tok=None):
             "kernel_ms": kms, "algorithmic_bytes": nbytes,
             "achieved_gbs": nbytes / (kms / 1e3) / 1e9,
             "frac_hbm": nbytes / (kms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    # the label loss's other entry points at the Qwen3 head shape: the forward
+    # alone (CTA-pair statistics), the backward alone (both separate passes), and
+    # the training step with fp16 inputs (the separate passes: the single-pass
+    # forward + d_hidden needs bf16's range)
+    del X, grad
+    torch.cuda.empty_cache()
+    wq = li.WORKLOADS["qwen3_0p6b_head"]
+    xq = li.make(wq, seed=0)
+    nq, dq, Vq = wq.n_tok, wq.d_model, wq.vocab
+    yq = torch.from_numpy(xq["targets"]).to(dev)
+    fl6 = 6.0 * nq * dq * Vq
+    for dt_name, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        Hq = torch.from_numpy(li.round_to(xq["hidden"], dt_name)).to(dev).to(tdt)
+        Wq = torch.from_numpy(li.round_to(xq["weight"], dt_name)).to(dev).to(tdt)
+        code = L.lossk.BF16 if dt_name == "bf16" else L.lossk.F16
+        dH = torch.empty(nq, dq, device=dev)
+        dW = torch.empty(Vq, dq, device=dev)
+        lse = torch.empty(nq, device=dev)
+        calls = {}
+        if dt_name == "bf16":
+            wsf = L.workspace(L.lossk.KIND_CE_FWD, nq, dq, Vq, code, dev)
+            wsb = L.workspace(L.lossk.KIND_CE_BWD, nq, dq, Vq, code, dev)
+            L.lossk_ce_fwd(Hq, Wq, yq, chunk=wq.chunk, lse_out=lse, ws=wsf)
+            calls["ce_fwd_only"] = (lambda: L.lossk_ce_fwd(Hq, Wq, yq, chunk=wq.chunk, lse_out=lse, ws=wsf), 2.0)
+            calls["ce_bwd_only"] = (lambda: L.lossk_ce_bwd(Hq, Wq, yq, lse, d_hidden=dH, d_weight=dW, ws=wsb), 4.0)
+        else:
+            wss = L.workspace(L.lossk.KIND_CE_FWD_BWD, nq, dq, Vq, code, dev)
+            calls["ce_fwd_bwd_f16"] = (lambda: L.lossk_ce_fwd_bwd(Hq, Wq, yq, chunk=wq.chunk, d_hidden=dH,
+                                                                  d_weight=dW, ws=wss), 6.0)
+        for name, (fn, units) in calls.items():
+            L.lossk_profile_read(reset=True)
+            L.lossk_profile_enable(True)
+            ms = _time(fn, 5)
+            L.lossk_profile_enable(False)
+            prof = L.lossk_profile_read(reset=True)
+            fl = units / 6.0 * fl6
+            res[name] = {"workload": f"{wq.name} ({dt_name})", "ms": ms, "tokens_per_s": nq / (ms / 1e3),
+                         "flops_counted": fl, "counted_as": f"{int(units)}*n*d*V",
+                         "tensor_frac": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+                         "kernels_ms": {k: v[0] / v[1] for k, v in prof.items()}}
+        del Hq, Wq, dH, dW
+        torch.cuda.empty_cache()
+    X = torch.randn(n, V, device=dev, generator=g).to(torch.bfloat16)
+    grad = torch.empty_like(X)
     # distillation from given student logits (HBM stream): read the student and
     # teacher logits once, write grad_logits once
     T = (torch.randn(n, V, device=dev, generator=g) * 3).to(torch.bfloat16)
