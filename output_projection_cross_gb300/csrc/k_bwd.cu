@@ -279,9 +279,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                             uint8_t *sp = acquire();
                             if (!sp) { ok = false; break; }
                             tma_load_2d(sp, &a.map_g, &full[st], h * 64, grow + sub * 128);
-                            for (int q = 0; q < 4; ++q)
-                                tma_load_2d(sp + B_APART + q * 8192, &a.map_ys, &full[st], slice0 + q * 64,
-                                            loop0 + sub * 128 + h * 64);
+                            if (a.ys3 && slice0 + TC_SLICE <= a.d)
+                                // the d-slice's four 64-column blocks in one box
+                                tma_load_3d(sp + B_APART, &a.map_ys3, &full[st], 0, loop0 + sub * 128 + h * 64,
+                                            slice0 / 64);
+                            else
+                                for (int q = 0; q < 4; ++q)
+                                    tma_load_2d(sp + B_APART + q * 8192, &a.map_ys, &full[st], slice0 + q * 64,
+                                                loop0 + sub * 128 + h * 64);
                             advance();
                         }
                     cnt_inc(cnt, wr);

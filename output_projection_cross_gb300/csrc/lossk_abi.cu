@@ -95,6 +95,25 @@ bool make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tensor seen as [inner/64 blocks][outer][64] -- dims {64, outer,
+// inner/64}, block stride 128 B -- so one box {64, box_outer, nblk} lands nblk
+// 64-column blocks one after another (the MN-major operand layout, 128-byte
+// swizzle).  Needs inner % 64 == 0.
+bool make_map_blocks(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, uint32_t box_outer,
+                     uint32_t nblk)
+{
+    if (inner % 64 != 0) return false;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, 128};
+    const cuuint32_t box[3] = {64, box_outer, nblk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- tracing: launch counter and optional per-kernel event timing ------------
 std::atomic<int64_t> g_launches{0};
 
@@ -274,6 +293,7 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
     if (!make_map(&a->map_fix, Fx, d, nf, 64, 128) || !make_map(&a->map_loop, Lp, d, nl, 64, BWD_BN) ||
         !make_map(&a->map_ys, Lp, d, nl, 64, 64) || !make_map(&a->map_g, w.gring(), 128, G_RING_ROWS, 64, 128))
         return false;
+    a->ys3 = make_map_blocks(&a->map_ys3, Lp, d, nl, 64, 4) ? 1 : 0;
     const BwdGeom g = bwd_geometry(d, false);
     a->gscr = w.gring();
     a->n_tok = static_cast<int>(n);

@@ -116,6 +116,8 @@ struct BwdArgs {
     CUtensorMap map_loop;  // the loop tensor as the logit MMA's B operand, box {64, 256}
     CUtensorMap map_ys;    // the loop tensor rows x d-slice (MN-major B of the accumulate), box {64, 64}
     CUtensorMap map_g;     // the grad-tile ring [G_RING_ROWS][128] bf16, box {64, 128}
+    CUtensorMap map_ys3;   // map_ys as [64-column blocks][rows][64] (d_model % 64 == 0): one box {64, 64, 4}
+    int ys3;               // map_ys3 is valid
     CUtensorMap map_teach; // distillation d_weight: teacher [n_tok][vocab] bf16, box {32, 32}
     uint16_t *gscr;        // the grad-tile ring itself
     const uint16_t *teacher; // teacher logits [n_tok][vocab] (bf16), read by the epilogue
