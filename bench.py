@@ -183,10 +183,35 @@ class Clocks:
 
 # ---- traffic from the committed ncu summary -----------------------------------
 
+def _code_only(text):
+    """C/C++ source without comments and whitespace: a comment edit leaves the
+    kernels, and so their recorded counters, unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch == '"' or ch == "'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    return "".join("".join(out).split())
+
+
 def kernel_src_sha():
     h = hashlib.sha256()
     for f in ("k_fwd2.cu", "k_bwd.cu", "k_simt.cu", "lossk_abi.cu", "ptx.cuh", "lossk_internal.h"):
-        h.update(open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), "rb").read())
+        with open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

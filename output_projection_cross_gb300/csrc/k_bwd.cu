@@ -24,19 +24,24 @@
 // computes its logits transposed, vocabulary rows x token columns) and B is
 // the loop tensor's rows x d-slice (MN-major).
 //
-// Why L2 and not distributed shared memory: these passes are bound by operand
-// bytes into each SM, which TMA from L2 and shared-to-shared copies share, and
-// shared-memory grad slots would take 4 x 32 KB per CTA.  Through L2 the grad
-// tiles cost the same inbound bytes, the shared memory holds only the operand
-// ring (so the logit tiles can be 256 columns wide: fewer operand bytes per
-// FLOP), and no slot is shared by two CTAs of a round (clusters of 8 do not
-// serialise).
+// Why L2 and not distributed shared memory: these passes are bound by how
+// fast operand bytes reach each SM (a 4-stage, 192 KB operand ring against the
+// L2 latency), and shared-memory grad slots would take 4 x 32 KB per CTA.
+// Through L2 the grad tiles cost the same inbound bytes, the shared memory
+// holds only the operand ring (so the logit tiles can be 256 columns wide:
+// fewer operand bytes per FLOP), and no slot is shared by two CTAs of a round.
+// The accumulate stage's B part (the d-slice's four 64-column blocks) comes in
+// one 3-D box when d_model % 64 == 0.
 //
 // Ring hand-over (per CTA, G_SLOTS slots of one supertile each): the writer
 // waits on its gfree[g] until every CTA of the cluster has loaded the slot's
-// previous tile (c remote arrivals, one per loader once its TMA completed),
-// writes, fences and arrives on gready[writer][g] in every CTA (4 warp
-// arrivals); a loader's TMA producer waits on gready before loading.
+// previous tile (c remote arrivals, one per loader's MMA issuer once the TMA
+// completed), writes, fences and arrives on gready[writer][g] in every CTA (4
+// warp arrivals, cluster-scope releases: they publish the tile); a loader's TMA
+// producer waits on gready before loading.  The MMA issuer's gfree arrival is
+// a CTA-scope release (it announces completed reads, and a cluster-scope
+// release would hold the issuer, and the tensor pipe, for about a thousand
+// clocks).
 //
 // BWD_FUSED is the d_hidden schedule run before any log-sum-exp is known: its
 // grad tile is the unnormalised G'[t][v] = 2^(s[t][v] log2e - r_t) with the
