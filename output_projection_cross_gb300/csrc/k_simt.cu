@@ -30,6 +30,7 @@
 #include "ptx.cuh"
 
 #include <cfloat>
+#include <type_traits>
 
 namespace lossk {
 
@@ -706,9 +707,9 @@ cudaError_t launch_combine_dh(const float *part, int64_t nsplit, int64_t n, int6
 }
 
 // ---------------------------------------------------------------------------
-// Cross-entropy from materialised logits.  One 512-thread block per row:
-// pass 1 streams the row with 16-byte loads and keeps an online (max, sum)
-// per thread, merged by a fixed tree; pass 2 (optional) writes grad_logits.
+// Cross-entropy from materialised logits.  One block per row: pass 1 streams
+// the row with 16-byte loads and keeps an online (max, sum) per thread, merged
+// by a fixed tree; pass 2 (optional) writes grad_logits.
 template <typename T> struct Vec;
 template <> struct Vec<float> { static constexpr int N = 4; };
 template <> struct Vec<uint16_t> { static constexpr int N = 8; };
@@ -790,93 +791,207 @@ __device__ __forceinline__ void online_merge(float &m, float &z, float m_o, floa
     m = M;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(512) from_logits_kernel(const T *__restrict__ logits,
-                                                          const int64_t *__restrict__ targets,
-                                                          const uint8_t *__restrict__ mask, int64_t V,
-                                                          double wz, double alpha,
-                                                          float *__restrict__ lse_out,
-                                                          float *__restrict__ ce_out,
-                                                          double *__restrict__ tokacc, int64_t n_pad,
-                                                          T *__restrict__ grad)
+// 16 bytes of a row as raw bits (`keep`: leave the line in L2 for a second
+// read; otherwise stream it past L2), and their NV values as fp32.
+__device__ __forceinline__ uint4 ld16(const void *p, bool keep)
+{
+    const uint4 *q = static_cast<const uint4 *>(p);
+    return keep ? __ldg(q) : __ldcs(q);
+}
+template <typename T> __device__ __forceinline__ void cvt16(const uint4 &v, float *f)
+{
+    if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = h16_lo<kIsF16<T>>(w[i]);
+            f[2 * i + 1] = h16_hi<kIsF16<T>>(w[i]);
+        }
+    }
+}
+
+// One 16-byte vector into a running (max m, sum z) in log2 units: the
+// vector's maximum first, one rescale if it rose, then its exponentials,
+// which do not depend on one another.
+template <int NV> __device__ __forceinline__ void online_vec(float &m, float &z, float (&f)[NV], float scale)
+{
+    float lm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        f[u] *= scale;
+        lm = fmaxf(lm, f[u]);
+    }
+    if (lm == -INFINITY) return;                   // every term is zero
+    if (lm > m) {
+        z *= ex2_approx(m - lm);
+        m = lm;
+    }
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; u += 2) {
+        z0 += ex2_approx(f[u] - m);
+        z1 += ex2_approx(f[u + 1] - m);
+    }
+    z += z0 + z1;
+}
+
+// The streaming row kernels run one block per row, each thread with FL_U
+// 16-byte loads in flight.  With a gradient, one 1024-thread block per SM:
+// enough bytes in flight to cover HBM latency, while the rows in flight (one
+// per SM, 46 MB at 152k bf16 logits) stay well inside L2, so the gradient
+// pass re-reads its row from L2 (four 512-thread blocks per SM kept 185 MB of
+// rows in flight, and the second read went back to HBM).  Without one, two
+// 512-thread blocks per SM, so that one block's end-of-row merge overlaps the
+// other's stream.
+constexpr int FL_THREADS_GRAD = 1024;
+constexpr int FL_THREADS_STAT = 512;
+constexpr int FL_U = 4;
+static_assert(FL_THREADS_GRAD / 32 <= 32 && FL_THREADS_STAT / 32 <= 32, "warp 0 merges one partial per warp");
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) from_logits_kernel(const T *__restrict__ logits,
+                                                                   const int64_t *__restrict__ targets,
+                                                                   const uint8_t *__restrict__ mask, int64_t V,
+                                                                   double wz, double alpha,
+                                                                   float *__restrict__ lse_out,
+                                                                   float *__restrict__ ce_out,
+                                                                   double *__restrict__ tokacc, int64_t n_pad,
+                                                                   T *__restrict__ grad)
 {
     constexpr int NV = Vec<T>::N;
     const int64_t t = blockIdx.x;
     const T *x = logits + t * V;
+    const int tid = threadIdx.x;
     const float L2E = static_cast<float>(LOG2E);
     const bool vec_ok = ((V * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    const bool keep = grad != nullptr;
     float m = -INFINITY, z = 0.f;
     if (vec_ok) {
         const int64_t nvec = V / NV;
-        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-            float f[NV];
-            load_vec<T>(x + i * NV, f, grad != nullptr);
+        for (int64_t base = 0; base < nvec; base += NT * FL_U) {
+            uint4 v[FL_U];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) online_add(m, z, f[u] * L2E);
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i < nvec) v[u] = ld16(x + i * NV, keep);
+            }
+#pragma unroll
+            for (int u = 0; u < FL_U; ++u) {
+                if (base + u * NT + tid >= nvec) continue;
+                float f[NV];
+                cvt16<T>(v[u], f);
+                online_vec<NV>(m, z, f, L2E);
+            }
         }
     } else {
-        for (int64_t i = threadIdx.x; i < V; i += blockDim.x) online_add(m, z, to_f(x[i]) * L2E);
+        for (int64_t i = tid; i < V; i += NT) online_add(m, z, to_f(x[i]) * L2E);
     }
-    // fixed-shape merge: warp butterfly, then warp 0 over the 16 warp results
+    // fixed-shape merge: a butterfly within each warp, then one over the 32
+    // warp partials in warp 0
     for (int o = 16; o > 0; o >>= 1) {
         const float mo = __shfl_xor_sync(0xffffffffu, m, o);
         const float zo = __shfl_xor_sync(0xffffffffu, z, o);
         online_merge(m, z, mo, zo);
     }
-    __shared__ float sm[16], sz[16];
-    __shared__ float s_lse2;
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) { sm[w] = m; sz[w] = z; }
+    __shared__ float sm[NT / 32], sz[NT / 32];
+    __shared__ float s_par[3];
+    const int w = tid >> 5, l = tid & 31;
+    if (l == 0) {
+        sm[w] = m;
+        sz[w] = z;
+    }
     __syncthreads();
     if (w == 0) {
-        m = l < 16 ? sm[l] : -INFINITY;
-        z = l < 16 ? sz[l] : 0.f;
+        m = l < NT / 32 ? sm[l] : -INFINITY;
+        z = l < NT / 32 ? sz[l] : 0.f;
         for (int o = 16; o > 0; o >>= 1) {
             const float mo = __shfl_xor_sync(0xffffffffu, m, o);
             const float zo = __shfl_xor_sync(0xffffffffu, z, o);
             online_merge(m, z, mo, zo);
         }
         if (l == 0) {
-            const double lse = (static_cast<double>(m) + log2(static_cast<double>(z))) * LN2;
+            // fp32 row statistics for 16-bit logits (far inside their 2e-3
+            // tolerance, and one lane's serial work per row here), fp64 for fp32
+            using M = typename std::conditional<sizeof(T) == 2, float, double>::type;
+            M lse2;
+            if constexpr (sizeof(T) == 2) lse2 = m + log2f(z);
+            else lse2 = static_cast<double>(m) + log2(static_cast<double>(z));
+            const M lse = lse2 * static_cast<M>(LN2);
             const bool on = mask ? (mask[t] != 0) : true;
-            const double ce = on ? lse - static_cast<double>(to_f(x[targets[t]])) : 0.0;
-            const double zz = on ? lse * lse : 0.0;
+            const M ce = on ? lse - static_cast<M>(to_f(x[targets[t]])) : M(0);
+            const M zz = on ? lse * lse : M(0);
             lse_out[t] = static_cast<float>(lse);
             if (ce_out) ce_out[t] = static_cast<float>(ce);
-            tokacc[t] = ce + wz * zz;
-            tokacc[n_pad + t] = ce;
-            tokacc[2 * n_pad + t] = zz;
-            s_lse2 = static_cast<float>(lse * LOG2E);
+            tokacc[t] = static_cast<double>(ce) + wz * static_cast<double>(zz);
+            tokacc[n_pad + t] = static_cast<double>(ce);
+            tokacc[2 * n_pad + t] = static_cast<double>(zz);
+            const M al = on ? static_cast<M>(alpha) : M(0);
+            s_par[0] = static_cast<float>(lse2);
+            s_par[1] = static_cast<float>(al * (M(1) + M(2) * static_cast<M>(wz) * lse));
+            s_par[2] = static_cast<float>(al);
         }
     }
     if (!grad) return;
     __syncthreads();
-    const float lse2 = s_lse2;
-    const bool on = mask ? (mask[t] != 0) : true;
-    const float at = on ? static_cast<float>(alpha) : 0.f;
-    const float c = on ? static_cast<float>(alpha * (1.0 + 2.0 * wz * lse2 * LN2)) : 0.f;
+    const float lse2 = s_par[0], c = s_par[1], at = s_par[2];
     const int64_t y = targets[t];
     T *g = grad + t * V;
     if (vec_ok) {
+        // the second read: from L2 (the row was read moments ago), then streamed out
         const int64_t nvec = V / NV;
-        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-            float f[NV], gv[NV];
-            load_vec<T>(x + i * NV, f, false);
+        for (int64_t base = 0; base < nvec; base += NT * FL_U) {
+            uint4 v[FL_U];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                gv[u] = c * ex2_approx(fmaf(f[u], L2E, -lse2));
-                if (i * NV + u == y) gv[u] -= at;
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i < nvec) v[u] = ld16(x + i * NV, false);
             }
-            store_vec(g + i * NV, gv);
+#pragma unroll
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i >= nvec) continue;
+                float f[NV], gv[NV];
+                cvt16<T>(v[u], f);
+#pragma unroll
+                for (int q = 0; q < NV; ++q) {
+                    gv[q] = c * ex2_approx(fmaf(f[q], L2E, -lse2));
+                    if (i * NV + q == y) gv[q] -= at;
+                }
+                store_vec(g + i * NV, gv);
+            }
         }
         return;
     }
-    for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
+    for (int64_t i = tid; i < V; i += NT) {
         float gv = c * ex2_approx(fmaf(to_f(x[i]), L2E, -lse2));
         if (i == y) gv -= at;
         from_f(gv, g[i]);
     }
+}
+
+template <typename T, int NT>
+static void launch_fl(const void *logits, const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
+                      double wz, double alpha, float *lse_out, float *ce_out, double *tokacc, int64_t n_pad,
+                      void *grad, cudaStream_t st)
+{
+    from_logits_kernel<T, NT><<<static_cast<unsigned>(n), NT, 0, st>>>(
+        static_cast<const T *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out, tokacc, n_pad,
+        static_cast<T *>(grad));
+}
+
+template <typename T>
+static void launch_fl_t(const void *logits, const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
+                        double wz, double alpha, float *lse_out, float *ce_out, double *tokacc, int64_t n_pad,
+                        void *grad, cudaStream_t st)
+{
+    if (grad)
+        launch_fl<T, FL_THREADS_GRAD>(logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, n_pad, grad, st);
+    else
+        launch_fl<T, FL_THREADS_STAT>(logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, n_pad, grad, st);
 }
 
 cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *targets,
@@ -886,24 +1001,18 @@ cudaError_t launch_from_logits(int dtype, const void *logits, const int64_t *tar
 {
     const int64_t n_pad = (n + TC_BM - 1) / TC_BM * TC_BM;
     if (dtype == 1)
-        from_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const uint16_t *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
-            tokacc, n_pad, static_cast<uint16_t *>(grad));
+        launch_fl_t<uint16_t>(logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, n_pad, grad, st);
     else if (dtype == 2)
-        from_logits_kernel<h16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const h16_t *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
-            tokacc, n_pad, static_cast<h16_t *>(grad));
+        launch_fl_t<h16_t>(logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, n_pad, grad, st);
     else
-        from_logits_kernel<float><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const float *>(logits), targets, mask, V, wz, alpha, lse_out, ce_out,
-            tokacc, n_pad, static_cast<float *>(grad));
+        launch_fl_t<float>(logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, n_pad, grad, st);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
 // Distillation from materialised student logits (the from-distribution
 // forward/backward with its z slot, "Fuse distillation + z-loss ...").  One
-// 512-thread block per token row.  Pass 1 streams the student and teacher
+// block per token row.  Pass 1 streams the student and teacher
 // rows once and keeps, per thread, online (max, sum) pairs for a = s log2e/T
 // and b = t log2e/T plus the direction's cross sums; the threads merge by a
 // fixed tree.  Pass 2 (optional) re-reads both rows (kept in L2 by pass 1's
@@ -961,8 +1070,72 @@ __device__ __forceinline__ void dl_merge(DlState<A> &S, const DlState<A> &O)
     S.mt = Mt;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(512) distill_logits_kernel(
+// One 16-byte vector of student and teacher logits into the running maxima,
+// sums and the direction's cross sums (as dl_add, vector-wise: the maxima
+// first, one rescale each if they rose, then the independent exponentials).
+template <typename T, typename A, int NV>
+__device__ __forceinline__ void dl_vec(DlState<A> &S, float (&fa)[NV], float (&fb)[NV], float kT, int direction)
+{
+    float lms = -INFINITY, lmt = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        fa[u] *= kT;
+        fb[u] *= kT;
+        lms = fmaxf(lms, fa[u]);
+        lmt = fmaxf(lmt, fb[u]);
+    }
+    if (lms > S.ms) {
+        const A f = static_cast<A>(teach_exp2<T>(S.ms - lms));
+        S.zs *= f;
+        S.xq *= f;
+        S.ms = lms;
+    }
+    if (lmt > S.mt) {
+        const A f = static_cast<A>(teach_exp2<T>(S.mt - lmt));
+        S.zt *= f;
+        S.xa *= f;
+        S.xb *= f;
+        S.mt = lmt;
+    }
+    A zs = 0, zt = 0, x1 = 0, x2 = 0;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const A es = static_cast<A>(teach_exp2<T>(fa[u] - S.ms));
+        const A et = static_cast<A>(teach_exp2<T>(fb[u] - S.mt));
+        zs += es;
+        zt += et;
+        if (direction == DIR_RKL) {
+            x1 += es * static_cast<A>(fa[u] - fb[u]);
+        } else {
+            x1 += et * static_cast<A>(fa[u]);
+            x2 += et * static_cast<A>(fb[u]);
+        }
+    }
+    S.zs += zs;
+    S.zt += zt;
+    if (direction == DIR_RKL) {
+        S.xq += x1;
+    } else {
+        S.xa += x1;
+        S.xb += x2;
+    }
+}
+
+template <typename T, typename A> __device__ __forceinline__ DlState<A> dl_shfl(const DlState<A> &x, int o)
+{
+    DlState<A> r;
+    r.ms = __shfl_xor_sync(0xffffffffu, x.ms, o);
+    r.mt = __shfl_xor_sync(0xffffffffu, x.mt, o);
+    r.zs = __shfl_xor_sync(0xffffffffu, x.zs, o);
+    r.zt = __shfl_xor_sync(0xffffffffu, x.zt, o);
+    r.xa = __shfl_xor_sync(0xffffffffu, x.xa, o);
+    r.xb = __shfl_xor_sync(0xffffffffu, x.xb, o);
+    r.xq = __shfl_xor_sync(0xffffffffu, x.xq, o);
+    return r;
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     const T *__restrict__ student, const T *__restrict__ teacher, const uint8_t *__restrict__ mask,
     int64_t V, int direction, float kT, double wz, double at_on, double inv_t, float *__restrict__ lse_out,
     float *__restrict__ per_token, double *__restrict__ tokacc, int64_t n_pad, T *__restrict__ grad,
@@ -972,68 +1145,85 @@ __global__ void __launch_bounds__(512) distill_logits_kernel(
     constexpr int NV = Vec<T>::N;
     const int64_t t = blockIdx.x;
     const T *xs = student + t * V, *xt = teacher + t * V;
+    const int tid = threadIdx.x;
     const bool vec_ok = ((V * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(student) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(teacher) % 16 == 0);
+    const bool keep = grad != nullptr;
     DlState<A> S{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
     if (vec_ok) {
         const int64_t nvec = V / NV;
-        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-            float fs[NV], ft[NV];
-            load_vec<T>(xs + i * NV, fs, grad != nullptr);
-            load_vec<T>(xt + i * NV, ft, grad != nullptr);
+        for (int64_t base = 0; base < nvec; base += NT * FL_U) {
+            uint4 vs[FL_U], vt[FL_U];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) dl_add<T, A>(S, fs[u] * kT, ft[u] * kT, direction);
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i < nvec) {
+                    vs[u] = ld16(xs + i * NV, keep);
+                    vt[u] = ld16(xt + i * NV, keep);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < FL_U; ++u) {
+                if (base + u * NT + tid >= nvec) continue;
+                float fa[NV], fb[NV];
+                cvt16<T>(vs[u], fa);
+                cvt16<T>(vt[u], fb);
+                dl_vec<T, A, NV>(S, fa, fb, kT, direction);
+            }
         }
     } else {
-        for (int64_t i = threadIdx.x; i < V; i += blockDim.x)
+        for (int64_t i = tid; i < V; i += NT)
             dl_add<T, A>(S, to_f(xs[i]) * kT, to_f(xt[i]) * kT, direction);
     }
-    for (int o = 16; o > 0; o >>= 1) {
-        DlState<A> O;
-        O.ms = __shfl_xor_sync(0xffffffffu, S.ms, o);
-        O.mt = __shfl_xor_sync(0xffffffffu, S.mt, o);
-        O.zs = __shfl_xor_sync(0xffffffffu, S.zs, o);
-        O.zt = __shfl_xor_sync(0xffffffffu, S.zt, o);
-        O.xa = __shfl_xor_sync(0xffffffffu, S.xa, o);
-        O.xb = __shfl_xor_sync(0xffffffffu, S.xb, o);
-        O.xq = __shfl_xor_sync(0xffffffffu, S.xq, o);
-        dl_merge<T, A>(S, O);
-    }
-    __shared__ DlState<A> sw[16];
+    // fixed-shape merge: a butterfly within each warp, then one over the 32
+    // warp partials in warp 0
+    for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(S, dl_shfl<T, A>(S, o));
+    __shared__ DlState<A> sw[NT / 32];
     __shared__ float sP[4];
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int w = tid >> 5, l = tid & 31;
     if (l == 0) sw[w] = S;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        DlState<A> R = sw[0];
-        for (int k = 1; k < 16; ++k) dl_merge<T, A>(R, sw[k]);
-        const double lse_s2 = static_cast<double>(R.ms) + log2(static_cast<double>(R.zs));
-        const double lse_t2 = static_cast<double>(R.mt) + log2(static_cast<double>(R.zt));
-        const double pa = static_cast<double>(R.xa) / static_cast<double>(R.zt);
-        const double pb = static_cast<double>(R.xb) / static_cast<double>(R.zt);
-        const double qx = static_cast<double>(R.xq) / static_cast<double>(R.zs);
-        double L2;
-        if (direction == DIR_CE) L2 = lse_s2 - pa;
-        else if (direction == DIR_FKL) L2 = pb - lse_t2 - pa + lse_s2;
-        else L2 = qx - lse_s2 + lse_t2;
-        const double L = L2 * LN2, lse_s = lse_s2 * LN2, lse_t = lse_t2 * LN2;
-        const bool on = mask ? (mask[t] != 0) : true;
-        const double Lm = on ? L : 0.0, z2 = on ? lse_s * lse_s : 0.0;
-        if (lse_out) lse_out[t] = static_cast<float>(lse_s);
-        if (per_token) per_token[t] = static_cast<float>(Lm);
-        tokacc[t] = Lm + wz * z2;
-        tokacc[n_pad + t] = Lm;
-        tokacc[2 * n_pad + t] = z2;
-        const double at = on ? at_on * inv_t : 0.0;
-        sP[0] = static_cast<float>(lse_s2);
-        sP[1] = static_cast<float>(lse_t2);
-        if (direction == DIR_RKL) {
-            sP[2] = static_cast<float>(at);
-            sP[3] = static_cast<float>(lse_t - lse_s - L + 2.0 * wz * lse_s);
-        } else {
-            sP[2] = static_cast<float>(at * (1.0 + 2.0 * wz * lse_s));
-            sP[3] = static_cast<float>(at);
+    if (w == 0) {
+        DlState<A> R = l < NT / 32 ? sw[l] : DlState<A>{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
+        for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(R, dl_shfl<T, A>(R, o));
+        if (l == 0) {
+            // fp32 row statistics for 16-bit logits (far inside their 2e-3
+            // tolerance, and one lane's serial work per row here), fp64 for fp32
+            using M = typename std::conditional<sizeof(T) == 2, float, double>::type;
+            auto lg2 = [](M v) -> M {
+                if constexpr (sizeof(T) == 2) return log2f(v);
+                else return log2(v);
+            };
+            const M lse_s2 = static_cast<M>(R.ms) + lg2(static_cast<M>(R.zs));
+            const M lse_t2 = static_cast<M>(R.mt) + lg2(static_cast<M>(R.zt));
+            const M pa = static_cast<M>(R.xa) / static_cast<M>(R.zt);
+            const M pb = static_cast<M>(R.xb) / static_cast<M>(R.zt);
+            const M qx = static_cast<M>(R.xq) / static_cast<M>(R.zs);
+            M L2;
+            if (direction == DIR_CE) L2 = lse_s2 - pa;
+            else if (direction == DIR_FKL) L2 = pb - lse_t2 - pa + lse_s2;
+            else L2 = qx - lse_s2 + lse_t2;
+            const M ln2 = static_cast<M>(LN2);
+            const M L = L2 * ln2, lse_s = lse_s2 * ln2, lse_t = lse_t2 * ln2;
+            const M wzm = static_cast<M>(wz);
+            const bool on = mask ? (mask[t] != 0) : true;
+            const M Lm = on ? L : M(0), z2 = on ? lse_s * lse_s : M(0);
+            if (lse_out) lse_out[t] = static_cast<float>(lse_s);
+            if (per_token) per_token[t] = static_cast<float>(Lm);
+            tokacc[t] = static_cast<double>(Lm) + wz * static_cast<double>(z2);
+            tokacc[n_pad + t] = static_cast<double>(Lm);
+            tokacc[2 * n_pad + t] = static_cast<double>(z2);
+            const M at = on ? static_cast<M>(at_on * inv_t) : M(0);
+            sP[0] = static_cast<float>(lse_s2);
+            sP[1] = static_cast<float>(lse_t2);
+            if (direction == DIR_RKL) {
+                sP[2] = static_cast<float>(at);
+                sP[3] = static_cast<float>(lse_t - lse_s - L + M(2) * wzm * lse_s);
+            } else {
+                sP[2] = static_cast<float>(at * (M(1) + M(2) * wzm * lse_s));
+                sP[3] = static_cast<float>(at);
+            }
         }
     }
     if (!grad) return;
@@ -1047,26 +1237,56 @@ __global__ void __launch_bounds__(512) distill_logits_kernel(
     };
     T *g = grad + t * V;
     if (vec_ok) {
+        // the second read: from L2 (both rows were read moments ago)
         const int64_t nvec = V / NV;
-        for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-            float fs[NV], ft[NV], gv[NV];
-            load_vec<T>(xs + i * NV, fs, false);
-            load_vec<T>(xt + i * NV, ft, false);
-            if (accumulate) load_vec<T>(g + i * NV, gv, false);
+        for (int64_t base = 0; base < nvec; base += NT * FL_U) {
+            uint4 vs[FL_U], vt[FL_U];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const float v = gval(fs[u] * kT, ft[u] * kT);
-                gv[u] = accumulate ? gv[u] + v : v;
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i < nvec) {
+                    vs[u] = ld16(xs + i * NV, false);
+                    vt[u] = ld16(xt + i * NV, false);
+                }
             }
-            store_vec(g + i * NV, gv);
+#pragma unroll
+            for (int u = 0; u < FL_U; ++u) {
+                const int64_t i = base + u * NT + tid;
+                if (i >= nvec) continue;
+                float fs[NV], ft[NV], gv[NV];
+                cvt16<T>(vs[u], fs);
+                cvt16<T>(vt[u], ft);
+                if (accumulate) load_vec<T>(g + i * NV, gv, false);
+#pragma unroll
+                for (int q = 0; q < NV; ++q) {
+                    const float v = gval(fs[q] * kT, ft[q] * kT);
+                    gv[q] = accumulate ? gv[q] + v : v;
+                }
+                store_vec(g + i * NV, gv);
+            }
         }
         return;
     }
-    for (int64_t i = threadIdx.x; i < V; i += blockDim.x) {
+    for (int64_t i = tid; i < V; i += NT) {
         float v = gval(to_f(xs[i]) * kT, to_f(xt[i]) * kT);
         if (accumulate) v += to_f(g[i]);
         from_f(v, g[i]);
     }
+}
+
+template <typename T>
+static void launch_dl_t(const void *student, const void *teacher, const uint8_t *mask, int64_t n, int64_t V,
+                        int direction, float kT, double wz, double at_on, double inv_t, float *lse_out,
+                        float *per_token, double *tokacc, int64_t n_pad, void *grad, int accumulate, cudaStream_t st)
+{
+    const T *xs = static_cast<const T *>(student), *xt = static_cast<const T *>(teacher);
+    T *g = static_cast<T *>(grad);
+    if (grad)
+        distill_logits_kernel<T, FL_THREADS_GRAD><<<static_cast<unsigned>(n), FL_THREADS_GRAD, 0, st>>>(
+            xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
+    else
+        distill_logits_kernel<T, FL_THREADS_STAT><<<static_cast<unsigned>(n), FL_THREADS_STAT, 0, st>>>(
+            xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
 }
 
 cudaError_t launch_distill_logits(int dtype, const void *student, const void *teacher, const uint8_t *mask,
@@ -1075,21 +1295,17 @@ cudaError_t launch_distill_logits(int dtype, const void *student, const void *te
                                   int64_t n_pad, void *grad, bool accumulate, cudaStream_t st)
 {
     const float kT = static_cast<float>(LOG2E / temperature);
+    const double inv_t = 1.0 / temperature;
+    const int acc = accumulate ? 1 : 0;
     if (dtype == 2)
-        distill_logits_kernel<h16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const h16_t *>(student), static_cast<const h16_t *>(teacher), mask, V, direction,
-            kT, wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<h16_t *>(grad),
-            accumulate ? 1 : 0);
+        launch_dl_t<h16_t>(student, teacher, mask, n, V, direction, kT, wz, at_on, inv_t, lse_out, per_token,
+                           tokacc, n_pad, grad, acc, st);
     else if (dtype == 1)
-        distill_logits_kernel<uint16_t><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const uint16_t *>(student), static_cast<const uint16_t *>(teacher), mask, V, direction,
-            kT, wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<uint16_t *>(grad),
-            accumulate ? 1 : 0);
+        launch_dl_t<uint16_t>(student, teacher, mask, n, V, direction, kT, wz, at_on, inv_t, lse_out, per_token,
+                              tokacc, n_pad, grad, acc, st);
     else
-        distill_logits_kernel<float><<<static_cast<unsigned>(n), 512, 0, st>>>(
-            static_cast<const float *>(student), static_cast<const float *>(teacher), mask, V, direction, kT,
-            wz, at_on, 1.0 / temperature, lse_out, per_token, tokacc, n_pad, static_cast<float *>(grad),
-            accumulate ? 1 : 0);
+        launch_dl_t<float>(student, teacher, mask, n, V, direction, kT, wz, at_on, inv_t, lse_out, per_token,
+                           tokacc, n_pad, grad, acc, st);
     return cudaGetLastError();
 }
 
