@@ -79,12 +79,16 @@ constexpr int B_MAXC = BWD_MAX_CL;                // CTAs per cluster at most
 constexpr int B_NBARS = 2 * B_NST + 4 + B_MAXC * G_SLOTS + G_SLOTS + 1 + 8;
 // The distillation d_weight pass reads its teacher block through TMA: per
 // epilogue warp two 32-token x 32-vocabulary bf16 buffers (2 KB each).
+// The plain d_weight pass uses the same 16 KB (four 1024-byte-aligned 4 KB
+// blocks) to stage each epilogue warp's 32 x 32 fp32 block of the accumulator
+// for a TMA store.
 constexpr int B_TBLK = 32 * 32 * 2;
 constexpr int B_TEACH = 4 * 2 * B_TBLK;
+constexpr int B_STG = 32 * 32 * 4;
+static_assert(4 * B_STG == B_TEACH, "the staging blocks fill the teacher-block region");
 template <int MODE, bool DISTILL> constexpr int bwd_smem()
 {
-    return 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + ((MODE == BWD_COLS && DISTILL) ? B_TEACH : 0) +
-           B_NBARS * 8 + 16;
+    return 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + (MODE == BWD_COLS ? B_TEACH : 0) + B_NBARS * 8 + 16;
 }
 static_assert(bwd_smem<BWD_COLS, true>() <= 232448, "fits the 227 KB per-CTA shared memory limit");
 static_assert(BWD_BN == 256 && TC_SLICE == 256, "one 256-column logit buffer + one 256-column accumulator");
@@ -161,8 +165,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     // d_weight: per-token parameters of a supertile's columns, one copy per epilogue warp
     float4 *sPall = reinterpret_cast<float4 *>(ring + B_NST * B_STAGE);
     constexpr bool TTMA = MODE == BWD_COLS && DISTILL;     // teacher blocks through TMA
+    constexpr bool STG = MODE == BWD_COLS && !DISTILL;     // accumulator staged for TMA stores
     uint8_t *tblk = reinterpret_cast<uint8_t *>(sPall + 4 * BWD_BN);   // [4 warps][2][32][32] bf16
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tblk + (TTMA ? B_TEACH : 0));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tblk + (MODE == BWD_COLS ? B_TEACH : 0));
     uint64_t *full = bars;                 // [B_NST]
     uint64_t *empty = full + B_NST;        // [B_NST]
     uint64_t *tfull = empty + B_NST;       // logit tile ready in TMEM
@@ -628,6 +633,42 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int n_rows = ROWS ? a.n_tok : a.vocab;
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(fixrow) * a.d;
+            if (STG && a.out_tma) {
+                // Plain d_weight: per 32-column chunk, each warp writes its 32 rows
+                // into its own 4 KB block (128-byte swizzle: the 16-byte piece k of
+                // row r sits at piece k ^ (r % 8), so a warp's stores hit every
+                // bank) and lane 0 stores the block with TMA, which also clips
+                // the vocabulary tail and d_model.  Only this warp waits on its
+                // block, so no barrier spans warps that may unwind apart.
+                uint8_t *stg = tblk + quad * B_STG;
+                const int row0 = w.fixed * 128 + quad * 32;
+                const uint32_t sb = smem_u32(stg) + static_cast<uint32_t>(lane) * 128;
+#pragma unroll 1
+                for (int q = 0; q < TC_SLICE / 32; ++q) {
+                    const int col = slice0 + q * 32;
+                    if (col >= a.d || row0 >= a.vocab) break;
+                    uint32_t v[32];
+                    tmem_ld32(trow + ACC_COL + q * 32, v);
+                    tmem_ld_wait();
+                    if (F16) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a.out_scale);
+                    }
+                    // the block's previous store has read it
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq)
+                        st_shared_v4(sb + ((static_cast<uint32_t>(kq) ^ (lane & 7)) << 4), v[4 * kq], v[4 * kq + 1],
+                                     v[4 * kq + 2], v[4 * kq + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&a.map_out, stg, col, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
             // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
             // stores (rows are d_model floats apart, d_model % 8 == 0, so every
             // chunk start is 32-byte aligned).
@@ -661,6 +702,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     }
                 }
             }
+            }
             tc_fence_before();
             mbar_arrive(accempty);
             u = u2;
@@ -671,6 +713,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         if (TTMA)
             for (int k = tuse_all; k < tiss_all; ++k) bw_wait_drain(&tw_b[k & 1], (k >> 1) & 1);
+        // this warp's accumulator stores are complete before the CTA leaves
+        if (STG && lane == 0) bulk_wait_all();
         tc_fence_before();
     }
     __syncthreads();

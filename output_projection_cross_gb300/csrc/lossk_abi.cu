@@ -99,6 +99,21 @@ bool make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, ui
 // inner/64}, block stride 128 B -- so one box {64, box_outer, nblk} lands nblk
 // 64-column blocks one after another (the MN-major operand layout, 128-byte
 // swizzle).  Needs inner % 64 == 0.
+// An fp32 [outer][inner] output written by 32 x 32 boxes from 128-byte-
+// swizzled shared memory (inner % 4 == 0, so rows are 16-byte multiples).
+bool make_map_out_f32(CUtensorMap *m, void *base, int64_t inner, int64_t outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || inner % 4 != 0) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_blocks(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, uint32_t box_outer,
                      uint32_t nblk)
 {
@@ -393,6 +408,9 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.out = (rows && L.nsplit > 1) ? w.dhpart() : dst;
             a.accumulate = (accumulate && a.out == dst) ? 1 : 0;
             a.out_scale = static_cast<float>(out_scale);
+            // d_weight leaves TMEM through shared memory and TMA stores (row-per-
+            // thread global stores would touch 32 lines per warp instruction)
+            a.out_tma = (!rows && !distill && !a.accumulate && make_map_out_f32(&a.map_out, dst, d, V)) ? 1 : 0;
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
