@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(fixrow) * a.d;
             if (STG && a.out_tma) {
-                // Plain d_weight: per 32-column chunk, each warp writes its 32 rows
+                // d_weight: per 32-column chunk, each warp writes its 32 rows
                 // into its own 4 KB block (128-byte swizzle: the 16-byte piece k of
                 // row r sits at piece k ^ (r % 8), so a warp's stores hit every
                 // bank) and lane 0 stores the block with TMA, which also clips
@@ -664,7 +664,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&a.map_out, stg, col, row0);
+                        // gradient accumulation: out += the accumulator, one add per element
+                        if (a.accumulate) tma_reduce_add_2d(&a.map_out, stg, col, row0);
+                        else tma_store_2d(&a.map_out, stg, col, row0);
                         bulk_commit_group();
                     }
                 }

@@ -120,7 +120,7 @@ struct BwdArgs {
     int ys3;               // map_ys3 is valid
     CUtensorMap map_teach; // distillation d_weight: teacher [n_tok][vocab] bf16, box {32, 32}
     CUtensorMap map_out;   // d_weight output [vocab][d_model] fp32, box {32, 32}, 128-byte swizzle
-    int out_tma;           // d_weight (no distillation, no accumulation): store through map_out
+    int out_tma;           // d_weight (no distillation): store (or, accumulating, add) through map_out
     uint16_t *gscr;        // the grad-tile ring itself
     const uint16_t *teacher; // teacher logits [n_tok][vocab] (bf16), read by the epilogue
     int n_tok, vocab, d;

@@ -165,6 +165,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                  "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
+// The same box added element-wise into global memory (fp32 add).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const void *src, int32_t x, int32_t y)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
