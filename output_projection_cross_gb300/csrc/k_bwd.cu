@@ -671,39 +671,40 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     }
                 }
             } else {
-            // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
-            // stores (rows are d_model floats apart, d_model % 8 == 0, so every
-            // chunk start is 32-byte aligned).
+                // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
+                // stores (rows are d_model floats apart, d_model % 8 == 0, so every
+                // chunk start is 32-byte aligned).
 #pragma unroll 1
-            for (int q = 0; q < TC_SLICE / 32; q += 2) {
-                uint32_t v[2][32];
-                tmem_ld32(trow + ACC_COL + q * 32, v[0]);
-                tmem_ld32(trow + ACC_COL + (q + 1) * 32, v[1]);
-                tmem_ld_wait();
+                for (int q = 0; q < TC_SLICE / 32; q += 2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(trow + ACC_COL + q * 32, v[0]);
+                    tmem_ld32(trow + ACC_COL + (q + 1) * 32, v[1]);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int col = slice0 + (q + h) * 32;
-                    if (fixrow < n_rows && col < a.d) {
-                        if (F16) {
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = slice0 + (q + h) * 32;
+                        if (fixrow < n_rows && col < a.d) {
+                            if (F16) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) * a.out_scale);
-                        }
-                        if (a.accumulate) {
-                            // gradient accumulation: out += this unit's accumulator
-                            for (int i = 0; i < 32; ++i)
-                                if (col + i < a.d) v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) + dst[col + i]);
-                        }
-                        if (col + 32 <= a.d) {
+                                for (int i = 0; i < 32; ++i)
+                                    v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) * a.out_scale);
+                            }
+                            if (a.accumulate) {
+                                // gradient accumulation: out += this unit's accumulator
+                                for (int i = 0; i < 32; ++i)
+                                    if (col + i < a.d)
+                                        v[h][i] = __float_as_uint(__uint_as_float(v[h][i]) + dst[col + i]);
+                            }
+                            if (col + 32 <= a.d) {
 #pragma unroll
-                            for (int i = 0; i < 32; i += 8) st_global_v8(dst + col + i, &v[h][i]);
-                        } else {
-                            for (int i = 0; i < 32; ++i)
-                                if (col + i < a.d) dst[col + i] = __uint_as_float(v[h][i]);
+                                for (int i = 0; i < 32; i += 8) st_global_v8(dst + col + i, &v[h][i]);
+                            } else {
+                                for (int i = 0; i < 32; ++i)
+                                    if (col + i < a.d) dst[col + i] = __uint_as_float(v[h][i]);
+                            }
                         }
                     }
                 }
-            }
             }
             tc_fence_before();
             mbar_arrive(accempty);
