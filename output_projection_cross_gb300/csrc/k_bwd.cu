@@ -408,6 +408,20 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                                   : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
         int m_all = 0;                                // own logit tiles consumed so far
         auto n_own_of = [&](const BwdUnit &w) { return crank < w.ny ? (w.ny - crank + c - 1) / c : 0; };
+        // d_weight with the token range whole (one split): a CTA's own token
+        // supertiles are the same in every unit, so their per-token parameters
+        // are loaded once, into one copy the four warps share (four supertiles
+        // at most: 16 KB).  The one barrier among the epilogue warps sits here,
+        // before any wait a warp could unwind from.
+        const int n_own_all = crank < a.n_loop ? (a.n_loop - crank + c - 1) / c : 0;
+        const bool pcache = !ROWS && a.n_split == 1 && n_own_all <= 4;
+        if (pcache) {
+            for (int i = r; i < n_own_all * BWD_BN; i += 128) {
+                const int t = ((i / BWD_BN) * c + crank) * BWD_BN + i % BWD_BN;
+                sPall[i] = t < a.n_tok ? a.tokp[t] : P0;
+            }
+            named_bar_sync(1, 128);
+        }
         auto params_of = [&](const BwdUnit &w) {      // d_hidden: the fixed token row's parameters
             const int fixrow = w.fixed * 128 + r;
             return (ROWS && fixrow < a.n_tok) ? a.tokp[fixrow] : P0;
@@ -444,7 +458,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int g = m_all % G_SLOTS;
             // the slot's previous tile has been loaded by every CTA of the cluster
             bool ok = mbar_wait_cluster(&gfree[g], ((m_all / G_SLOTS) & 1) ^ 1, err);
-            if (!ROWS) {
+            if (!ROWS && !pcache) {
                 // per-token parameters of this supertile's 256 token columns (each warp
                 // keeps its own copy, so no barrier spans warps that may unwind apart)
                 __syncwarp();
@@ -455,6 +469,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 }
                 __syncwarp();
             }
+            const float4 *sPt = pcache ? sPall + m * BWD_BN : sP;   // d_weight: the tile's token parameters
             if (DISTILL && m + 1 < n_own_of(w)) teacher_prefetch(w, m + 1);
             ok = ok && mbar_wait(tfull, m_all & 1, err);
             if (!__all_sync(0xffffffffu, ok)) return false;
@@ -548,7 +563,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     for (int uu = 0; uu < 2; ++uu) {
                         const int j = q * 32 + i + uu;           // loop column within the supertile
                         const float s = __uint_as_float(v[i + uu]);
-                        const float4 Pq = ROWS ? P : sP[j];
+                        const float4 Pq = ROWS ? P : sPt[j];
                         if (FUSED) {
                             const float gv = ex2_approx(fmaf(s, L2E, -Pq.x));
                             gg[uu] = gv;
