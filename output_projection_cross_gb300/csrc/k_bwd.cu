@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     float4 *sPall = reinterpret_cast<float4 *>(ring + B_NST * B_STAGE);
     constexpr bool TTMA = MODE == BWD_COLS && DISTILL;     // teacher blocks through TMA
     constexpr bool STG = MODE == BWD_COLS && !DISTILL;     // accumulator staged for TMA stores
+    constexpr bool GSTG = !TTMA;                           // grad tiles staged for TMA stores
+    static_assert(4 * BWD_BN * 16 == 4 * B_STG, "the parameter region holds four staging blocks");
     uint8_t *tblk = reinterpret_cast<uint8_t *>(sPall + 4 * BWD_BN);   // [4 warps][2][32][32] bf16
     uint64_t *bars = reinterpret_cast<uint64_t *>(tblk + (MODE == BWD_COLS ? B_TEACH : 0));
     uint64_t *full = bars;                 // [B_NST]
@@ -395,6 +397,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int quad = warp & 3;
         const int r = quad * 32 + lane;               // logit-tile row of this thread
         float4 *sP = sPall + quad * BWD_BN;           // this warp's copy
+        // This warp's 4 KB staging block for TMA stores: the teacher-block region
+        // in the d_weight pass, the (there unused) parameter region in the row passes.
+        uint8_t *gblk = (ROWS ? reinterpret_cast<uint8_t *>(sPall) : tblk) + quad * B_STG;
         uint8_t *tw_s = tblk + quad * 2 * B_TBLK;     // TTMA: this warp's two teacher buffers
         uint64_t *tw_b = tbar + quad * 2;
         // TTMA: issued and waited fills of each buffer.  Chunk q always uses buffer
@@ -540,6 +545,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             if (DISTILL) tload(0);
             if (TTMA) tissue(2);
             uint16_t *gdst = a.gscr + static_cast<int64_t>(((blockIdx.x * G_SLOTS + g) * 2) * 128 + r) * 128;
+            const int grow0 = ((blockIdx.x * G_SLOTS + g) * 2) * 128 + quad * 32;   // this warp's first ring row
             float zt = 0.f;
 #pragma unroll 1
             for (int q = 0; q < BWD_BN / 32; ++q) {
@@ -585,12 +591,38 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     pk[i >> 1] = pack_16x2<F16>(gg[0], gg[1]);
                 }
                 // columns q*32 .. q*32+31: sub-tile q/4, 64 bytes at column (q%4)*32
-                uint16_t *dst = gdst + (q >> 2) * (128 * 128) + (q & 3) * 32;
-                st_global_v8(dst, pk);
-                st_global_v8(dst + 16, pk + 8);
+                if (GSTG && a.g_tma) {
+                    // through this warp's staging block: chunk q in half q % 2 (64-byte
+                    // swizzle: the 16-byte piece k of row r sits at piece k ^ ((r / 2) % 4)),
+                    // stored by lane 0 with TMA once the half's previous store has read it
+                    uint8_t *h = gblk + (q & 1) * (B_STG / 2);
+                    if (lane == 0) {
+                        if (q == 0) bulk_wait_read_all();
+                        else if (q >= 2) bulk_wait_read_but1();
+                    }
+                    __syncwarp();
+                    const uint32_t hb = smem_u32(h) + static_cast<uint32_t>(lane) * 64;
+                    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3;
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq)
+                        st_shared_v4(hb + ((static_cast<uint32_t>(kq) ^ sw) << 4), pk[4 * kq], pk[4 * kq + 1],
+                                     pk[4 * kq + 2], pk[4 * kq + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&a.map_gst, h, (q & 3) * 32, grow0 + (q >> 2) * 128);
+                        bulk_commit_group();
+                    }
+                } else {
+                    uint16_t *dst = gdst + (q >> 2) * (128 * 128) + (q & 3) * 32;
+                    st_global_v8(dst, pk);
+                    st_global_v8(dst + 16, pk + 8);
+                }
             }
             if (FUSED) zsum += static_cast<double>(zt);
             if (TTMA && !__all_sync(0xffffffffu, tok_all)) return false;
+            // the staged stores have landed in global memory before the slot is published
+            if (GSTG && a.g_tma && lane == 0) bulk_wait_all();
             // the tile is out of TMEM: give the buffer back, then publish the slot
             tc_fence_before();
             mbar_arrive(tempty);
@@ -655,7 +687,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                 // bank) and lane 0 stores the block with TMA, which also clips
                 // the vocabulary tail and d_model.  Only this warp waits on its
                 // block, so no barrier spans warps that may unwind apart.
-                uint8_t *stg = tblk + quad * B_STG;
+                uint8_t *stg = gblk;
                 const int row0 = w.fixed * 128 + quad * 32;
                 const uint32_t sb = smem_u32(stg) + static_cast<uint32_t>(lane) * 128;
 #pragma unroll 1
@@ -731,8 +763,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         if (TTMA)
             for (int k = tuse_all; k < tiss_all; ++k) bw_wait_drain(&tw_b[k & 1], (k >> 1) & 1);
-        // this warp's accumulator stores are complete before the CTA leaves
-        if (STG && lane == 0) bulk_wait_all();
+        // this warp's TMA stores are complete before the CTA leaves
+        if (GSTG && lane == 0) bulk_wait_all();
         tc_fence_before();
     }
     __syncthreads();

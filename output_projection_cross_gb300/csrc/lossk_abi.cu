@@ -99,6 +99,21 @@ bool make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, ui
 // inner/64}, block stride 128 B -- so one box {64, box_outer, nblk} lands nblk
 // 64-column blocks one after another (the MN-major operand layout, 128-byte
 // swizzle).  Needs inner % 64 == 0.
+// The grad-tile ring [rows][128] bf16 written by 32 x 32 boxes from 64-byte-
+// swizzled shared memory.
+bool make_map_ring_store(CUtensorMap *m, void *base, int64_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {128 * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // An fp32 [outer][inner] output written by 32 x 32 boxes from 128-byte-
 // swizzled shared memory (inner % 4 == 0, so rows are 16-byte multiples).
 bool make_map_out_f32(CUtensorMap *m, void *base, int64_t inner, int64_t outer)
@@ -309,6 +324,7 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
         !make_map(&a->map_ys, Lp, d, nl, 64, 64) || !make_map(&a->map_g, w.gring(), 128, G_RING_ROWS, 64, 128))
         return false;
     a->ys3 = make_map_blocks(&a->map_ys3, Lp, d, nl, 64, 4) ? 1 : 0;
+    a->g_tma = make_map_ring_store(&a->map_gst, w.gring(), G_RING_ROWS) ? 1 : 0;
     const BwdGeom g = bwd_geometry(d, false);
     a->gscr = w.gring();
     a->n_tok = static_cast<int>(n);

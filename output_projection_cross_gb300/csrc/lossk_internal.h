@@ -119,6 +119,8 @@ struct BwdArgs {
     CUtensorMap map_ys3;   // map_ys as [64-column blocks][rows][64] (d_model % 64 == 0): one box {64, 64, 4}
     int ys3;               // map_ys3 is valid
     CUtensorMap map_teach; // distillation d_weight: teacher [n_tok][vocab] bf16, box {32, 32}
+    CUtensorMap map_gst;   // the grad-tile ring for stores, box {32, 32} bf16, 64-byte swizzle
+    int g_tma;             // map_gst is valid: grad tiles leave through shared memory and TMA
     CUtensorMap map_out;   // d_weight output [vocab][d_model] fp32, box {32, 32}, 128-byte swizzle
     int out_tma;           // d_weight (no distillation): store (or, accumulating, add) through map_out
     uint16_t *gscr;        // the grad-tile ring itself

@@ -182,6 +182,11 @@ __device__ __forceinline__ void bulk_wait_read_all()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// All but this thread's most recent committed bulk store have read their sources.
+__device__ __forceinline__ void bulk_wait_read_but1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // This thread's committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all()
 {
