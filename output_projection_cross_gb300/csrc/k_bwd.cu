@@ -15,7 +15,8 @@
 // + z-loss ...", "What it does": prob_coeff * softmax - label_coeff * onehot,
 // with the z term folded into prob_coeff, or the distribution-family form),
 // stores the bf16 tile into one of that CTA's slots of a global ring that
-// stays in L2, and signals every CTA of the cluster.  Every CTA then loads the
+// stays in L2 (each warp stages 32 x 32 chunks in shared memory and stores them
+// with TMA), and signals every CTA of the cluster.  Every CTA then loads the
 // tile with TMA like any other operand and adds G times its d-slice of the
 // loop tensor into its accumulator:
 //   d_hidden: D[tok][slice] += G[tok][voc] . W[voc][slice]
@@ -36,8 +37,9 @@
 // Ring hand-over (per CTA, G_SLOTS slots of one supertile each): the writer
 // waits on its gfree[g] until every CTA of the cluster has loaded the slot's
 // previous tile (c remote arrivals, one per loader's MMA issuer once the TMA
-// completed), writes, fences and arrives on gready[writer][g] in every CTA (4
-// warp arrivals, cluster-scope releases: they publish the tile); a loader's TMA
+// completed), writes, waits for its TMA stores to complete, fences and arrives
+// on gready[writer][g] in every CTA (4 warp arrivals, cluster-scope releases:
+// they publish the tile); a loader's TMA
 // producer waits on gready before loading.  The MMA issuer's gfree arrival is
 // a CTA-scope release (it announces completed reads, and a cluster-scope
 // release would hold the issuer, and the tensor pipe, for about a thousand
