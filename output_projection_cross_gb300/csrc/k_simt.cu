@@ -1239,9 +1239,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     };
     T *g = grad + t * V;
     if (vec_ok) {
-        // the second read: from L2 (both rows were read moments ago)
+        // the second read, last rounds first: the most recently read part of the
+        // rows is the most likely to be still in L2
         const int64_t nvec = V / NV;
-        for (int64_t base = 0; base < nvec; base += NT * FL_U) {
+        const int64_t nround = (nvec + NT * FL_U - 1) / (NT * FL_U);
+        for (int64_t rr = nround - 1; rr >= 0; --rr) {
+            const int64_t base = rr * NT * FL_U;
             uint4 vs[FL_U], vt[FL_U];
 #pragma unroll
             for (int u = 0; u < FL_U; ++u) {
