@@ -473,6 +473,41 @@ def test_distill_temperature_scaling_identity():
         assert np.array_equal(a["per_token"], b["per_token"])
 
 
+@pytest.mark.parametrize("T", [0.5, 2.0, 3.0])
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+def test_distill_two_class_closed_form(T, direction):
+    """Absolute distillation values at T != 1 by hand.  Student logits (0, T ln 3)
+    and teacher logits (0, 0) give q = softmax(s/T) = (1/4, 3/4) and p = (1/2, 1/2)
+    exactly, so every loss, lse, z term and gradient is a log of small rationals:
+      CE  = -(1/2 ln 1/4 + 1/2 ln 3/4) = ln 4 - 1/2 ln 3
+      fKL = 1/2 ln(1/2 / 1/4) + 1/2 ln(1/2 / 3/4) = 1/2 ln 4/3
+      rKL = 1/4 ln(1/4 / 1/2) + 3/4 ln(3/4 / 1/2) = 1/4 ln 1/2 + 3/4 ln 3/2
+      lse(s/T) = ln(1 + 3) = ln 4, z = (ln 4)^2
+    gradients with respect to s: (q - p)/T for CE and fKL,
+    q_i (ln q_i - ln p_i - rKL)/T for rKL, plus 2 w_z lse q / T for the z term."""
+    X = np.array([[0.0, T * math.log(3.0)]], dtype=np.float64)
+    Tt = np.zeros((1, 2))
+    wz = 0.3
+    r = oracle.distill_from_logits(X, Tt, direction, temperature=T, z_weight=wz)
+    q, pt = np.array([0.25, 0.75]), np.array([0.5, 0.5])
+    L = {"ce": math.log(4) - 0.5 * math.log(3), "fkl": 0.5 * math.log(4 / 3),
+         "rkl": 0.25 * math.log(0.5) + 0.75 * math.log(1.5)}[direction]
+    lse = math.log(4)
+    if direction == "rkl":
+        g = q * (np.log(q) - np.log(pt) - L) / T
+    else:
+        g = (q - pt) / T
+    g = g + 2 * wz * lse * q / T
+    # the student logit T ln 3 goes through fp32 in the oracle's interface:
+    # about 1e-7 relative, far below these bounds
+    assert abs(r["per_token"][0] - L) <= 1e-6
+    assert abs(r["lse"][0] - lse) <= 1e-6
+    assert abs(r["distill_mean"] - L) <= 1e-6
+    assert abs(r["z_mean"] - lse * lse) <= 1e-6
+    assert abs(r["total"] - (L + wz * lse * lse)) <= 1e-6
+    assert np.allclose(r["grad"][0], g, rtol=0, atol=1e-6)
+
+
 @pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
 @pytest.mark.parametrize("wz", [0.0, 0.2])
 def test_distill_grad_central_difference(direction, wz):
