@@ -632,6 +632,36 @@ def test_all_masked_gives_zeros(L):
     assert torch.all(torch.isfinite(o["lse"]))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
+def test_vocab_of_one(L, dtype):
+    """A single class: CE is zero and its gradient vanishes; only the z term
+    (lse^2, gradient 2 w_z lse) remains.  Both the training step and CE from
+    given logits, against the oracle."""
+    n, d, V = 130, 72, 1
+    g = np.random.default_rng(62)
+    Hn = li.round_to(g.standard_normal((n, d)).astype(np.float32), dtype)
+    Wn = li.round_to((g.standard_normal((V, d)) * 0.3).astype(np.float32), dtype)
+    yn = np.zeros(n, np.int64)
+    wz, gs = 0.05, 0.75
+    out = L.lossk_ce_fwd_bwd(_dev(Hn, dtype), _dev(Wn, dtype), _dev(yn, ""), z_weight=wz, grad_scale=gs)
+    torch.cuda.synchronize()
+    ref = oracle.ce_fwd(Hn, Wn, yn, z_weight=wz)
+    dH, dW = oracle.ce_bwd(Hn, Wn, yn, z_weight=wz, grad_scale=gs)
+    lt, gt = _tol(dtype)
+    close_loss(_np(out["ce"]), ref["ce"], lt)
+    close_loss(_np(out["lse"]), ref["lse"], lt)
+    close_loss(_np(out["scalars"]), [ref["total"], ref["ce_mean"], ref["z_mean"]], lt)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= gt
+    assert rel_l2(_np(out["d_weight"]), dW) <= gt
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    o = L.lossk_ce_from_logits(_dev(X, dtype), _dev(yn, ""), z_weight=wz, grad_scale=gs, want_grad=True)
+    torch.cuda.synchronize()
+    r = oracle.ce_from_logits(X, yn, z_weight=wz, grad_scale=gs, want_grad=True)
+    close_loss(_np(o["ce"]), r["ce"], lt)
+    close_loss(_np(o["scalars"]), [r["total"], r["ce_mean"], r["z_mean"]], lt)
+    assert rel_l2(_np(o["grad_logits"]), _grad_ref(r["grad"], dtype)) <= gt
+
+
 def test_device_status_clean_after_calls(L):
     n, d, V = 64, 64, 256
     ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, d, V, 1)

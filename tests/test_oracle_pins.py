@@ -162,6 +162,26 @@ def test_zero_weight_gives_log_vocab(V):
         assert r["total"] == pytest.approx(math.log(V) + 0.5 * math.log(V) ** 2, rel=1e-15)
 
 
+def test_vocab_of_one_closed_form():
+    """One class: the softmax is 1, so CE = lse - s_y = 0 and its gradient
+    vanishes; what remains is the z term, z = lse^2 = s^2, with d(loss)/ds =
+    a 2 w_z lse (a = grad_scale / n)."""
+    n, d, wz, gs = 5, 8, 0.05, 0.75
+    g = np.random.default_rng(61)
+    H = g.standard_normal((n, d)).astype(np.float32)
+    W = (g.standard_normal((1, d)) * 0.3).astype(np.float32)
+    y = np.zeros(n, np.int64)
+    r = oracle.ce_fwd(H, W, y, z_weight=wz)
+    dH, dW = oracle.ce_bwd(H, W, y, z_weight=wz, grad_scale=gs)
+    s = H.astype(np.float64) @ W.astype(np.float64).T          # [n][1]
+    assert np.all(r["ce"] == 0.0)
+    assert np.allclose(r["lse"], s[:, 0], rtol=0, atol=1e-12)
+    assert np.isclose(r["z_mean"], np.mean(s[:, 0] ** 2), rtol=1e-12)
+    gl = (gs / n) * 2 * wz * s                                   # d(loss)/ds, [n][1]
+    assert np.allclose(dH, gl * W.astype(np.float64), rtol=1e-10, atol=1e-14)
+    assert np.allclose(dW, gl.T @ H.astype(np.float64), rtol=1e-10, atol=1e-14)
+
+
 def test_z_is_lse_squared():
     H, W, y = _rand(3, 7, 4, 13)
     r = oracle.ce_fwd(H, W, y, chunk=3, z_weight=0.25)
