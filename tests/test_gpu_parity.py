@@ -662,6 +662,24 @@ def test_vocab_of_one(L, dtype):
     assert rel_l2(_np(o["grad_logits"]), _grad_ref(r["grad"], dtype)) <= gt
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
+@pytest.mark.parametrize("V", [1003, 3000, 70000])
+def test_distill_identical_teacher(L, dtype, V):
+    """Teacher logits equal to the student's: forward and reverse KL are zero
+    per token and their gradients are the z term's alone, against the oracle."""
+    n = 40
+    X = li.round_to((np.random.default_rng(V).standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    lt, gt = _tol(dtype)
+    for direction in ("fkl", "rkl"):
+        o = L.lossk_distill_from_logits(_dev(X, dtype), _dev(X, dtype), direction, temperature=1.7,
+                                        z_weight=0.2, want_grad=True)
+        torch.cuda.synchronize()
+        r = oracle.distill_from_logits(X, X, direction, temperature=1.7, z_weight=0.2)
+        assert np.abs(_np(o["per_token"])).max() <= lt
+        close_loss(_np(o["lse"]), r["lse"], lt)
+        assert rel_l2(_np(o["grad_logits"]), _grad_ref(r["grad"], dtype)) <= gt
+
+
 def test_device_status_clean_after_calls(L):
     n, d, V = 64, 64, 256
     ws = L.workspace(L.lossk.KIND_CE_FWD_BWD, n, d, V, 1)

@@ -493,6 +493,20 @@ def test_distill_temperature_scaling_identity():
         assert np.array_equal(a["per_token"], b["per_token"])
 
 
+@pytest.mark.parametrize("direction", ["fkl", "rkl"])
+def test_distill_identical_teacher_is_zero(direction):
+    """Teacher = student: both KL directions are zero and their gradient is the
+    z term's alone, 2 w_z lse q / T per token (mean over the counted tokens)."""
+    n, V, T, wz = 6, 11, 1.7, 0.2
+    X = (np.random.default_rng(63).standard_normal((n, V)) * 2).astype(np.float32)
+    r = oracle.distill_from_logits(X, X, direction, temperature=T, z_weight=wz)
+    assert np.allclose(r["per_token"], 0.0, rtol=0, atol=1e-12)
+    a = X.astype(np.float64) / T
+    lse = np.log(np.exp(a - a.max(1, keepdims=True)).sum(1)) + a.max(1)
+    q = np.exp(a - lse[:, None])
+    assert np.allclose(r["grad"], (1.0 / n) * 2 * wz * lse[:, None] * q / T, rtol=1e-10, atol=1e-14)
+
+
 @pytest.mark.parametrize("T", [0.5, 2.0, 3.0])
 @pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
 def test_distill_two_class_closed_form(T, direction):
