@@ -294,6 +294,32 @@ def test_qwen3_head_full_size_sampled(L, dtype):
     assert np.abs(dws).max() <= 1e-2 * np.abs(_np(out["d_weight"])).max()
 
 
+def test_largest_vocab(L):
+    """The largest vocabulary the contract accepts (2^24) at the largest chunk
+    it then allows (chunk * vocab = 2^27), with a few tokens: 65536 vocabulary
+    supertiles per token tile, 2 GB of bf16 weight and a 4.3 GB fp32 d_weight.
+    Every token's loss and d_hidden row and sampled d_weight rows against the
+    oracle, plus the vocabulary-sum identity of d_weight."""
+    n, d, V = 8, 64, 1 << 24
+    g = torch.Generator(device="cuda").manual_seed(11)
+    H = torch.randn(n, d, device="cuda", generator=g).to(torch.bfloat16)
+    W = (torch.randn(V, d, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    y = torch.randint(0, V, (n,), device="cuda", generator=g)
+    y[0], y[1] = 0, V - 1                       # the first and the last vocabulary row
+    out = L.lossk_ce_fwd_bwd(H, W, y, chunk=8)
+    torch.cuda.synchronize()
+    Hn, Wn, yn = H.float().cpu().numpy(), W.float().cpu().numpy(), y.cpu().numpy()
+    s = oracle.ce_token_rows(Hn, Wn, yn, np.arange(n))
+    close_loss(_np(out["lse"]), s["lse"], BF16_LOSS)
+    close_loss(_np(out["ce"]), s["lse"] - s["tgt"], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), s["dH"]) <= BF16_GRAD
+    vrows = np.concatenate([np.unique(yn), np.random.default_rng(12).choice(V, 24, replace=False)])
+    dw = oracle.ce_dweight_rows(Hn, Wn, yn, s["lse"], vrows)
+    assert rel_l2(_np(out["d_weight"][torch.from_numpy(vrows).cuda()]), dw) <= BF16_GRAD
+    dws = out["d_weight"].double().sum(0).cpu().numpy()
+    assert np.abs(dws).max() <= 1e-2 * np.abs(_np(out["d_weight"][torch.from_numpy(vrows).cuda()])).max()
+
+
 def test_ce_z_mask_reduced_full(L):
     """The CE + z-loss + mask recipe at a size the oracle finishes in seconds."""
     w = li.WORKLOADS["ce_z_8192x4096x128256"]
