@@ -320,6 +320,33 @@ def test_largest_vocab(L):
     assert np.abs(dws).max() <= 1e-2 * np.abs(_np(out["d_weight"][torch.from_numpy(vrows).cuda()])).max()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_d_weight_many_token_supertiles(L, dtype):
+    """1500 tokens at d_model 128: clusters of one CTA, each owning all six token
+    supertiles of a unit, more than the d_weight epilogue keeps in its shared
+    parameter copy; it then loads the parameters tile by tile.  Label CE and
+    distillation (the TMA teacher-block variant of the pass)."""
+    n, d, V = 1500, 128, 2000
+    x = _redraw(_inputs("ce_512x1024x32000", seed=71, n_tok=n, d_model=d, vocab=V), dtype, 3, n, d, V)
+    mask = li.mask(4, n, 0.1)
+    H, W, y = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(x["targets"], "")
+    out = L.lossk_ce_fwd_bwd(H, W, y, loss_mask=_dev(mask, ""), z_weight=1e-3, grad_scale=0.5)
+    torch.cuda.synchronize()
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], x["targets"], mask=mask, z_weight=1e-3, grad_scale=0.5)
+    lt, gt = _tol(dtype)
+    assert rel_l2(_np(out["d_hidden"]), dH) <= gt
+    assert rel_l2(_np(out["d_weight"]), dW) <= gt
+    Tt = li.round_to((np.random.default_rng(72).standard_normal((n, V)) * 3).astype(np.float32), dtype)
+    o = L.lossk_distill_fwd_bwd(H, W, _dev(Tt, dtype), "rkl", temperature=2.0, loss_mask=_dev(mask, ""),
+                                z_weight=1e-3, grad_scale=0.5)
+    torch.cuda.synchronize()
+    r = oracle.distill(x["hidden"], x["weight"], Tt, "rkl", temperature=2.0, mask=mask, z_weight=1e-3,
+                       grad_scale=0.5)
+    close_loss(_np(o["per_token"]), r["per_token"], lt)
+    assert rel_l2(_np(o["d_hidden"]), r["dH"]) <= gt
+    assert rel_l2(_np(o["d_weight"]), r["dW"]) <= gt
+
+
 def test_ce_z_mask_reduced_full(L):
     """The CE + z-loss + mask recipe at a size the oracle finishes in seconds."""
     w = li.WORKLOADS["ce_z_8192x4096x128256"]
