@@ -775,12 +775,15 @@ __device__ __forceinline__ void store_vec(h16_t *p, const float *g)
                                                     pack_f16x2(g[4], g[5]), pack_f16x2(g[6], g[7])));
 }
 
+// One term into a running (max m, sum z) in log2 units.  A -inf term (a
+// vocabulary entry masked out of the row) adds nothing; skipping it also
+// avoids 2^(-inf - (-inf)) while every term so far has been -inf.
 __device__ __forceinline__ void online_add(float &m, float &z, float x2)
 {
     if (x2 > m) {
         z = z * ex2_approx(m - x2) + 1.f;
         m = x2;
-    } else {
+    } else if (x2 != -INFINITY) {
         z += ex2_approx(x2 - m);
     }
 }

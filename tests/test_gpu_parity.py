@@ -531,6 +531,32 @@ def test_logits_rows_full_size_sampled(L):
         del o
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("V", [1000, 1003])
+def test_from_logits_masked_vocabulary(L, dtype, V):
+    """-inf logits (vocabulary entries masked out of a row) have probability 0:
+    finite lse and ce, a zero gradient there.  Whole 16-byte vectors of -inf
+    (V 1000) and the element-wise path (V 1003); one row keeps a single finite
+    entry, its target."""
+    n = 40
+    g = np.random.default_rng(V + 3)
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    X[:, 8:600] = -np.inf
+    X[:, : 3] = -np.inf
+    X[5, :] = -np.inf
+    y = g.integers(600, V, n).astype(np.int64)
+    X[5, y[5]] = 1.25
+    out = L.lossk_ce_from_logits(_dev(X, dtype), _dev(y, ""), z_weight=1e-3, want_grad=True)
+    torch.cuda.synchronize()
+    r = oracle.ce_from_logits(X, y, z_weight=1e-3, want_grad=True)
+    assert np.isfinite(_np(out["lse"])).all() and np.isfinite(_np(out["grad_logits"])).all()
+    lt, gt = _tol(dtype)
+    close_loss(_np(out["lse"]), r["lse"], lt)
+    close_loss(_np(out["ce"]), r["ce"], lt)
+    assert rel_l2(_np(out["grad_logits"]), r["grad"]) <= gt
+    assert np.all(_np(out["grad_logits"])[:, 8:600] == 0)
+
+
 def test_from_logits_uniform_golden(L):
     """6 tokens, vocab 9, every logit 0.25 -> mean loss ln 9 (the pages' worked example)."""
     X = torch.full((6, 9), 0.25, device="cuda", dtype=torch.float32)
