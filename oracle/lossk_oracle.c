@@ -448,17 +448,22 @@ static double distill_row(const double *s, const float *teach, int64_t V, int di
     for (int64_t v = 0; v < V; ++v) { a[v] = s[v] / T; b[v] = (double)teach[v] / T; }
     double la = lse_row(a, V), lb = lse_row(b, V);
     double L = 0.0;
+    /* An entry of probability 0 (a logit of -inf: a vocabulary entry masked
+     * out of the row) adds nothing: the limit x log x -> 0 as x -> 0.  Where the
+     * weighting probability is positive and the other one is 0, the term is
+     * +inf, and so is the loss. */
     for (int64_t v = 0; v < V; ++v) {
         double lq = a[v] - la, lp = b[v] - lb;
-        if (direction == 0) L -= exp(lp) * lq;
-        else if (direction == 1) L += exp(lp) * (lp - lq);
-        else L += exp(lq) * (lq - lp);
+        double q = exp(lq), p = exp(lp);
+        if (direction == 0) L -= p > 0.0 ? p * lq : 0.0;
+        else if (direction == 1) L += p > 0.0 ? p * (lp - lq) : 0.0;
+        else L += q > 0.0 ? q * (lq - lp) : 0.0;
     }
     if (g_out) {
         for (int64_t v = 0; v < V; ++v) {
             double lq = a[v] - la, lp = b[v] - lb;
             double q = exp(lq), p = exp(lp);
-            g_out[v] = direction == 2 ? q * (lq - lp - L) / T : (q - p) / T;
+            g_out[v] = direction == 2 ? (q > 0.0 ? q * (lq - lp - L) / T : 0.0) : (q - p) / T;
         }
     }
     *lse_a_out = la;

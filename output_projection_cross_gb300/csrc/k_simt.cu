@@ -202,9 +202,11 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
             E *= f;
             M = cm;
         }
+        // a -inf logit (a vocabulary entry masked out of the row) has
+        // probability 0 and adds nothing (0 log 0 = 0)
 #pragma unroll
         for (int i = 0; i < VEC; ++i)
-            if (i < nv) {
+            if (i < nv && x[i] != -INFINITY) {
                 const A e = static_cast<A>(teach_exp2<T>(fmaf(x[i], kT, -M)));
                 Z += e;
                 E += e * static_cast<A>(x[i]);
@@ -1046,13 +1048,15 @@ __device__ __forceinline__ void dl_add(DlState<A> &S, float a, float b, int dire
         S.xb *= f;
         S.mt = b;
     }
-    const A es = static_cast<A>(teach_exp2<T>(a - S.ms));
-    const A et = static_cast<A>(teach_exp2<T>(b - S.mt));
+    // a -inf logit has probability 0 and adds nothing to a sum it weights
+    // (0 log 0 = 0); a term whose weight is positive keeps its +-inf
+    const A es = a != -INFINITY ? static_cast<A>(teach_exp2<T>(a - S.ms)) : A(0);
+    const A et = b != -INFINITY ? static_cast<A>(teach_exp2<T>(b - S.mt)) : A(0);
     S.zs += es;
     S.zt += et;
     if (direction == DIR_RKL) {
-        S.xq += es * static_cast<A>(a - b);
-    } else {
+        if (es != A(0)) S.xq += es * static_cast<A>(a - b);
+    } else if (et != A(0)) {
         S.xa += et * static_cast<A>(a);
         S.xb += et * static_cast<A>(b);
     }
@@ -1105,13 +1109,14 @@ __device__ __forceinline__ void dl_vec(DlState<A> &S, float (&fa)[NV], float (&f
     A zs = 0, zt = 0, x1 = 0, x2 = 0;
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const A es = static_cast<A>(teach_exp2<T>(fa[u] - S.ms));
-        const A et = static_cast<A>(teach_exp2<T>(fb[u] - S.mt));
+        // as dl_add: a -inf logit adds nothing to the sums it weights
+        const A es = fa[u] != -INFINITY ? static_cast<A>(teach_exp2<T>(fa[u] - S.ms)) : A(0);
+        const A et = fb[u] != -INFINITY ? static_cast<A>(teach_exp2<T>(fb[u] - S.mt)) : A(0);
         zs += es;
         zt += et;
         if (direction == DIR_RKL) {
-            x1 += es * static_cast<A>(fa[u] - fb[u]);
-        } else {
+            if (es != A(0)) x1 += es * static_cast<A>(fa[u] - fb[u]);
+        } else if (et != A(0)) {
             x1 += et * static_cast<A>(fa[u]);
             x2 += et * static_cast<A>(fb[u]);
         }
@@ -1237,8 +1242,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     const float ln2f = static_cast<float>(LN2);
     auto gval = [&](float a, float b) {
         const float qv = teach_exp2<T>(a - ls2);
-        return direction == DIR_RKL ? pz * qv * fmaf(a - b, ln2f, pw)
-                                    : pz * qv - pw * teach_exp2<T>(b - lt2);
+        if (direction == DIR_RKL) return qv != 0.f ? pz * qv * fmaf(a - b, ln2f, pw) : 0.f;
+        return pz * qv - pw * teach_exp2<T>(b - lt2);
     };
     T *g = grad + t * V;
     if (vec_ok) {

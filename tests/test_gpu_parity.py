@@ -742,6 +742,57 @@ def test_vocab_of_one(L, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
+@pytest.mark.parametrize("V", [1000, 1003])
+def test_distill_from_logits_masked_vocabulary(L, dtype, V):
+    """The same vocabulary entries masked out (-inf) in student and teacher rows:
+    probability 0 on both sides, so the losses are finite and the gradient is 0
+    there; against the oracle, in all three directions, through whole 16-byte
+    vectors of -inf (V 1000) and the element-wise path (V 1003)."""
+    n = 37
+    g = np.random.default_rng(V + 5)
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    Tt = li.round_to((g.standard_normal((n, V)) * 3).astype(np.float32), dtype)
+    X[:, 0:3] = -np.inf
+    X[:, 40:400] = -np.inf
+    Tt[:, 0:3] = -np.inf
+    Tt[:, 40:400] = -np.inf
+    lt, gt = _tol(dtype)
+    for direction in ("ce", "fkl", "rkl"):
+        o = L.lossk_distill_from_logits(_dev(X, dtype), _dev(Tt, dtype), direction, temperature=1.5,
+                                        z_weight=1e-3, want_grad=True)
+        torch.cuda.synchronize()
+        r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, z_weight=1e-3)
+        assert np.isfinite(_np(o["per_token"])).all() and np.isfinite(_np(o["grad_logits"])).all()
+        close_loss(_np(o["per_token"]), r["per_token"], lt)
+        close_loss(_np(o["lse"]), r["lse"], lt)
+        assert rel_l2(_np(o["grad_logits"]), _grad_ref(r["grad"], dtype)) <= gt
+        assert np.all(_np(o["grad_logits"])[:, 40:400] == 0)
+
+
+@pytest.mark.parametrize("direction", ["ce", "fkl"])
+def test_distill_step_teacher_zeros(L, direction):
+    """The distillation training step with teacher logits of -inf on some vocabulary
+    entries (probability 0 for the teacher, the student's stays positive): CE and
+    forward KL stay finite (0 log 0 = 0 in the teacher's statistics), against the
+    oracle.  Reverse KL is +inf there by definition."""
+    n, d, V = 200, 136, 1032
+    x = _inputs("distill_z_4096x2048", seed=13, n_tok=n, d_model=d, vocab=V)
+    Tt = x["teacher"].copy()
+    Tt[:, 100:300] = -np.inf
+    Tt[7, :] = -np.inf
+    Tt[7, 5] = 2.0                               # a one-hot teacher row
+    H, W = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16")
+    out = L.lossk_distill_fwd_bwd(H, W, _dev(Tt, "bf16"), direction, temperature=2.0, z_weight=1e-3)
+    torch.cuda.synchronize()
+    r = oracle.distill(x["hidden"], x["weight"], Tt, direction, temperature=2.0, z_weight=1e-3)
+    assert np.isfinite(_np(out["per_token"])).all()
+    close_loss(_np(out["per_token"]), r["per_token"], BF16_LOSS)
+    close_loss(_np(out["scalars"]), [r["total"], r["distill_mean"], r["z_mean"]], BF16_LOSS)
+    assert rel_l2(_np(out["d_hidden"]), r["dH"]) <= BF16_GRAD
+    assert rel_l2(_np(out["d_weight"]), r["dW"]) <= BF16_GRAD
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
 @pytest.mark.parametrize("V", [1003, 3000, 70000])
 def test_distill_identical_teacher(L, dtype, V):
     """Teacher logits equal to the student's: forward and reverse KL are zero

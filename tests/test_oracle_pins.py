@@ -493,6 +493,30 @@ def test_distill_temperature_scaling_identity():
         assert np.array_equal(a["per_token"], b["per_token"])
 
 
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+def test_distill_masked_vocabulary_is_the_smaller_vocabulary(direction):
+    """Vocabulary entries masked out (-inf) in both the student and the teacher
+    row have probability 0 in both: the losses, lse and the gradient on the kept
+    entries equal those over the kept entries alone, and the gradient is 0 on
+    the masked ones."""
+    n, V, T, wz = 5, 23, 1.5, 0.1
+    g = np.random.default_rng(64)
+    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
+    Tt = (g.standard_normal((n, V)) * 3).astype(np.float32)
+    drop = np.array([0, 4, 5, 6, 13, 22])
+    keep = np.setdiff1d(np.arange(V), drop)
+    Xm, Tm = X.copy(), Tt.copy()
+    Xm[:, drop] = -np.inf
+    Tm[:, drop] = -np.inf
+    a = oracle.distill_from_logits(Xm, Tm, direction, temperature=T, z_weight=wz)
+    b = oracle.distill_from_logits(X[:, keep], Tt[:, keep], direction, temperature=T, z_weight=wz)
+    assert np.allclose(a["per_token"], b["per_token"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(a["lse"], b["lse"], rtol=1e-12, atol=1e-13)
+    assert np.isclose(a["total"], b["total"], rtol=1e-12)
+    assert np.allclose(a["grad"][:, keep], b["grad"], rtol=1e-12, atol=1e-15)
+    assert np.all(a["grad"][:, drop] == 0.0)
+
+
 @pytest.mark.parametrize("direction", ["fkl", "rkl"])
 def test_distill_identical_teacher_is_zero(direction):
     """Teacher = student: both KL directions are zero and their gradient is the
