@@ -207,10 +207,20 @@ def _code_only(text):
     return "".join("".join(out).split())
 
 
-def kernel_src_sha():
+# What builds the cluster passes and launches them: the kernel, the headers it
+# includes, and the host side that encodes its tensor maps and launch shapes.
+# The streaming and CTA-pair kernels are other translation units.
+BWD_KERNEL_SRCS = ("output_projection_cross_gb300/csrc/k_bwd.cu",
+                   "output_projection_cross_gb300/csrc/ptx.cuh",
+                   "output_projection_cross_gb300/csrc/lossk_internal.h",
+                   "output_projection_cross_gb300/csrc/lossk_abi.cu",
+                   "include/lossk.h")
+
+
+def kernel_src_sha(files=BWD_KERNEL_SRCS):
     h = hashlib.sha256()
-    for f in ("k_fwd2.cu", "k_bwd.cu", "k_simt.cu", "lossk_abi.cu", "ptx.cuh", "lossk_internal.h"):
-        with open(os.path.join(ROOT, "output_projection_cross_gb300", "csrc", f), encoding="utf-8") as fh:
+    for f in files:
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
