@@ -172,24 +172,24 @@ __device__ __forceinline__ float teach_exp2(float x)
     else return exp2f(x);
 }
 
-// One warp per token row, all rows at once (no block-level merge and no
-// partial last wave of blocks): 8 x 16 bytes in flight per lane.
-template <typename T>
-__global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict__ teach, int64_t n, int64_t V,
-                                                           float kT, double2 *__restrict__ out)
+// One warp's scan of a teacher row into (M, Z, E), merged over the lanes:
+// b = x kT for raw logits x, M the running maximum of b, Z = sum 2^(b - M) and
+// E = sum 2^(b - M) x (scaled by kT at the end), so each element costs one FFMA
+// into the exponent, one exp2, one add and one FFMA.
+// GUARD: a -inf logit (a vocabulary entry masked out of the row) has
+// probability 0 and adds nothing (0 log 0 = 0).  Without GUARD such a logit
+// leaves a NaN in Z or E (0 * -inf, or -inf - -inf while every entry so far
+// was -inf), so a row is scanned without it first and again with it only if
+// its sums come out non-finite.
+template <typename T, bool GUARD, typename A>
+__device__ __forceinline__ void teacher_scan(const T *__restrict__ row, int64_t V, int lane, float kT, float &M,
+                                             A &Z, A &E)
 {
-    using A = typename TeachAcc<T>::type;
     constexpr int VEC = 16 / sizeof(T);
     constexpr int UNR = 8;
-    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (t >= n) return;
-    const T *row = teach + t * V;
-    // Raw logits x, b = x kT.  M is the running maximum of b; E accumulates
-    // 2^(b - M) x (scaled by kT at the end), so each element costs one FFMA
-    // into the exponent, one exp2, one add and one FFMA.
-    float M = -INFINITY;
-    A Z = 0, E = 0;
+    M = -INFINITY;
+    Z = 0;
+    E = 0;
     auto absorb = [&](const float (&x)[VEC], int nv) {
         float cm = -INFINITY;
 #pragma unroll
@@ -202,11 +202,9 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
             E *= f;
             M = cm;
         }
-        // a -inf logit (a vocabulary entry masked out of the row) has
-        // probability 0 and adds nothing (0 log 0 = 0)
 #pragma unroll
         for (int i = 0; i < VEC; ++i)
-            if (i < nv && x[i] != -INFINITY) {
+            if (i < nv && (!GUARD || x[i] != -INFINITY)) {
                 const A e = static_cast<A>(teach_exp2<T>(fmaf(x[i], kT, -M)));
                 Z += e;
                 E += e * static_cast<A>(x[i]);
@@ -247,7 +245,7 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
     }
     E *= static_cast<A>(kT);
     // fixed xor tree over the lanes, in the accumulation type (fp64 is slow on
-    // this part, so bf16 rows merge in fp32)
+    // this part, so bf16 rows merge in fp32); every lane ends with the row
     for (int o = 16; o > 0; o >>= 1) {
         const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
         const A zo = __shfl_xor_sync(0xffffffffu, Z, o), eo = __shfl_xor_sync(0xffffffffu, E, o);
@@ -258,6 +256,24 @@ __global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict_
         E = E * f1 + eo * f2;
         M = Mn;
     }
+}
+
+// One warp per token row, all rows at once (no block-level merge and no
+// partial last wave of blocks): 8 x 16 bytes in flight per lane.
+template <typename T>
+__global__ void __launch_bounds__(256) teacher_stats_kernel(const T *__restrict__ teach, int64_t n, int64_t V,
+                                                           float kT, double2 *__restrict__ out)
+{
+    using A = typename TeachAcc<T>::type;
+    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= n) return;
+    const T *row = teach + t * V;
+    float M;
+    A Z, E;
+    teacher_scan<T, false>(row, V, lane, kT, M, Z, E);
+    if (!(isfinite(static_cast<float>(Z)) && isfinite(static_cast<float>(E))))
+        teacher_scan<T, true>(row, V, lane, kT, M, Z, E);
     if (lane == 0) {
         const double Zd = static_cast<double>(Z);
         out[t] = make_double2(static_cast<double>(M) + log2(Zd), static_cast<double>(E) / Zd);
@@ -1106,17 +1122,19 @@ __device__ __forceinline__ void dl_vec(DlState<A> &S, float (&fa)[NV], float (&f
         S.xb *= f;
         S.mt = lmt;
     }
+    // No -inf handling here: a -inf logit leaves a NaN or an infinity in the
+    // sums (0 * -inf, -inf - -inf), and the kernel recomputes such a row with
+    // dl_add, so rows of finite logits pay nothing for it.
     A zs = 0, zt = 0, x1 = 0, x2 = 0;
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        // as dl_add: a -inf logit adds nothing to the sums it weights
-        const A es = fa[u] != -INFINITY ? static_cast<A>(teach_exp2<T>(fa[u] - S.ms)) : A(0);
-        const A et = fb[u] != -INFINITY ? static_cast<A>(teach_exp2<T>(fb[u] - S.mt)) : A(0);
+        const A es = static_cast<A>(teach_exp2<T>(fa[u] - S.ms));
+        const A et = static_cast<A>(teach_exp2<T>(fb[u] - S.mt));
         zs += es;
         zt += et;
         if (direction == DIR_RKL) {
-            if (es != A(0)) x1 += es * static_cast<A>(fa[u] - fb[u]);
-        } else if (et != A(0)) {
+            x1 += es * static_cast<A>(fa[u] - fb[u]);
+        } else {
             x1 += et * static_cast<A>(fa[u]);
             x2 += et * static_cast<A>(fb[u]);
         }
@@ -1160,7 +1178,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
                         (reinterpret_cast<uintptr_t>(student) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(teacher) % 16 == 0);
     const bool keep = grad != nullptr;
-    DlState<A> S{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
+    const DlState<A> S0{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
+    DlState<A> S = S0;
     if (vec_ok) {
         const int64_t nvec = V / NV;
         for (int64_t base = 0; base < nvec; base += NT * FL_U) {
@@ -1187,16 +1206,44 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
             dl_add<T, A>(S, to_f(xs[i]) * kT, to_f(xt[i]) * kT, direction);
     }
     // fixed-shape merge: a butterfly within each warp, then one over the 32
-    // warp partials in warp 0
-    for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(S, dl_shfl<T, A>(S, o));
+    // warp partials in warp 0 (whose lanes hold the row's state after it)
     __shared__ DlState<A> sw[NT / 32];
     __shared__ float sP[4];
+    __shared__ int s_redo;
     const int w = tid >> 5, l = tid & 31;
-    if (l == 0) sw[w] = S;
-    __syncthreads();
+    auto block_merge = [&](DlState<A> X) {
+        for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(X, dl_shfl<T, A>(X, o));
+        if (l == 0) sw[w] = X;
+        __syncthreads();
+        DlState<A> R = S0;
+        if (w == 0) {
+            if (l < NT / 32) R = sw[l];
+            for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(R, dl_shfl<T, A>(R, o));
+        }
+        return R;
+    };
+    DlState<A> R = block_merge(S);
+    bool masked = false;
+    if (vec_ok) {
+        // vector sums that are not finite mean a -inf logit in the row (or an
+        // overflow, which the element-wise sums reproduce): recompute the row
+        // with dl_add's handling of -inf
+        if (tid == 0)
+            s_redo = !(isfinite(static_cast<float>(R.zs)) && isfinite(static_cast<float>(R.zt)) &&
+                       isfinite(static_cast<float>(R.xa)) && isfinite(static_cast<float>(R.xb)) &&
+                       isfinite(static_cast<float>(R.xq)));
+        __syncthreads();
+        masked = s_redo != 0;
+        if (masked) {
+            S = S0;
+            for (int64_t i = tid; i < V; i += NT)
+                dl_add<T, A>(S, to_f(xs[i]) * kT, to_f(xt[i]) * kT, direction);
+            R = block_merge(S);
+        }
+    } else {
+        masked = true;
+    }
     if (w == 0) {
-        DlState<A> R = l < NT / 32 ? sw[l] : DlState<A>{-INFINITY, -INFINITY, 0, 0, 0, 0, 0};
-        for (int o = 16; o > 0; o >>= 1) dl_merge<T, A>(R, dl_shfl<T, A>(R, o));
         if (l == 0) {
             // fp32 row statistics for 16-bit logits (far inside their 2e-3
             // tolerance, and one lane's serial work per row here), fp64 for fp32
@@ -1242,11 +1289,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     const float ln2f = static_cast<float>(LN2);
     auto gval = [&](float a, float b) {
         const float qv = teach_exp2<T>(a - ls2);
-        if (direction == DIR_RKL) return qv != 0.f ? pz * qv * fmaf(a - b, ln2f, pw) : 0.f;
+        if (direction == DIR_RKL) return pz * qv * fmaf(a - b, ln2f, pw);
         return pz * qv - pw * teach_exp2<T>(b - lt2);
     };
     T *g = grad + t * V;
-    if (vec_ok) {
+    // In reverse KL a -inf student logit has q = 0 and a gradient of 0, where
+    // gval's product q (a - b) would be 0 * -inf: rows that held a -inf take the
+    // element-wise loop, which tests for it.
+    if (vec_ok && !(masked && direction == DIR_RKL)) {
         // the second read, last rounds first: the most recently read part of the
         // rows is the most likely to be still in L2
         const int64_t nvec = V / NV;
@@ -1281,7 +1331,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
         return;
     }
     for (int64_t i = tid; i < V; i += NT) {
-        float v = gval(to_f(xs[i]) * kT, to_f(xt[i]) * kT);
+        const float a = to_f(xs[i]) * kT;
+        float v = direction == DIR_RKL && teach_exp2<T>(a - ls2) == 0.f ? 0.f : gval(a, to_f(xt[i]) * kT);
         if (accumulate) v += to_f(g[i]);
         from_f(v, g[i]);
     }
