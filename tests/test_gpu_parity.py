@@ -769,6 +769,42 @@ def test_distill_from_logits_masked_vocabulary(L, dtype, V):
         assert np.all(_np(o["grad_logits"])[:, 40:400] == 0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("V", [1000, 1003])
+@pytest.mark.parametrize("side", ["teacher", "student"])
+def test_distill_from_logits_one_sided_mask(L, dtype, V, side):
+    """Entries masked out (-inf) on one side only, against the oracle in all three
+    directions.  Where only the masked side's probability weights the term
+    (teacher zeros in CE and forward KL, student zeros in reverse KL) the loss
+    and the gradient are finite and match; where the other side keeps mass on a
+    masked entry the loss is +inf in both.  The whole-vector path recomputes
+    these rows element-wise (V 1000); V 1003 takes the element-wise path."""
+    n = 29
+    g = np.random.default_rng(V + 17)
+    X = li.round_to((g.standard_normal((n, V)) * 2).astype(np.float32), dtype)
+    Tt = li.round_to((g.standard_normal((n, V)) * 3).astype(np.float32), dtype)
+    tgt = Tt if side == "teacher" else X
+    tgt[:, 5:9] = -np.inf
+    tgt[:, 300:360] = -np.inf
+    tgt[3, 100] = -np.inf                                   # one more entry in one row
+    lt, gt = _tol(dtype)
+    for direction in ("ce", "fkl", "rkl"):
+        o = L.lossk_distill_from_logits(_dev(X, dtype), _dev(Tt, dtype), direction, temperature=1.5,
+                                        z_weight=1e-3, want_grad=True)
+        torch.cuda.synchronize()
+        r = oracle.distill_from_logits(X, Tt, direction, temperature=1.5, z_weight=1e-3)
+        got = _np(o["per_token"])
+        if (side == "student") == (direction != "rkl"):
+            assert np.all(np.isposinf(r["per_token"])) and np.all(np.isposinf(got))
+            continue
+        assert np.isfinite(got).all() and np.isfinite(_np(o["grad_logits"])).all()
+        close_loss(got, r["per_token"], lt)
+        close_loss(_np(o["lse"]), r["lse"], lt)
+        assert rel_l2(_np(o["grad_logits"]), _grad_ref(r["grad"], dtype)) <= gt
+        if side == "student":
+            assert np.all(_np(o["grad_logits"])[:, 300:360] == 0)
+
+
 @pytest.mark.parametrize("direction", ["ce", "fkl"])
 def test_distill_step_teacher_zeros(L, direction):
     """The distillation training step with teacher logits of -inf on some vocabulary

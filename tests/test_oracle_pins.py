@@ -517,6 +517,43 @@ def test_distill_masked_vocabulary_is_the_smaller_vocabulary(direction):
     assert np.all(a["grad"][:, drop] == 0.0)
 
 
+@pytest.mark.parametrize("direction", ["ce", "fkl", "rkl"])
+@pytest.mark.parametrize("side", ["teacher", "student"])
+def test_distill_one_sided_mask_is_the_limit(direction, side):
+    """Entries masked out (-inf) on one side only give the limit of a logit going
+    to -inf there.  Where the masked side's probability only weights the term
+    (teacher zeros in CE and forward KL, student zeros in reverse KL), the -inf
+    result equals that at a finite logit far enough down for exp to underflow
+    to 0.  Where the other side keeps mass on a masked entry (student zeros in
+    CE and forward KL, teacher zeros in reverse KL), the loss is +inf: the
+    finite stand-ins grow in proportion to the logit's depth."""
+    n, V, T, wz = 4, 19, 1.5, 0.1
+    g = np.random.default_rng(71)
+    X = (g.standard_normal((n, V)) * 2).astype(np.float32)
+    Tt = (g.standard_normal((n, V)) * 3).astype(np.float32)
+    drop = np.array([2, 3, 11])
+
+    def run(value):
+        Xm, Tm = X.copy(), Tt.copy()
+        (Tm if side == "teacher" else Xm)[:, drop] = value
+        return oracle.distill_from_logits(Xm, Tm, direction, temperature=T, z_weight=wz)
+
+    a, far, farther = run(-np.inf), run(-3000.0), run(-6000.0)
+    infinite = (side == "student") == (direction != "rkl")
+    if infinite:
+        assert np.all(np.isposinf(a["per_token"])) and np.isposinf(a["total"])
+        # the masked terms grow in proportion to the logit's depth: doubling it
+        # nearly doubles the loss
+        assert np.all(np.isfinite(far["per_token"])) and np.all(farther["per_token"] > 1.5 * far["per_token"])
+    else:
+        assert np.all(np.isfinite(a["per_token"]))
+        assert np.allclose(a["per_token"], far["per_token"], rtol=1e-12, atol=1e-13)
+        assert np.allclose(a["lse"], far["lse"], rtol=1e-12, atol=1e-13)
+        assert np.allclose(a["grad"], far["grad"], rtol=1e-12, atol=1e-15)
+        if side == "student":
+            assert np.all(a["grad"][:, drop] == 0.0)
+
+
 @pytest.mark.parametrize("direction", ["fkl", "rkl"])
 def test_distill_identical_teacher_is_zero(direction):
     """Teacher = student: both KL directions are zero and their gradient is the
