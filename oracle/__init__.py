@@ -72,6 +72,13 @@ def _load():
                                                         vp, vp, vp, vp]
             lib.oracle_distill_token_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, dbl,
                                                       dbl, dbl, vp, i64, vp, vp, vp]
+            lib.oracle_ce_shard_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp]
+            lib.oracle_ce_shard_combine.argtypes = [vp, i64, i64, vp, dbl, vp, vp, vp]
+            lib.oracle_ce_shard_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl,
+                                                vp, vp, vp]
+            lib.oracle_reduce_tokens.argtypes = [vp, vp, vp, i64, dbl, vp]
+            lib.oracle_distill_dweight_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, dbl,
+                                                        dbl, dbl, vp, vp, vp, i64, vp]
             _lib = lib
     return _lib
 
@@ -267,3 +274,79 @@ def distill_token_rows(H, W, teacher, direction, rows, temperature=1.0, mask=Non
     if st != 580:
         raise OracleError(st)
     return {"loss": loss, "lse": lse, "dH": dh}
+
+
+def distill_dweight_rows(H, W, teacher, direction, lse_all, loss_all, vrows, temperature=1.0,
+                         mask=None, z_weight=0.0, grad_scale=1.0):
+    """dW for the listed vocabulary rows, given every token's oracle lse(s/T)
+    and distillation loss (see oracle_distill_dweight_rows)."""
+    H, W, Tt = _f32(H), _f32(W), _f32(teacher)
+    n, d = H.shape
+    V = W.shape[0]
+    m, r = _mask(mask), _i64(vrows)
+    dirn = DIRECTIONS[direction] if isinstance(direction, str) else int(direction)
+    lse_all = np.ascontiguousarray(lse_all, dtype=np.float64)
+    loss_all = np.ascontiguousarray(loss_all, dtype=np.float64)
+    out = np.zeros((r.shape[0], d))
+    st = _load().oracle_distill_dweight_rows(_p(H), _p(W), _p(Tt), _p(m), n, d, V, dirn,
+                                             temperature, z_weight, grad_scale, _p(lse_all),
+                                             _p(loss_all), _p(r), r.shape[0], _p(out))
+    if st != 580:
+        raise OracleError(st)
+    return out
+
+
+def reduce_tokens(loss, lse, mask=None, z_weight=0.0):
+    """{total, loss mean, z mean} of per-token values (see oracle_reduce_tokens)."""
+    loss = np.ascontiguousarray(loss, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    m = _mask(mask)
+    scal = np.zeros(3)
+    st = _load().oracle_reduce_tokens(_p(loss), _p(lse), _p(m), loss.shape[0], z_weight, _p(scal))
+    if st != 580:
+        raise OracleError(st)
+    return {"total": scal[0], "loss_mean": scal[1], "z_mean": scal[2]}
+
+
+# ---- vocabulary-parallel cross-entropy (see oracle_ce_shard_fwd) ---------------
+
+def ce_shard_fwd(H, W_shard, targets, v0, vocab_total):
+    """Partials [3][n] of one vocabulary shard: lse over the shard, the target
+    logit if the shard holds the target (else 0), and that 1/0 flag."""
+    H, Ws = _f32(H), _f32(W_shard)
+    n, d = H.shape
+    Vs = Ws.shape[0]
+    y = _i64(targets)
+    out = np.zeros((3, n))
+    st = _load().oracle_ce_shard_fwd(_p(H), _p(Ws), _p(y), n, d, Vs, v0, vocab_total, _p(out))
+    if st != 580:
+        raise OracleError(st)
+    return out
+
+
+def ce_shard_combine(partials_all, mask=None, z_weight=0.0):
+    """lse, ce and the three scalars from the shards' partials [P][3][n]."""
+    pa = np.ascontiguousarray(partials_all, dtype=np.float64)
+    P, _, n = pa.shape
+    m = _mask(mask)
+    lse, ce, scal = np.zeros(n), np.zeros(n), np.zeros(3)
+    st = _load().oracle_ce_shard_combine(_p(pa), P, n, _p(m), z_weight, _p(lse), _p(ce), _p(scal))
+    if st != 580:
+        raise OracleError(st)
+    return {"lse": lse, "ce": ce, "total": scal[0], "ce_mean": scal[1], "z_mean": scal[2]}
+
+
+def ce_shard_bwd(H, W_shard, targets, v0, vocab_total, lse_all, mask=None, z_weight=0.0,
+                 grad_scale=1.0):
+    """The shard's share of d_hidden [n][d] and its d_weight rows [Vs][d]."""
+    H, Ws = _f32(H), _f32(W_shard)
+    n, d = H.shape
+    Vs = Ws.shape[0]
+    y, m = _i64(targets), _mask(mask)
+    lse_all = np.ascontiguousarray(lse_all, dtype=np.float64)
+    dh, dw = np.zeros((n, d)), np.zeros((Vs, d))
+    st = _load().oracle_ce_shard_bwd(_p(H), _p(Ws), _p(y), _p(m), n, d, Vs, v0, vocab_total,
+                                     z_weight, grad_scale, _p(lse_all), _p(dh), _p(dw))
+    if st != 580:
+        raise OracleError(st)
+    return dh, dw

@@ -656,3 +656,209 @@ int oracle_distill_token_rows(const float *H, const float *W, const float *teach
     }
     return OR_OK;
 }
+
+/* Sampled distillation d_weight rows, for checks at sizes where the whole
+ * oracle is too slow.  Per listed vocabulary row v, dW_v = sum_t G_tv H_t in
+ * ascending t, with G_tv exactly as in oracle_distill: the student's lse(a)
+ * and L_t of every token are given (from oracle_distill_token_rows over all
+ * tokens); the teacher's lse(b) is recomputed here from each teacher row. */
+int oracle_distill_dweight_rows(const float *H, const float *W, const float *teacher,
+                                const uint8_t *mask, int64_t n, int64_t d, int64_t V,
+                                int direction, double T, double wz, double grad_scale,
+                                const double *lse_all, const double *loss_all,
+                                const int64_t *vrows, int64_t n_vrows, double *dW_rows)
+{
+    int st = fused_checks(n, d, V, 0, NULL, wz, grad_scale);
+    if (st != OR_OK) return st;
+    if (!scalar_ok(T) || T <= 0.0) return OR_NON_FINITE_SCALAR;
+    if (direction < 0 || direction > 2) return OR_UNKNOWN_OBJECTIVE;
+    int64_t nvalid = count_valid(mask, n);
+    double *lb = (double *)malloc(sizeof(double) * (size_t)n);
+    #pragma omp parallel
+    {
+        double *b = (double *)malloc(sizeof(double) * (size_t)V);
+        #pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            const float *tr = teacher + t * V;
+            for (int64_t v = 0; v < V; ++v) b[v] = (double)tr[v] / T;
+            lb[t] = lse_row(b, V);
+        }
+        free(b);
+    }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_vrows; ++i) {
+        int64_t v = vrows[i];
+        double *dw = dW_rows + i * d;
+        for (int64_t k = 0; k < d; ++k) dw[k] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            int on = mask ? (mask[t] != 0) : 1;
+            if (!on || nvalid == 0) continue;
+            double alpha = grad_scale / (double)nvalid;
+            double a = dot_asc(H + t * d, W + v * d, d) / T;
+            double b = (double)teacher[t * V + v] / T;
+            double lq = a - lse_all[t], lp = b - lb[t];
+            double q = exp(lq), p = exp(lp);
+            double g = direction == 2 ? (q > 0.0 ? q * (lq - lp - loss_all[t]) / T : 0.0) : (q - p) / T;
+            double gv = alpha * (g + 2.0 * wz * lse_all[t] * q / T);
+            const float *h = H + t * d;
+            for (int64_t k = 0; k < d; ++k) dw[k] += gv * (double)h[k];
+        }
+    }
+    free(lb);
+    return OR_OK;
+}
+
+/* The token reduction of oracle_distill and oracle_ce_fwd on its own, for
+ * per-token values computed row by row (oracle_distill_token_rows over every
+ * token): loss[t] is L_t (or ce_t) of every token whether counted or not,
+ * lse[t] the token's log-sum-exp; masked tokens add nothing.  Sums run in
+ * ascending t; scal = {total, loss mean, z mean} ([P3] shared mask and
+ * divisor), zeros when N_valid = 0. */
+int oracle_reduce_tokens(const double *loss, const double *lse, const uint8_t *mask, int64_t n,
+                         double wz, double *scal)
+{
+    if (n < 1) return OR_EMPTY_DIMENSION;
+    if (!scalar_ok(wz) || wz < 0.0) return OR_NON_FINITE_SCALAR;
+    int64_t nvalid = count_valid(mask, n);
+    double sum_tok = 0.0, sum_l = 0.0, sum_z = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        int on = mask ? (mask[t] != 0) : 1;
+        double l = on ? loss[t] : 0.0, z = on ? lse[t] * lse[t] : 0.0;
+        sum_tok += l + wz * z;
+        sum_l += l;
+        sum_z += z;
+    }
+    if (nvalid > 0) {
+        scal[0] = sum_tok / (double)nvalid;
+        scal[1] = sum_l / (double)nvalid;
+        scal[2] = sum_z / (double)nvalid;
+    } else {
+        scal[0] = scal[1] = scal[2] = 0.0;
+    }
+    return OR_OK;
+}
+
+/* ---- vocabulary-parallel cross-entropy -----------------------------------
+ * [P3] "Changes" (its tests add a tensor-parallel distributed subtest) and
+ * "Validation" (the world_size=2 tensor-parallel subtests): the weight's
+ * vocabulary rows are split into contiguous shards, one per rank.  The pages
+ * do not print the exchange; the plain reading, which this oracle states:
+ *
+ *   shard p holds rows [v0, v0 + Vs) of a vocabulary of V_total.  Per token
+ *   its partials are  lse_p = log sum_{v in shard} exp(s_tv),  the target
+ *   logit s_{t,y_t} when v0 <= y_t < v0 + Vs (else 0), and a flag 1/0 saying
+ *   which.  The whole row's log-sum-exp is the max-shifted log of the sum of
+ *   exp(lse_p) over the shards, the target logit comes from the one shard
+ *   whose flag is set, and everything after that (ce, z, the token mean) is
+ *   the unsharded loss's.  The backward of a shard is the unsharded
+ *   backward restricted to the shard's vocabulary columns, with the whole
+ *   row's lse: it gives the shard's d_weight rows and its share of d_hidden,
+ *   whose sum over the shards is d_hidden.
+ *
+ * partials layout: [3][n] for one shard, [P][3][n] gathered in shard order. */
+int oracle_ce_shard_fwd(const float *H, const float *Ws, const int64_t *y, int64_t n, int64_t d,
+                        int64_t Vs, int64_t v0, int64_t V_total, double *partials)
+{
+    if (n < 1 || d < 1 || Vs < 1 || V_total < 1) return OR_EMPTY_DIMENSION;
+    if (v0 < 0 || v0 > V_total - Vs) return OR_LENGTH_MISMATCH;
+    if (!oracle_targets_in_range(y, n, V_total)) return OR_TARGET_OUT_OF_RANGE;
+    #pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Vs);
+        #pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            for (int64_t v = 0; v < Vs; ++v) s[v] = dot_asc(H + t * d, Ws + v * d, d);
+            int64_t yl = y[t] - v0;
+            int in = yl >= 0 && yl < Vs;
+            partials[t] = lse_row(s, Vs);
+            partials[n + t] = in ? s[yl] : 0.0;
+            partials[2 * n + t] = in ? 1.0 : 0.0;
+        }
+        free(s);
+    }
+    return OR_OK;
+}
+
+int oracle_ce_shard_combine(const double *partials, int64_t P, int64_t n, const uint8_t *mask,
+                            double wz, double *lse_out, double *ce_out, double *scal)
+{
+    if (n < 1 || P < 1) return OR_EMPTY_DIMENSION;
+    if (!scalar_ok(wz) || wz < 0.0) return OR_NON_FINITE_SCALAR;
+    for (int64_t t = 0; t < n; ++t) {
+        double flags = 0.0;
+        for (int64_t p = 0; p < P; ++p) flags += partials[(p * 3 + 2) * n + t];
+        if (flags != 1.0) return OR_TARGET_OUT_OF_RANGE;   /* no shard, or two, hold the target */
+    }
+    int64_t nvalid = count_valid(mask, n);
+    double sum_tok = 0.0, sum_ce = 0.0, sum_z = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        double m = partials[t];
+        for (int64_t p = 1; p < P; ++p)
+            if (partials[p * 3 * n + t] > m) m = partials[p * 3 * n + t];
+        double acc = 0.0, tgt = 0.0;
+        for (int64_t p = 0; p < P; ++p) {
+            acc += exp(partials[p * 3 * n + t] - m);
+            if (partials[(p * 3 + 2) * n + t] != 0.0) tgt = partials[(p * 3 + 1) * n + t];
+        }
+        double lse = m + log(acc);
+        int on = mask ? (mask[t] != 0) : 1;
+        lse_out[t] = lse;
+        ce_out[t] = on ? lse - tgt : 0.0;
+        double z = on ? lse * lse : 0.0;
+        sum_tok += ce_out[t] + wz * z;
+        sum_ce += ce_out[t];
+        sum_z += z;
+    }
+    if (nvalid > 0) {
+        scal[0] = sum_tok / (double)nvalid;
+        scal[1] = sum_ce / (double)nvalid;
+        scal[2] = sum_z / (double)nvalid;
+    } else {
+        scal[0] = scal[1] = scal[2] = 0.0;
+    }
+    return OR_OK;
+}
+
+int oracle_ce_shard_bwd(const float *H, const float *Ws, const int64_t *y, const uint8_t *mask,
+                        int64_t n, int64_t d, int64_t Vs, int64_t v0, int64_t V_total, double wz,
+                        double grad_scale, const double *lse_all, double *dH_part, double *dW_shard)
+{
+    if (n < 1 || d < 1 || Vs < 1 || V_total < 1) return OR_EMPTY_DIMENSION;
+    if (v0 < 0 || v0 > V_total - Vs) return OR_LENGTH_MISMATCH;
+    if (!scalar_ok(wz) || wz < 0.0 || !scalar_ok(grad_scale)) return OR_NON_FINITE_SCALAR;
+    if (!oracle_targets_in_range(y, n, V_total)) return OR_TARGET_OUT_OF_RANGE;
+    int64_t nvalid = count_valid(mask, n);
+    double *G = (double *)malloc(sizeof(double) * (size_t)(n * Vs));
+    #pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        int on = mask ? (mask[t] != 0) : 1;
+        double alpha = (on && nvalid > 0) ? grad_scale / (double)nvalid : 0.0;
+        double c = alpha * (1.0 + 2.0 * wz * lse_all[t]);
+        for (int64_t v = 0; v < Vs; ++v) {
+            double g = c * exp(dot_asc(H + t * d, Ws + v * d, d) - lse_all[t]);
+            if (v0 + v == y[t]) g -= alpha;
+            G[t * Vs + v] = g;
+        }
+        if (dH_part) {
+            double *dh = dH_part + t * d;
+            for (int64_t k = 0; k < d; ++k) dh[k] = 0.0;
+            for (int64_t v = 0; v < Vs; ++v) {
+                const float *w = Ws + v * d;
+                for (int64_t k = 0; k < d; ++k) dh[k] += G[t * Vs + v] * (double)w[k];
+            }
+        }
+    }
+    if (dW_shard) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t v = 0; v < Vs; ++v) {
+            double *dw = dW_shard + v * d;
+            for (int64_t k = 0; k < d; ++k) dw[k] = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                const float *h = H + t * d;
+                for (int64_t k = 0; k < d; ++k) dw[k] += G[t * Vs + v] * (double)h[k];
+            }
+        }
+    }
+    free(G);
+    return OR_OK;
+}

@@ -670,3 +670,95 @@ def test_sampled_rows_match_full():
     assert np.allclose(sd["loss"][[0, 2]], full["per_token"][rows][[0, 2]], rtol=1e-13)
     assert np.array_equal(sd["lse"], full["lse"][rows])
     assert np.allclose(sd["dH"], full["dH"][rows], rtol=1e-12, atol=1e-17)
+    # d_weight rows from every token's lse and loss, all three objectives, with the
+    # masked token among the sums (its loss enters nothing)
+    for direction in ("ce", "fkl", "rkl"):
+        full = oracle.distill(H, W, Tt, direction, temperature=2.0, mask=mask, z_weight=wz,
+                              grad_scale=gs)
+        allr = oracle.distill_token_rows(H, W, Tt, direction, np.arange(12), temperature=2.0,
+                                         mask=mask, z_weight=wz, grad_scale=gs, want_dh=False)
+        assert np.array_equal(allr["lse"], full["lse"])
+        dwd = oracle.distill_dweight_rows(H, W, Tt, direction, allr["lse"], allr["loss"], v,
+                                          temperature=2.0, mask=mask, z_weight=wz, grad_scale=gs)
+        assert np.allclose(dwd, full["dW"][v], rtol=1e-11, atol=1e-17), direction
+        # the token reduction on its own gives the full oracle's scalars, bit for bit
+        r = oracle.reduce_tokens(allr["loss"], allr["lse"], mask=mask, z_weight=wz)
+        assert (r["total"], r["loss_mean"], r["z_mean"]) == (full["total"], full["distill_mean"],
+                                                             full["z_mean"])
+    r = oracle.reduce_tokens(f["ce"], f["lse"], mask=mask, z_weight=wz)
+    assert (r["total"], r["loss_mean"], r["z_mean"]) == (f["total"], f["ce_mean"], f["z_mean"])
+    assert oracle.reduce_tokens(f["ce"], f["lse"], mask=np.zeros(12, np.uint8))["total"] == 0.0
+
+
+# ---- vocabulary-parallel cross-entropy ------------------------------------------
+
+def _shards(V, bounds):
+    """[(v0, Vs)] for cut points `bounds` inside [0, V)."""
+    cuts = [0] + list(bounds) + [V]
+    return [(a, b - a) for a, b in zip(cuts[:-1], cuts[1:])]
+
+
+def test_one_shard_is_the_unsharded_loss_bit_for_bit():
+    H, W, y = _rand(81, 9, 6, 33)
+    mask = np.ones(9, np.uint8)
+    mask[4] = 0
+    p = oracle.ce_shard_fwd(H, W, y, 0, 33)
+    c = oracle.ce_shard_combine(p[None], mask=mask, z_weight=0.1)
+    f = oracle.ce_fwd(H, W, y, mask=mask, z_weight=0.1)
+    assert np.array_equal(c["lse"], f["lse"]) and np.array_equal(c["ce"], f["ce"])
+    assert (c["total"], c["ce_mean"], c["z_mean"]) == (f["total"], f["ce_mean"], f["z_mean"])
+    dh, dw = oracle.ce_shard_bwd(H, W, y, 0, 33, f["lse"], mask=mask, z_weight=0.1, grad_scale=1.5)
+    dH, dW = oracle.ce_bwd(H, W, y, mask=mask, z_weight=0.1, grad_scale=1.5)
+    assert np.allclose(dh, dH, rtol=1e-13, atol=1e-18) and np.allclose(dw, dW, rtol=1e-13, atol=1e-18)
+
+
+@pytest.mark.parametrize("bounds", [(16,), (5, 6, 30), (1,), (32,)])
+def test_shards_recombine_into_the_unsharded_loss(bounds):
+    """Uneven shards, a one-row shard, the target in the first and last rows of
+    a shard: the combined loss and the summed (concatenated) gradients are the
+    unsharded ones, and the whole-row lse is torch's logsumexp."""
+    n, d, V = 12, 7, 33
+    H, W, y = _rand(82, n, d, V)
+    y[0], y[1], y[2] = 0, V - 1, bounds[0]
+    mask = np.ones(n, np.uint8)
+    mask[[3, 7]] = 0
+    wz, gs = 0.05, 0.7
+    parts = np.stack([oracle.ce_shard_fwd(H, W[v0:v0 + vs], y, v0, V) for v0, vs in _shards(V, bounds)])
+    assert np.all(parts[:, 2].sum(0) == 1.0)
+    c = oracle.ce_shard_combine(parts, mask=mask, z_weight=wz)
+    f = oracle.ce_fwd(H, W, y, mask=mask, z_weight=wz)
+    logits = torch.from_numpy(H).double() @ torch.from_numpy(W).double().T
+    assert np.allclose(c["lse"], torch.logsumexp(logits, 1).numpy(), rtol=1e-14, atol=0)
+    assert np.allclose(c["lse"], f["lse"], rtol=1e-14, atol=0)
+    assert np.allclose(c["ce"], f["ce"], rtol=1e-13, atol=1e-15)
+    assert np.allclose([c["total"], c["ce_mean"], c["z_mean"]], [f["total"], f["ce_mean"], f["z_mean"]],
+                       rtol=1e-13)
+    dH, dW = oracle.ce_bwd(H, W, y, mask=mask, z_weight=wz, grad_scale=gs)
+    dh = np.zeros_like(dH)
+    for v0, vs in _shards(V, bounds):
+        a, b = oracle.ce_shard_bwd(H, W[v0:v0 + vs], y, v0, V, c["lse"], mask=mask, z_weight=wz,
+                                   grad_scale=gs)
+        dh += a
+        assert np.allclose(b, dW[v0:v0 + vs], rtol=1e-12, atol=1e-16)
+    assert np.allclose(dh, dH, rtol=1e-12, atol=1e-16)
+
+
+def test_shard_contract_refusals():
+    H, W, y = _rand(83, 4, 3, 10)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.ce_shard_fwd(H, W[:6], y, 5, 10)            # rows 5..10 of a vocabulary of 10
+    assert e.value.status == 582
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.ce_shard_fwd(H, W[:6], np.array([0, 1, 2, 10]), 0, 10)
+    assert e.value.status == 586
+    # a target held by no shard (the shards leave rows 6..9 out) or by two
+    p = oracle.ce_shard_fwd(H, W[:6], y % 6, 0, 10)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.ce_shard_combine(np.stack([p, p]))
+    assert e.value.status == 586
+    y2 = y.copy()
+    y2[0] = 8
+    p2 = oracle.ce_shard_fwd(H, W[:6], y2, 0, 10)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.ce_shard_combine(p2[None])
+    assert e.value.status == 586
