@@ -87,8 +87,8 @@ extern "C" {
 typedef struct CUstream_st *lossk_stream_t;
 
 /* Status vocabulary 580-599 ("Loss functions and resident-context kernels",
- * section "Status codes").  589-591 are this library's own additions inside
- * the same range; 592-599 are unassigned. */
+ * section "Status codes").  589-592 are this library's own additions inside
+ * the same range; 593-599 are unassigned. */
 enum lossk_status {
     LOSSK_OK = 580,
     LOSSK_EMPTY_DIMENSION = 581,
@@ -129,7 +129,10 @@ enum lossk_kind {
     LOSSK_KIND_CE_FWD_BWD = 2,
     LOSSK_KIND_FROM_LOGITS = 3,
     LOSSK_KIND_DISTILL = 4,
-    LOSSK_KIND_CE_CHUNK_CHECK = 5
+    LOSSK_KIND_CE_CHUNK_CHECK = 5,
+    LOSSK_KIND_SHARD_FWD = 6,      /* lossk_ce_shard_fwd, sized at (n_tok, d_model, vocab_shard) */
+    LOSSK_KIND_SHARD_BWD = 7,      /* lossk_ce_shard_bwd, sized at (n_tok, d_model, vocab_shard) */
+    LOSSK_KIND_SHARD_COMBINE = 8   /* lossk_ce_shard_combine, sized at (n_tok, 1, 1) */
 };
 
 /* ---- contract: host arithmetic, no device ------------------------------- */
@@ -332,6 +335,82 @@ int32_t lossk_distill_from_logits(int64_t n_tok, int64_t vocab, int32_t dtype, c
  * error word: 580 (none), 590 (a bounded device wait timed out) or 589. */
 int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
 
+/* ---- vocabulary-parallel cross-entropy ---------------------------------------
+ * The weight's vocabulary rows split into contiguous shards, one per rank
+ * ("Fuse distillation + z-loss ...", "Changes": its tests add a
+ * tensor-parallel distributed subtest; "Validation": the world_size=2
+ * tensor-parallel subtests).  Shard p holds rows [v0, v0 + vocab_shard) of a
+ * vocabulary of vocab_total.  A step runs, per rank:
+ *   1. lossk_ce_shard_fwd on the rank's shard -> partials float[3][n_tok];
+ *   2. an exchange the caller makes (an all-gather of the 3 n_tok floats of
+ *      every rank, in shard order, over NCCL or any other transport) ->
+ *      partials_all float[n_shards][3][n_tok];
+ *   3. lossk_ce_shard_combine -> lse, ce and the three scalars, exactly the
+ *      outputs of lossk_ce_fwd on the whole vocabulary (every rank gets them);
+ *   4. lossk_ce_shard_bwd with that lse -> the shard's d_weight rows and its
+ *      share of d_hidden; the caller's all-reduce (sum) of the shares over the
+ *      ranks gives d_hidden.
+ * Partials of one shard, per token t:
+ *   partials[0][t] = log sum_{v in shard} exp(s_tv)  (the shard's lse)
+ *   partials[1][t] = s_{t,y_t} if the shard holds y_t, else 0
+ *   partials[2][t] = 1 if the shard holds y_t, else 0
+ * The shard's partials depend on the shard alone (its lse comes from the
+ * same CTA-pair statistics pass as lossk_ce_fwd, on the shard's rows).
+ * Targets are global ids: each must lie in [0, vocab_total) (586).
+ * Shape checks: the fused calls' checks at (n_tok, d_model, vocab_shard);
+ * vocab_total < 1: 581, > 2^24: 583; v0 < 0 or v0 + vocab_shard >
+ * vocab_total: 582. */
+int32_t lossk_ce_shard_fwd(int64_t n_tok, int64_t d_model, int64_t vocab_shard, int64_t v0, int64_t vocab_total,
+                           int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight_shard,
+                           int64_t weight_len, const int64_t *targets, int64_t targets_len, float *partials,
+                           int64_t partials_len, void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
+/* Combines the gathered partials float[n_shards][3][n_tok] (device) into
+ * lse_out, ce_out (or NULL) and scalars_out {total, ce_mean, z_mean}, as
+ * lossk_ce_fwd defines them: lse = M + log sum_p exp(lse_p - M) over the
+ * shards, ce = lse - the target logit of the one shard whose flag is set.  A
+ * token whose flags do not sum to 1 (no shard, or two, held its target: the
+ * shards do not tile the vocabulary) gives 586 before any output is written.
+ * Synchronises `stream` once, after that check. */
+int32_t lossk_ce_shard_combine(int64_t n_tok, int64_t n_shards, const float *partials_all, int64_t partials_len,
+                               const uint8_t *loss_mask, double z_weight, float *lse_out, float *ce_out,
+                               double *scalars_out, void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
+/* The shard's backward, given the whole row's lse (from
+ * lossk_ce_shard_combine): grad_logits restricted to the shard's columns,
+ * a_t((1 + 2 z_weight lse_t) softmax - onehot) with a_t = grad_scale m_t /
+ * N_valid, folded into
+ *   d_hidden_part  float[n_tok][d_model] = sum over the shard's columns of G W
+ *                  (NULL to skip; summed over the shards it is d_hidden)
+ *   d_weight_shard float[vocab_shard][d_model] = G^T H for the shard's rows
+ *                  (NULL to skip)
+ * Both are overwritten. */
+int32_t lossk_ce_shard_bwd(int64_t n_tok, int64_t d_model, int64_t vocab_shard, int64_t v0, int64_t vocab_total,
+                           int32_t dtype, const void *hidden, int64_t hidden_len, const void *weight_shard,
+                           int64_t weight_len, const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask,
+                           double z_weight, double grad_scale, const float *lse, int64_t lse_len,
+                           float *d_hidden_part, float *d_weight_shard, void *workspace, int64_t workspace_bytes,
+                           lossk_stream_t stream);
+
+/* Self-test of the failure detection every tensor-core kernel carries: each
+ * device-side wait gives up after a time limit, records a timeout in the
+ * workspace's error word and lets its kernel unwind (copies drained, tensor
+ * memory freed, every thread exits), so a stalled pipeline surfaces as 590
+ * instead of a hung GPU.  This call runs that mechanism on purpose in one
+ * small block with the kernels' roles: a producer arrives on n_arrive of
+ * n_stages (1..8) pipeline barriers and a consumer waits on each of them in
+ * turn with a limit of limit_ns (1e3..1e9 ns, else 585).  With n_arrive <
+ * n_stages the consumer's wait on stage n_arrive runs out after limit_ns.
+ * Writes the number of stages the consumer saw complete to the host int
+ * *stages_seen (may be NULL).  Synchronises `stream`.  Returns 590 when the
+ * wait ran out (the error word stays set, as after a real timeout:
+ * lossk_device_status reports and clears it, and until then every call on
+ * this workspace returns 590), else 580.  Stage counts out of range, or a
+ * workspace of fewer than 256 bytes or NULL: 582; a workspace not 256-byte
+ * aligned: 591; limit_ns out of range: 585. */
+int32_t lossk_selftest_wait(int32_t n_stages, int32_t n_arrive, int64_t limit_ns, int32_t *stages_seen,
+                            void *workspace, int64_t workspace_bytes, lossk_stream_t stream);
+
 /* lossk_ce_from_logits without a workspace, for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point.
  *
@@ -348,14 +427,23 @@ int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stre
  * Limits and rules:
  *  - n_tok <= 16384 (the array holds 256 + 3*8*16384 bytes, about 384 KB,
  *    held by every GPU that loads the library until the process exits);
- *    larger n_tok returns 583.
+ *    larger n_tok returns 583.  Every other check, its order and its status
+ *    code are those of lossk_ce_from_logits (the two share them), 590
+ *    included.
  *  - The first call on each device looks up the array's device address with
  *    that device current (cudaGetSymbolAddress) and caches it; make that
- *    first call before any stream capture on that device.
+ *    first call before any stream capture on that device.  The cached
+ *    address is that of the device's primary context: after a
+ *    cudaDeviceReset of a device, do not call this entry point on it again
+ *    in the same process.
+ *  - Like lossk_ce_from_logits, each call synchronises `stream` once, after
+ *    its validation kernel, to read back the target-range flag.
  *  - All calls share the one array, which keeps the previous call's
  *    contents; each call clears the header before use.  Calls that overlap
  *    on the GPU (two streams, or two host threads on one device) race on it
- *    and must be serialised by the caller. */
+ *    and must be serialised by the caller.
+ *  - Its kernels are counted and traced like every other launch
+ *    (lossk_launch_count, lossk_profile_read). */
 int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype, const void *logits,
                                     int64_t logits_len, const int64_t *targets, int64_t targets_len,
                                     const uint8_t *loss_mask, double z_weight, double grad_scale,
@@ -371,7 +459,7 @@ int32_t lossk_ce_from_logits_static(int64_t n_tok, int64_t vocab, int32_t dtype,
  * events, adds their durations per kind into total_ms[kind] and
  * launches[kind] (host arrays of `cap` entries), and clears them if `reset`.
  * Returns the number of kinds written, or -1 on a CUDA error. */
-#define LOSSK_N_KERNELS 20
+#define LOSSK_N_KERNELS 23
 const char *lossk_kernel_name(int32_t kind);
 int64_t lossk_launch_count(void);
 int32_t lossk_profile_enable(int32_t on);

@@ -83,6 +83,55 @@ cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t
 }
 
 // ---------------------------------------------------------------------------
+// Failure-detection self-test: the tensor-core kernels' role structure in
+// miniature.  Thread 0 of warp 0 (the producer) arrives on the first n_arrive
+// of n_stages single-arrival barriers; lane 0 of warp 1 (the consumer, also
+// the tensor-memory owner's warp) waits on every stage with the same bounded
+// wait the real kernels use, here with a limit of limit_ns.  When the
+// producer skipped a stage, that wait runs out, sets ERR_TIMEOUT in the error
+// word and returns false, and the block unwinds the way the real kernels do:
+// every thread reaches the final barrier and the tensor memory is freed.
+// seen[0] = the number of stages the consumer saw complete.
+__global__ void __launch_bounds__(64) wait_selftest_kernel(int n_stages, int n_arrive, uint64_t limit_ns,
+                                                           int *err, int *seen)
+{
+    __shared__ uint64_t full[8];
+    __shared__ uint32_t slot;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 8; ++s) mbar_init(&full[s], 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(&slot, 32);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = slot;
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < n_arrive && s < n_stages; ++s) mbar_arrive(&full[s]);
+    } else if (warp == 1 && lane == 0) {
+        int k = 0;
+        for (; k < n_stages; ++k)
+            if (!mbar_wait(&full[k], 0, err, limit_ns)) break;
+        seen[0] = k;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
+    }
+}
+
+cudaError_t launch_wait_selftest(int n_stages, int n_arrive, uint64_t limit_ns, int *err, int *seen,
+                                 cudaStream_t st)
+{
+    wait_selftest_kernel<<<1, 64, 0, st>>>(n_stages, n_arrive, limit_ns, err, seen);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Merging the per-tile partials of each token.  A block covers 32 tokens
 // (threadIdx.x, so every load of one tile's partials is a 128-byte line) and
 // splits the tiles into MG contiguous groups (threadIdx.y).  Pass 1 takes the
@@ -98,6 +147,9 @@ __device__ __forceinline__ void tile_range(int64_t n_ct, int g, int64_t &c0, int
     c1 = n_ct * (g + 1) / MG;
 }
 
+// PRECISE (the fp32 inputs path, tolerance 1e-6 relative): the rescale
+// factors are exp2 in double instead of ex2.approx.
+template <bool PRECISE>
 __global__ void __launch_bounds__(32 * MG) merge_ce_kernel(
     const float *__restrict__ part, const float *__restrict__ tgt, const uint8_t *__restrict__ mask,
     int64_t n, int64_t n_ct, int64_t n_pad, double wz, float *__restrict__ lse_out,
@@ -122,7 +174,9 @@ __global__ void __launch_bounds__(32 * MG) merge_ce_kernel(
     double Z = 0.0;
     if (live)
         for (int64_t c = c0; c < c1; ++c)
-            Z += static_cast<double>(zz[c * n_pad + t] * ex2_approx(m2[c * n_pad + t] - M));
+            Z += PRECISE ? static_cast<double>(zz[c * n_pad + t]) *
+                               exp2(static_cast<double>(m2[c * n_pad + t]) - static_cast<double>(M))
+                         : static_cast<double>(zz[c * n_pad + t] * ex2_approx(m2[c * n_pad + t] - M));
     ssum[g][tx] = Z;
     __syncthreads();
     if (g != 0 || !live) return;
@@ -142,11 +196,15 @@ __global__ void __launch_bounds__(32 * MG) merge_ce_kernel(
 cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
                             const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
                             double wz, float *lse_out, float *ce_out, double *tokacc,
-                            cudaStream_t st)
+                            cudaStream_t st, bool precise)
 {
     (void)targets;
-    merge_ce_kernel<<<static_cast<unsigned>((n + 31) / 32), dim3(32, MG), 0, st>>>(
-        part, tgt, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
+    if (precise)
+        merge_ce_kernel<true><<<static_cast<unsigned>((n + 31) / 32), dim3(32, MG), 0, st>>>(
+            part, tgt, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
+    else
+        merge_ce_kernel<false><<<static_cast<unsigned>((n + 31) / 32), dim3(32, MG), 0, st>>>(
+            part, tgt, mask, n, n_ct, n_pad, wz, lse_out, ce_out, tokacc);
     return cudaGetLastError();
 }
 
@@ -431,9 +489,12 @@ cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const 
 }
 
 // ---------------------------------------------------------------------------
+// P.w holds the target's column in the weight rows the passes see: y - v0
+// when that lies in [0, n_rows) (a vocabulary shard starting at row v0), else
+// -1, which matches no column (the one-hot term then belongs to another shard).
 __global__ void tokp_ce_kernel(const float *__restrict__ lse, const int64_t *__restrict__ targets,
                                const uint8_t *__restrict__ mask, int64_t n, int64_t n_pad,
-                               double alpha, double wz, float4 *__restrict__ tokp)
+                               double alpha, double wz, int64_t v0, int64_t n_rows, float4 *__restrict__ tokp)
 {
     const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (t >= n_pad) return;
@@ -443,16 +504,18 @@ __global__ void tokp_ce_kernel(const float *__restrict__ lse, const int64_t *__r
     }
     const double l = lse[t];
     const double at = (mask ? (mask[t] != 0) : true) ? alpha : 0.0;
+    const int64_t col = targets[t] - v0;
     tokp[t] = make_float4(static_cast<float>(l * LOG2E), static_cast<float>(at * (1.0 + 2.0 * wz * l)),
-                          static_cast<float>(at), __int_as_float(static_cast<int>(targets[t])));
+                          static_cast<float>(at),
+                          __int_as_float(col >= 0 && col < n_rows ? static_cast<int>(col) : -1));
 }
 
 cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,
                            int64_t n, int64_t n_pad, double alpha, double wz, float4 *tokp,
-                           cudaStream_t st)
+                           cudaStream_t st, int64_t v0, int64_t n_rows)
 {
-    tokp_ce_kernel<<<static_cast<int>((n_pad + 127) / 128), 128, 0, st>>>(lse, targets, mask, n,
-                                                                          n_pad, alpha, wz, tokp);
+    tokp_ce_kernel<<<static_cast<int>((n_pad + 127) / 128), 128, 0, st>>>(lse, targets, mask, n, n_pad, alpha,
+                                                                          wz, v0, n_rows, tokp);
     return cudaGetLastError();
 }
 
@@ -742,6 +805,139 @@ __device__ __forceinline__ float to_f(h16_t x) { return f16_to_f(x.bits); }
 __device__ __forceinline__ void from_f(float v, float &o) { o = v; }
 __device__ __forceinline__ void from_f(float v, uint16_t &o) { o = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
 __device__ __forceinline__ void from_f(float v, h16_t &o) { o.bits = static_cast<uint16_t>(pack_f16x2(v, 0.f) & 0xFFFFu); }
+
+// ---------------------------------------------------------------------------
+// Vocabulary-parallel cross-entropy ("Fuse distillation + z-loss ...",
+// "Changes": the tensor-parallel subtest).  A shard holds weight rows
+// [v0, v0 + n_rows) of the vocabulary.  shard_tgt: per token (one warp), the
+// target logit when the shard holds the target, else 0, and that 1/0 flag,
+// written into the shard's partials (rows 1 and 2 of [3][n]; row 0 is its
+// log-sum-exp, from the statistics pass and merge_ce).  The dot product runs
+// in fp32, lanes strided over k, then a fixed xor tree.
+template <typename T>
+__global__ void __launch_bounds__(256) shard_tgt_kernel(const T *__restrict__ H, const T *__restrict__ Ws,
+                                                        const int64_t *__restrict__ targets, int64_t n, int64_t d,
+                                                        int64_t v0, int64_t n_rows, float *__restrict__ tgt,
+                                                        float *__restrict__ flag)
+{
+    const int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= n) return;
+    const int64_t col = targets[t] - v0;
+    const bool in = col >= 0 && col < n_rows;
+    float acc = 0.f, err = 0.f;
+    if (in) {
+        // compensated (Dot2, as in the fp32 statistics pass): the rounding
+        // residuals of every product and sum are added on the side
+        const T *h = H + t * d, *w = Ws + col * d;
+        for (int64_t k = lane; k < d; k += 32) {
+            const float a = to_f(h[k]), b = to_f(w[k]);
+            const float p = __fmul_rn(a, b), pe = __fmaf_rn(a, b, -p);
+            const float u = __fadd_rn(acc, p), z = __fsub_rn(u, acc);
+            err = __fadd_rn(err, __fadd_rn(pe, __fadd_rn(__fsub_rn(acc, __fsub_rn(u, z)), __fsub_rn(p, z))));
+            acc = u;
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float q = __shfl_xor_sync(0xffffffffu, acc, o), qe = __shfl_xor_sync(0xffffffffu, err, o);
+            const float u = __fadd_rn(acc, q), z = __fsub_rn(u, acc);
+            err = __fadd_rn(__fadd_rn(err, qe), __fadd_rn(__fsub_rn(acc, __fsub_rn(u, z)), __fsub_rn(q, z)));
+            acc = u;
+        }
+        acc = __fadd_rn(acc, err);
+    }
+    if (lane == 0) {
+        tgt[t] = in ? acc : 0.f;
+        flag[t] = in ? 1.f : 0.f;
+    }
+}
+
+cudaError_t launch_shard_tgt(int dtype, const void *H, const void *Ws, const int64_t *targets, int64_t n,
+                             int64_t d, int64_t v0, int64_t n_rows, float *tgt, float *flag, cudaStream_t st)
+{
+    const unsigned grid = static_cast<unsigned>((n + 7) / 8);
+    if (dtype == 2)
+        shard_tgt_kernel<h16_t><<<grid, 256, 0, st>>>(static_cast<const h16_t *>(H), static_cast<const h16_t *>(Ws),
+                                                      targets, n, d, v0, n_rows, tgt, flag);
+    else if (dtype == 1)
+        shard_tgt_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(H),
+                                                         static_cast<const uint16_t *>(Ws), targets, n, d, v0,
+                                                         n_rows, tgt, flag);
+    else
+        shard_tgt_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(H), static_cast<const float *>(Ws),
+                                                      targets, n, d, v0, n_rows, tgt, flag);
+    return cudaGetLastError();
+}
+
+// The gathered partials [P][3][n] of every shard: count the tokens whose
+// target is held by no shard or by more than one (flags not summing to 1)
+// into bad_targets, and the counted tokens into n_valid, as the validation
+// does (the header's counters are cleared first).
+__global__ void shard_check_kernel(const float *__restrict__ parts, int64_t P, int64_t n,
+                                   const uint8_t *__restrict__ mask, WsHeader *hdr)
+{
+    int bad = 0, valid = 0;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < n;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float f = 0.f;
+        for (int64_t p = 0; p < P; ++p) f += parts[(p * 3 + 2) * n + t];
+        bad += f == 1.f ? 0 : 1;
+        valid += mask ? (mask[t] != 0) : 1;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        valid += __shfl_xor_sync(0xffffffffu, valid, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (bad) atomicAdd(&hdr->bad_targets, bad);
+        if (valid) atomicAdd(&hdr->n_valid, valid);
+    }
+}
+
+cudaError_t launch_shard_check(const float *parts, int64_t P, int64_t n, const uint8_t *mask, WsHeader *hdr,
+                               cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(&hdr->bad_targets, 0, 3 * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    int grid = static_cast<int>((n + 255) / 256);
+    if (grid > 1024) grid = 1024;
+    shard_check_kernel<<<grid, 256, 0, st>>>(parts, P, n, mask, hdr);
+    return cudaGetLastError();
+}
+
+// One thread per token: lse = M + log sum_p exp(lse_p - M) over the shards in
+// shard order (double), the target logit from the shard whose flag is set,
+// then ce, z and the token-mean terms as in merge_ce.
+__global__ void shard_combine_kernel(const float *__restrict__ parts, int64_t P, int64_t n, int64_t n_pad,
+                                     const uint8_t *__restrict__ mask, double wz, float *__restrict__ lse_out,
+                                     float *__restrict__ ce_out, double *__restrict__ tokacc)
+{
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= n) return;
+    double M = parts[t], tgt = 0.0;
+    for (int64_t p = 1; p < P; ++p) M = fmax(M, static_cast<double>(parts[p * 3 * n + t]));
+    double Z = 0.0;
+    for (int64_t p = 0; p < P; ++p) {
+        Z += exp(static_cast<double>(parts[p * 3 * n + t]) - M);
+        if (parts[(p * 3 + 2) * n + t] != 0.f) tgt = parts[(p * 3 + 1) * n + t];
+    }
+    const double lse = M + log(Z);
+    const bool on = mask ? (mask[t] != 0) : true;
+    const double ce = on ? lse - tgt : 0.0;
+    const double z2 = on ? lse * lse : 0.0;
+    lse_out[t] = static_cast<float>(lse);
+    if (ce_out) ce_out[t] = static_cast<float>(ce);
+    tokacc[t] = ce + wz * z2;
+    tokacc[n_pad + t] = ce;
+    tokacc[2 * n_pad + t] = z2;
+}
+
+cudaError_t launch_shard_combine(const float *parts, int64_t P, int64_t n, int64_t n_pad, const uint8_t *mask,
+                                 double wz, float *lse_out, float *ce_out, double *tokacc, cudaStream_t st)
+{
+    shard_combine_kernel<<<static_cast<unsigned>((n + 127) / 128), 128, 0, st>>>(parts, P, n, n_pad, mask, wz,
+                                                                                lse_out, ce_out, tokacc);
+    return cudaGetLastError();
+}
 
 // 16-byte loads of a logit row.  `keep` leaves the line in L2 (the row is read
 // again for its gradient); otherwise the load streams past L2.
@@ -1420,10 +1616,18 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
     }
     const int xrow0 = xt * FP_BM;
     float acc[4][4] = {};
+    // STATS: the logits are compensated dot products (Dot2 of Ogita, Rump and
+    // Oishi, "Accurate sum and dot product", SIAM J. Sci. Comput. 26 (2005)):
+    // each product is split exactly into its rounded value and the FMA
+    // residual, each sum into its rounded value and the TwoSum residual, and
+    // the residuals are added on the side, so a logit carries about one
+    // rounding of its own size however much its terms cancel.  The plain
+    // intrinsics keep the compiler from contracting the split operations.
+    constexpr bool DOT2 = MODE == TC_STATS;
 
     for (int yt = yt_begin; yt < yt_end; ++yt) {
         const int ycol0 = yt * FP_BN;
-        float s[4][4] = {};
+        float s[4][4] = {}, sc[4][4] = {};
         for (int k0 = 0; k0 < d; k0 += FP_BK) {
             for (int e = threadIdx.x; e < FP_BM * FP_BK; e += 256) {
                 const int rr = e / FP_BK, kk = e % FP_BK;
@@ -1443,9 +1647,27 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int jx = 0; jx < 4; ++jx) s[i][jx] = fmaf(xa[i], yb[jx], s[i][jx]);
+                    for (int jx = 0; jx < 4; ++jx) {
+                        if (DOT2) {
+                            const float p = __fmul_rn(xa[i], yb[jx]);
+                            const float pe = __fmaf_rn(xa[i], yb[jx], -p);       // a b = p + pe exactly
+                            const float t = __fadd_rn(s[i][jx], p);
+                            const float z = __fsub_rn(t, s[i][jx]);
+                            const float se = __fadd_rn(__fsub_rn(s[i][jx], __fsub_rn(t, z)), __fsub_rn(p, z));
+                            s[i][jx] = t;                                      // s + p = t + se exactly
+                            sc[i][jx] = __fadd_rn(sc[i][jx], __fadd_rn(pe, se));
+                        } else {
+                            s[i][jx] = fmaf(xa[i], yb[jx], s[i][jx]);
+                        }
+                    }
             }
             __syncthreads();
+        }
+        if (DOT2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jx = 0; jx < 4; ++jx) s[i][jx] = __fadd_rn(s[i][jx], sc[i][jx]);
         }
         if (MODE == TC_STATS) {
             // rows ty*4+i, columns tx*4+jx; a row's 64 columns live in 16
@@ -1475,7 +1697,8 @@ __global__ void __launch_bounds__(256) fp_kernel(const float *__restrict__ X,
                             part[o] = m;
                             part[part_plane + o] = z;
                         }
-                        const int64_t rel = targets[t] - ycol0 - tx * 4;
+                        // no targets (a vocabulary shard): the target logit comes from elsewhere
+                        const int64_t rel = targets ? targets[t] - ycol0 - tx * 4 : -1;
 #pragma unroll
                         for (int jx = 0; jx < 4; ++jx)
                             if (rel == jx) tgt[t] = s[i][jx];

@@ -177,35 +177,6 @@ Profiler &profiler()
     return p;
 }
 
-// Brackets one kernel launch: counts it and, when profiling is on, records an
-// event pair around it on its stream.
-class Launch {
-  public:
-    Launch(int kind, cudaStream_t st) : kind_(kind), st_(st)
-    {
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        Profiler &p = profiler();
-        if (!p.on.load(std::memory_order_relaxed)) return;
-        std::lock_guard<std::mutex> g(p.mu);
-        a_ = p.get();
-        b_ = p.get();
-        if (a_ && b_ && cudaEventRecord(a_, st_) == cudaSuccess) active_ = true;
-    }
-    ~Launch()
-    {
-        if (!active_) return;
-        Profiler &p = profiler();
-        std::lock_guard<std::mutex> g(p.mu);
-        if (cudaEventRecord(b_, st_) == cudaSuccess) p.pending.push_back({kind_, a_, b_});
-    }
-
-  private:
-    int kind_;
-    cudaStream_t st_;
-    cudaEvent_t a_ = nullptr, b_ = nullptr;
-    bool active_ = false;
-};
-
 struct Hdr {
     int err, bad, n_valid;
 };
@@ -389,7 +360,7 @@ int32_t run_ce_fwd(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, 
     {
         Launch k(KK_MERGE_CE, st);
         e = launch_merge_ce(w.part(), w.tgt(), targets, mask, n, L.n_ct, L.n_pad, wz, lse_out,
-                            ce_out, w.tokacc(), st);
+                            ce_out, w.tokacc(), st, !is16(dtype));
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     Launch k(KK_REDUCE, st);
@@ -580,6 +551,66 @@ bool scalars_ok(double wz, double gs) { return is_finite(wz) && wz >= 0.0 && is_
 // ===========================================================================
 namespace lossk {
 
+Launch::Launch(int kind, cudaStream_t st) : kind_(kind), st_(st)
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    Profiler &p = profiler();
+    if (!p.on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> g(p.mu);
+    a_ = p.get();
+    b_ = p.get();
+    if (a_ && b_ && cudaEventRecord(a_, st_) == cudaSuccess) active_ = true;
+}
+
+Launch::~Launch()
+{
+    if (!active_) return;
+    Profiler &p = profiler();
+    std::lock_guard<std::mutex> g(p.mu);
+    if (cudaEventRecord(b_, st_) == cudaSuccess) p.pending.push_back({kind_, a_, b_});
+}
+
+int32_t check_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, int64_t logits_len,
+                          const int64_t *targets, int64_t targets_len, const float *lse_out,
+                          const double *scalars_out, const void *grad, int64_t grad_len, double wz,
+                          double gs, const void *workspace, int64_t workspace_bytes, int64_t max_tok,
+                          WsLayout *L)
+{
+    const bool ws = max_tok <= 0;
+    if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
+    if (n > (ws ? MAX_DIM : max_tok) || V > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
+    if (!dtype_ok(dtype)) return LOSSK_LENGTH_MISMATCH;
+    if (ws && !ws_layout(LOSSK_KIND_FROM_LOGITS, n, 1, V, dtype, L)) return LOSSK_DIMENSION_TOO_LARGE;
+    if (!logits || !targets || !lse_out || !scalars_out || (ws && !workspace)) return LOSSK_LENGTH_MISMATCH;
+    if (logits_len < n * V || targets_len < n || (grad && grad_len < n * V) ||
+        (ws && workspace_bytes < static_cast<int64_t>(L->total)))
+        return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(logits) || (grad && !aligned16(grad)) ||
+        (ws && (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return LOSSK_UNALIGNED;
+    if (!scalars_ok(wz, gs)) return LOSSK_NON_FINITE_SCALAR;
+    return LOSSK_OK;
+}
+
+int32_t run_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, const int64_t *targets,
+                        const uint8_t *mask, double wz, double gs, float *lse_out, float *ce_out,
+                        double *scalars_out, void *grad, WsHeader *hdr, double *tokacc, int64_t n_pad,
+                        cudaStream_t st)
+{
+    Hdr h;
+    int32_t s = validate(targets, mask, n, V, hdr, st, &h);
+    if (s != LOSSK_OK) return s;
+    const double alpha = h.n_valid > 0 ? gs / h.n_valid : 0.0;
+    {
+        Launch k(KK_FROM_LOGITS, st);
+        if (launch_from_logits(dtype, logits, targets, mask, n, V, wz, alpha, lse_out, ce_out, tokacc, grad,
+                               st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    Launch k(KK_REDUCE, st);
+    return status_of(launch_reduce(tokacc, n, n_pad, hdr, wz, scalars_out, st));
+}
+
 BwdGeom bwd_geometry(int64_t d, bool distill)
 {
     // Per loop supertile and d-group a cluster of c CTAs spends nk + 4c stages
@@ -634,6 +665,10 @@ int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
 
 bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L)
 {
+    // the vocabulary-shard calls use the unsharded layouts at the shard's size
+    if (kind == LOSSK_KIND_SHARD_FWD) kind = LOSSK_KIND_CE_FWD;
+    else if (kind == LOSSK_KIND_SHARD_BWD) kind = LOSSK_KIND_CE_BWD;
+    else if (kind == LOSSK_KIND_SHARD_COMBINE) kind = LOSSK_KIND_FROM_LOGITS;
     if (lossk_dims_check(n, d, V) != LOSSK_OK) return false;
     *L = WsLayout();
     const bool tc = is16(dtype);
@@ -855,7 +890,7 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
         const double a_tok = f16 ? (alpha != 0.0 ? 1.0 : 0.0) : alpha;
         {
             Launch k(KK_TOKP, st);
-            if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, a_tok, wz, w.tokp(), st) != cudaSuccess)
+            if (launch_tokp_ce(lse_io, targets, mask, n, w.L.n_pad, a_tok, wz, w.tokp(), st, 0, V) != cudaSuccess)
                 return LOSSK_DEVICE_ERROR;
         }
         s = run_acc(w, n, d, V, dtype, H, W, nullptr, false, 0, 1.0, dH, dW, st, acc, f16 ? alpha : 1.0);
@@ -915,33 +950,14 @@ int32_t lossk_ce_from_logits(int64_t n, int64_t V, int32_t dtype, const void *lo
                              double *scalars_out, void *grad_logits, int64_t grad_len, void *workspace,
                              int64_t workspace_bytes, lossk_stream_t stream)
 {
-    if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
-    if (n > MAX_DIM || V > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
-    if (!dtype_ok(dtype)) return LOSSK_LENGTH_MISMATCH;
     Ws w;
-    if (!ws_layout(LOSSK_KIND_FROM_LOGITS, n, 1, V, dtype, &w.L)) return LOSSK_DIMENSION_TOO_LARGE;
-    if (!logits || !targets || !lse_out || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
-    if (logits_len < n * V || targets_len < n || (grad_logits && grad_len < n * V) ||
-        workspace_bytes < static_cast<int64_t>(w.L.total))
-        return LOSSK_LENGTH_MISMATCH;
-    if (!aligned16(logits) || (grad_logits && !aligned16(grad_logits)) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return LOSSK_UNALIGNED;
-    if (!scalars_ok(z_weight, grad_scale)) return LOSSK_NON_FINITE_SCALAR;
-    w.base = static_cast<uint8_t *>(workspace);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    Hdr h;
-    int32_t s = validate(targets, loss_mask, n, V, w.hdr(), st, &h);
+    int32_t s = check_from_logits(n, V, dtype, logits, logits_len, targets, targets_len, lse_out, scalars_out,
+                                  grad_logits, grad_len, z_weight, grad_scale, workspace, workspace_bytes, 0, &w.L);
     if (s != LOSSK_OK) return s;
-    const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
-    {
-        Launch k(KK_FROM_LOGITS, st);
-        if (launch_from_logits(dtype, logits, targets, loss_mask, n, V, z_weight, alpha, lse_out,
-                               ce_out, w.tokacc(), grad_logits, st) != cudaSuccess)
-            return LOSSK_DEVICE_ERROR;
-    }
-    Launch k(KK_REDUCE, st);
-    return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st));
+    w.base = static_cast<uint8_t *>(workspace);
+    return run_from_logits(n, V, dtype, logits, targets, loss_mask, z_weight, grad_scale, lse_out, ce_out,
+                           scalars_out, grad_logits, w.hdr(), w.tokacc(), w.L.n_pad,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t lossk_distill_fwd_bwd_ex(int64_t n, int64_t d, int64_t V, int64_t chunk, int32_t dtype,
@@ -1144,13 +1160,180 @@ int32_t lossk_device_status(void *workspace, int64_t workspace_bytes, lossk_stre
     return LOSSK_DEVICE_TIMEOUT;
 }
 
+// ---- vocabulary-parallel cross-entropy ---------------------------------------
+// Checks shared by the two shard calls, in the documented order: the fused
+// calls' checks at the shard's size (581, 583, 584, 582, 591), the whole
+// vocabulary's size (581, 583) and the shard's place in it (582).
+static int32_t check_shard(int64_t n, int64_t d, int64_t Vs, int64_t v0, int64_t V_total, int32_t dtype,
+                           const void *H, int64_t hl, const void *Ws, int64_t wl, const int64_t *targets,
+                           int64_t tl, const void *workspace, int64_t wsb, int kind, WsLayout *L)
+{
+    if (V_total < 1) return LOSSK_EMPTY_DIMENSION;
+    int32_t s = check_fused(n, d, Vs, 0, false, dtype, H, hl, Ws, wl, workspace, wsb, kind, L);
+    if (s != LOSSK_OK) return s;
+    if (V_total > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
+    if (v0 < 0 || v0 > V_total - Vs) return LOSSK_LENGTH_MISMATCH;
+    if (!targets || tl < n) return LOSSK_LENGTH_MISMATCH;
+    return LOSSK_OK;
+}
+
+int32_t lossk_ce_shard_fwd(int64_t n, int64_t d, int64_t Vs, int64_t v0, int64_t V_total, int32_t dtype,
+                           const void *hidden, int64_t hidden_len, const void *weight_shard, int64_t weight_len,
+                           const int64_t *targets, int64_t targets_len, float *partials, int64_t partials_len,
+                           void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    Ws w;
+    int32_t s = check_shard(n, d, Vs, v0, V_total, dtype, hidden, hidden_len, weight_shard, weight_len, targets,
+                            targets_len, workspace, workspace_bytes, LOSSK_KIND_SHARD_FWD, &w.L);
+    if (s != LOSSK_OK) return s;
+    if (!partials || partials_len < 3 * n) return LOSSK_LENGTH_MISMATCH;
+    if (!aligned16(partials)) return LOSSK_UNALIGNED;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    s = validate(targets, nullptr, n, V_total, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    const WsLayout &L = w.L;
+    {
+        Launch k(KK_SHARD_TGT, st);
+        if (launch_shard_tgt(dtype, hidden, weight_shard, targets, n, d, v0, Vs, partials + n, partials + 2 * n,
+                             st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    cudaError_t e;
+    if (is16(dtype)) {
+        TcArgs a;
+        std::memset(&a, 0, sizeof(a));
+        if (!make_map(&a.map_x, hidden, d, n, 64, TC_BM) || !make_map(&a.map_y, weight_shard, d, Vs, 64, 128))
+            return LOSSK_DEVICE_ERROR;
+        a.n_x = static_cast<int>(n);
+        a.n_y = static_cast<int>(Vs);
+        a.d = static_cast<int>(d);
+        a.n_tok = static_cast<int>(n);
+        a.vocab = static_cast<int>(Vs);
+        a.n_xt = static_cast<int>(cdiv(n, TC_BM));
+        a.n_yt = static_cast<int>(L.n_ct);
+        a.n_items = static_cast<int>(cdiv(a.n_xt, 2)) * a.n_yt;
+        a.part = w.part();
+        a.part_stride = L.n_pad;
+        a.part_plane = L.n_ct * L.n_pad;
+        a.err = &w.hdr()->err;
+        const int pairs = a.n_items < sm_count() / 2 ? a.n_items : sm_count() / 2;
+        Launch k(KK_TC_STATS, st);
+        e = launch_fwd2(a, false, dtype == LOSSK_F16, 2 * pairs, st);
+    } else {
+        Launch k(KK_FP_STATS, st);
+        e = launch_fp(TC_STATS, false, hidden, weight_shard, nullptr, static_cast<int>(n), static_cast<int>(Vs),
+                      static_cast<int>(d), static_cast<int>(n), static_cast<int>(Vs), 1, 0, 1.f, nullptr, nullptr,
+                      nullptr, w.part(), w.tgt(), L.n_pad, L.n_ct * L.n_pad, nullptr, 0, st);
+    }
+    if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
+    // the shard's log-sum-exp per token into row 0 (merge_ce's other outputs
+    // land in the workspace)
+    Launch k(KK_MERGE_CE, st);
+    return status_of(launch_merge_ce(w.part(), partials + n, nullptr, nullptr, n, L.n_ct, L.n_pad, 0.0, partials,
+                                     nullptr, w.tokacc(), st, !is16(dtype)));
+}
+
+int32_t lossk_ce_shard_combine(int64_t n, int64_t n_shards, const float *partials_all, int64_t partials_len,
+                               const uint8_t *loss_mask, double z_weight, float *lse_out, float *ce_out,
+                               double *scalars_out, void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    if (n < 1 || n_shards < 1) return LOSSK_EMPTY_DIMENSION;
+    if (n > MAX_DIM || n_shards > MAX_DIM) return LOSSK_DIMENSION_TOO_LARGE;
+    Ws w;
+    if (!ws_layout(LOSSK_KIND_SHARD_COMBINE, n, 1, 1, LOSSK_F32, &w.L)) return LOSSK_DIMENSION_TOO_LARGE;
+    if (!partials_all || !lse_out || !scalars_out || !workspace) return LOSSK_LENGTH_MISMATCH;
+    if (partials_len < 3 * n * n_shards || workspace_bytes < static_cast<int64_t>(w.L.total))
+        return LOSSK_LENGTH_MISMATCH;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LOSSK_UNALIGNED;
+    if (!scalars_ok(z_weight, 1.0)) return LOSSK_NON_FINITE_SCALAR;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    {
+        Launch k(KK_VALIDATE, st);
+        if (launch_shard_check(partials_all, n_shards, n, loss_mask, w.hdr(), st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    int buf[4] = {0, 0, 0, 0};
+    if (!read_header(w.hdr(), st, buf)) return LOSSK_DEVICE_ERROR;
+    if (buf[0]) return LOSSK_DEVICE_TIMEOUT;
+    if (buf[1]) return LOSSK_TARGET_OUT_OF_RANGE;
+    {
+        Launch k(KK_SHARD_COMBINE, st);
+        if (launch_shard_combine(partials_all, n_shards, n, w.L.n_pad, loss_mask, z_weight, lse_out, ce_out,
+                                 w.tokacc(), st) != cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    Launch k(KK_REDUCE, st);
+    return status_of(launch_reduce(w.tokacc(), n, w.L.n_pad, w.hdr(), z_weight, scalars_out, st));
+}
+
+int32_t lossk_ce_shard_bwd(int64_t n, int64_t d, int64_t Vs, int64_t v0, int64_t V_total, int32_t dtype,
+                           const void *hidden, int64_t hidden_len, const void *weight_shard, int64_t weight_len,
+                           const int64_t *targets, int64_t targets_len, const uint8_t *loss_mask, double z_weight,
+                           double grad_scale, const float *lse, int64_t lse_len, float *d_hidden_part,
+                           float *d_weight_shard, void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    Ws w;
+    int32_t s = check_shard(n, d, Vs, v0, V_total, dtype, hidden, hidden_len, weight_shard, weight_len, targets,
+                            targets_len, workspace, workspace_bytes, LOSSK_KIND_SHARD_BWD, &w.L);
+    if (s != LOSSK_OK) return s;
+    if (!lse || lse_len < n) return LOSSK_LENGTH_MISMATCH;
+    if ((d_hidden_part && !aligned16(d_hidden_part)) || (d_weight_shard && !aligned16(d_weight_shard)))
+        return LOSSK_UNALIGNED;
+    if (!scalars_ok(z_weight, grad_scale)) return LOSSK_NON_FINITE_SCALAR;
+    w.base = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Hdr h;
+    s = validate(targets, loss_mask, n, V_total, w.hdr(), st, &h);
+    if (s != LOSSK_OK) return s;
+    if (!d_hidden_part && !d_weight_shard) return LOSSK_OK;
+    const double alpha = h.n_valid > 0 ? grad_scale / h.n_valid : 0.0;
+    const bool f16 = dtype == LOSSK_F16;
+    const double a_tok = f16 ? (alpha != 0.0 ? 1.0 : 0.0) : alpha;
+    {
+        Launch k(KK_TOKP, st);
+        if (launch_tokp_ce(lse, targets, loss_mask, n, w.L.n_pad, a_tok, z_weight, w.tokp(), st, v0, Vs) !=
+            cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    return run_acc(w, n, d, Vs, dtype, hidden, weight_shard, nullptr, false, 0, 1.0, d_hidden_part, d_weight_shard,
+                   st, false, f16 ? alpha : 1.0);
+}
+
+int32_t lossk_selftest_wait(int32_t n_stages, int32_t n_arrive, int64_t limit_ns, int32_t *stages_seen,
+                            void *workspace, int64_t workspace_bytes, lossk_stream_t stream)
+{
+    if (n_stages < 1 || n_stages > 8 || n_arrive < 0 || n_arrive > n_stages) return LOSSK_LENGTH_MISMATCH;
+    if (!workspace || workspace_bytes < 256) return LOSSK_LENGTH_MISMATCH;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LOSSK_UNALIGNED;
+    if (limit_ns < 1000 || limit_ns > 1000000000) return LOSSK_NON_FINITE_SCALAR;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader *hdr = static_cast<WsHeader *>(workspace);
+    int *seen = &hdr->pad[0];
+    {
+        Launch k(KK_SELFTEST, st);
+        if (launch_wait_selftest(n_stages, n_arrive, static_cast<uint64_t>(limit_ns), &hdr->err, seen, st) !=
+            cudaSuccess)
+            return LOSSK_DEVICE_ERROR;
+    }
+    int h[5] = {0, 0, 0, 0, 0};
+    if (cudaMemcpyAsync(h, hdr, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return LOSSK_DEVICE_ERROR;
+    if (stages_seen) *stages_seen = h[4];
+    return h[0] ? LOSSK_DEVICE_TIMEOUT : LOSSK_OK;
+}
+
 const char *lossk_kernel_name(int32_t kind)
 {
     static const char *names[KK_N] = {"validate",     "tc_stats",      "tc_rows",     "tc_cols",
                                       "fp_stats",     "fp_rows",       "fp_cols",     "merge_ce",
                                       "merge_distill", "reduce",        "tokp_ce",     "sum_splits",
                                       "from_logits",  "tc_fused",      "tgt_logit",   "merge_fused",
-                                      "combine_dh",   "teacher_stats", "distill_logits", "readback"};
+                                      "combine_dh",   "teacher_stats", "distill_logits", "readback",
+                                      "wait_selftest", "shard_tgt",    "shard_combine"};
     return (kind >= 0 && kind < KK_N) ? names[kind] : "unknown_kernel";
 }
 

@@ -174,12 +174,54 @@ enum KernelKind : int {
     KK_TEACHER_STATS,
     KK_DISTILL_LOGITS,
     KK_READBACK,
+    KK_SELFTEST,
+    KK_SHARD_TGT,
+    KK_SHARD_COMBINE,
     KK_N
 };
+
+// Brackets one kernel launch: counts it (lossk_launch_count) and, when
+// profiling is on, records a CUDA event pair around it on its stream
+// (lossk_profile_read).  Every launch of the library goes through one.
+class Launch {
+  public:
+    Launch(int kind, cudaStream_t st);
+    ~Launch();
+    Launch(const Launch &) = delete;
+    Launch &operator=(const Launch &) = delete;
+
+  private:
+    int kind_;
+    cudaStream_t st_;
+    cudaEvent_t a_ = nullptr, b_ = nullptr;
+    bool active_ = false;
+};
+
+// ---- cross-entropy from given logits, shared by its two entry points --------
+// The argument checks of lossk_ce_from_logits in the documented order (581,
+// 583, 582, 591, 585).  With `workspace` the scratch is the caller's workspace
+// (null, size and alignment checked, its layout returned in *L); without it
+// the scratch is a built-in array holding at most max_tok tokens (more: 583).
+int32_t check_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, int64_t logits_len,
+                          const int64_t *targets, int64_t targets_len, const float *lse_out,
+                          const double *scalars_out, const void *grad, int64_t grad_len, double wz,
+                          double gs, const void *workspace, int64_t workspace_bytes, int64_t max_tok,
+                          WsLayout *L);
+// Validation (586, or 590 for a device error word already set in hdr), the
+// row stream and the token mean, on scratch hdr (256 bytes) + tokacc
+// (3 x n_pad doubles).  Synchronises `st` once, after the validation.
+int32_t run_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits, const int64_t *targets,
+                        const uint8_t *mask, double wz, double gs, float *lse_out, float *ce_out,
+                        double *scalars_out, void *grad, WsHeader *hdr, double *tokacc, int64_t n_pad,
+                        cudaStream_t st);
 
 // ---- launchers (all enqueue on `st`) -----------------------------------------
 cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t n, int64_t V,
                             WsHeader *hdr, cudaStream_t st);
+// One block: a producer arrives on n_arrive of n_stages barriers, a consumer
+// waits on each with the bounded wait (limit_ns); an expired wait sets *err.
+cudaError_t launch_wait_selftest(int n_stages, int n_arrive, uint64_t limit_ns, int *err, int *seen,
+                                 cudaStream_t st);
 // Persistent clusters: at most as many as fit at once, walking `n_units` units.
 // f16: fp16 operands (BWD_ROWS / BWD_COLS only); otherwise bf16.
 cudaError_t launch_bwd(int mode, bool distill, bool f16, const BwdArgs &a, int n_units, cudaStream_t st);
@@ -190,10 +232,11 @@ cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, cons
                       float *part,
                       float *tgt, int64_t part_stride, int64_t part_plane, float *out,
                       int64_t out_split_stride, cudaStream_t st, bool accumulate = false);
+// precise: exact exp2 rescales (the fp32 inputs path); else ex2.approx.
 cudaError_t launch_merge_ce(const float *part, const float *tgt, const int64_t *targets,
                             const uint8_t *mask, int64_t n, int64_t n_ct, int64_t n_pad,
                             double wz, float *lse_out, float *ce_out, double *tokacc,
-                            cudaStream_t st);
+                            cudaStream_t st, bool precise);
 cudaError_t launch_merge_distill(const float *part, const double2 *tstat, const uint8_t *mask, int64_t n,
                                  int64_t n_ct, int64_t n_pad, int direction, double wz, float *lse_out,
                                  float *per_token, double *tokacc, float4 *tokp, double alpha,
@@ -205,9 +248,20 @@ cudaError_t launch_teacher_stats(int dtype, const void *teach, int64_t n, int64_
 // sum: the three scalars are sums over the tokens instead of means over N_valid.
 cudaError_t launch_reduce(const double *tokacc, int64_t n, int64_t n_pad, const WsHeader *hdr,
                           double wz, double *scalars_out, cudaStream_t st, bool sum = false);
+// v0, n_rows: the weight rows the passes see are vocabulary rows [v0, v0 + n_rows)
+// (a shard); a target outside them gets no one-hot term.
 cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8_t *mask,
                            int64_t n, int64_t n_pad, double alpha, double wz, float4 *tokp,
-                           cudaStream_t st);
+                           cudaStream_t st, int64_t v0, int64_t n_rows);
+// Vocabulary shards: the target logit and its flag per token; the gathered
+// partials' check (bad_targets, n_valid into the header) and their combination
+// into lse, ce and the token-mean terms.
+cudaError_t launch_shard_tgt(int dtype, const void *H, const void *Ws, const int64_t *targets, int64_t n,
+                             int64_t d, int64_t v0, int64_t n_rows, float *tgt, float *flag, cudaStream_t st);
+cudaError_t launch_shard_check(const float *parts, int64_t P, int64_t n, const uint8_t *mask, WsHeader *hdr,
+                               cudaStream_t st);
+cudaError_t launch_shard_combine(const float *parts, int64_t P, int64_t n, int64_t n_pad, const uint8_t *mask,
+                                 double wz, float *lse_out, float *ce_out, double *tokacc, cudaStream_t st);
 // accumulate: out += the sum instead of out = the sum.
 cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, float *out,
                               cudaStream_t st, bool accumulate = false);

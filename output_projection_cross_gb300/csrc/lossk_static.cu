@@ -15,7 +15,6 @@
 #include "../../include/lossk.h"
 #include "lossk_internal.h"
 
-#include <cmath>
 #include <mutex>
 
 namespace {
@@ -31,7 +30,10 @@ static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_B
 
 // The array's device address, looked up once per device with that device
 // current.  In host code the symbol itself is only a host-side stand-in, never
-// a device address, so it is never passed to a kernel directly.
+// a device address, so it is never passed to a kernel directly.  The address
+// belongs to the device's primary context: a cudaDeviceReset on that device
+// makes the cached value stale, so this library must not be called on a
+// device after it has been reset.
 constexpr int MAX_DEVICES = 64;
 void *g_scratch_addr[MAX_DEVICES] = {nullptr};
 std::mutex g_scratch_mu;
@@ -63,39 +65,23 @@ extern "C" int32_t lossk_ce_from_logits_static(int64_t n, int64_t V, int32_t dty
                                                double *scalars_out, void *grad_logits,
                                                int64_t grad_len, lossk_stream_t stream)
 {
-    if (n < 1 || V < 1) return LOSSK_EMPTY_DIMENSION;
-    if (n > STATIC_MAX_TOKENS || V > (int64_t(1) << 24)) return LOSSK_DIMENSION_TOO_LARGE;
-    if (dtype != LOSSK_F32 && dtype != LOSSK_BF16 && dtype != LOSSK_F16) return LOSSK_LENGTH_MISMATCH;
-    if (!logits || !targets || !lse_out || !scalars_out) return LOSSK_LENGTH_MISMATCH;
-    if (logits_len < n * V || targets_len < n || (grad_logits && grad_len < n * V))
-        return LOSSK_LENGTH_MISMATCH;
-    if ((reinterpret_cast<uintptr_t>(logits) & 15u) ||
-        (grad_logits && (reinterpret_cast<uintptr_t>(grad_logits) & 15u)))
-        return LOSSK_UNALIGNED;
-    if (!std::isfinite(z_weight) || z_weight < 0.0 || !std::isfinite(grad_scale))
-        return LOSSK_NON_FINITE_SCALAR;
-
+    // The same checks, in the same order, as the workspace entry point; only
+    // the token limit differs (the array's size, 583 beyond it).
+    int32_t s = check_from_logits(n, V, dtype, logits, logits_len, targets, targets_len, lse_out, scalars_out,
+                                  grad_logits, grad_len, z_weight, grad_scale, nullptr, 0, STATIC_MAX_TOKENS,
+                                  nullptr);
+    if (s != LOSSK_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return LOSSK_DEVICE_ERROR;
     WsHeader *hdr = static_cast<WsHeader *>(scratch);
     double *tokacc = reinterpret_cast<double *>(static_cast<unsigned char *>(scratch) + 256);
     const int64_t n_pad = (n + TC_BM - 1) / TC_BM * TC_BM;
-
     // The array keeps the previous call's contents: clear the header (error
     // word and counters).  The per-token terms are fully rewritten before use.
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    if (launch_validate(targets, loss_mask, n, V, hdr, st) != cudaSuccess) return LOSSK_DEVICE_ERROR;
-    int h[3] = {0, 0, 0};
-    if (cudaMemcpyAsync(h, hdr, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return LOSSK_DEVICE_ERROR;
-    if (h[1]) return LOSSK_TARGET_OUT_OF_RANGE;
-    const double alpha = h[2] > 0 ? grad_scale / h[2] : 0.0;
-    if (launch_from_logits(dtype, logits, targets, loss_mask, n, V, z_weight, alpha, lse_out, ce_out,
-                           tokacc, grad_logits, st) != cudaSuccess)
-        return LOSSK_DEVICE_ERROR;
-    if (launch_reduce(tokacc, n, n_pad, hdr, z_weight, scalars_out, st) != cudaSuccess)
-        return LOSSK_DEVICE_ERROR;
-    return LOSSK_OK;
+    // The same launches as the workspace entry point (validation read-back,
+    // row stream, token mean), each counted and traced like every other launch.
+    return run_from_logits(n, V, dtype, logits, targets, loss_mask, z_weight, grad_scale, lse_out, ce_out,
+                           scalars_out, grad_logits, hdr, tokacc, n_pad, st);
 }

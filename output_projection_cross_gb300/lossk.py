@@ -20,6 +20,7 @@ _i64, _i32, _dbl, _vp, _u32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, c
 
 F32, BF16, F16 = 0, 1, 2
 KIND_CE_FWD, KIND_CE_BWD, KIND_CE_FWD_BWD, KIND_FROM_LOGITS, KIND_DISTILL, KIND_CE_CHUNK_CHECK = 0, 1, 2, 3, 4, 5
+KIND_SHARD_FWD, KIND_SHARD_BWD, KIND_SHARD_COMBINE = 6, 7, 8
 ACCUMULATE_GRADS, REDUCE_SUM = 1, 2
 DIRECTIONS = {"ce": 0, "fkl": 1, "rkl": 2}
 OK = 580
@@ -70,6 +71,12 @@ def _load():
         "lossk_device_status": (_i32, [_vp, _i64, _vp]),
         "lossk_ce_from_logits_static": (_i32, [_i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _dbl,
                                                _dbl, _vp, _vp, _vp, _vp, _i64, _vp]),
+        "lossk_ce_shard_fwd": (_i32, [_i64, _i64, _i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _i64,
+                                      _vp, _i64, _vp, _i64, _vp]),
+        "lossk_ce_shard_combine": (_i32, [_i64, _i64, _vp, _i64, _vp, _dbl, _vp, _vp, _vp, _vp, _i64, _vp]),
+        "lossk_ce_shard_bwd": (_i32, [_i64, _i64, _i64, _i64, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _i64,
+                                      _vp, _dbl, _dbl, _vp, _i64, _vp, _vp, _vp, _i64, _vp]),
+        "lossk_selftest_wait": (_i32, [_i32, _i32, _i64, ctypes.POINTER(_i32), _vp, _i64, _vp]),
         "lossk_kernel_name": (ctypes.c_char_p, [_i32]),
         "lossk_launch_count": (_i64, []),
         "lossk_profile_enable": (_i32, [_i32]),
@@ -89,8 +96,9 @@ EXPORTED = ("lossk_status_name", "lossk_dims_check", "lossk_chunk_check", "lossk
             "lossk_ce_from_logits", "lossk_distill_fwd_bwd", "lossk_device_status",
             "lossk_ce_fwd_bwd_ex", "lossk_distill_fwd_bwd_ex", "lossk_ce_chunk_invariance",
             "lossk_distill_from_logits",
-            "lossk_ce_from_logits_static", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
-N_KERNELS = 20
+            "lossk_ce_from_logits_static", "lossk_selftest_wait", "lossk_ce_shard_fwd",
+            "lossk_ce_shard_combine", "lossk_ce_shard_bwd", "lossk_kernel_name", "lossk_launch_count", "lossk_profile_enable", "lossk_profile_read")
+N_KERNELS = 23
 
 
 class LosskError(RuntimeError):
@@ -413,6 +421,76 @@ def lossk_distill_from_logits(logits, teacher_logits, direction="fkl", temperatu
 
 def lossk_device_status(ws, stream=None) -> int:
     return lib.lossk_device_status(_ptr(ws), ws.numel(), _stream(stream))
+
+
+# ---- vocabulary-parallel cross-entropy ---------------------------------------------
+
+def lossk_ce_shard_fwd(hidden, weight_shard, targets, v0, vocab_total, partials=None, ws=None, stream=None):
+    """Partials float[3][n] of the shard holding vocabulary rows [v0, v0 + rows)."""
+    for t, nm in ((hidden, "hidden"), (weight_shard, "weight_shard"), (targets, "targets")):
+        _contig(t, nm)
+    n, d = hidden.shape
+    Vs = weight_shard.shape[0]
+    dt = _dtype_code(hidden)
+    dev = hidden.device
+    partials = partials if partials is not None else torch.empty(3, n, dtype=torch.float32, device=dev)
+    ws = _ws(ws, KIND_SHARD_FWD, n, d, Vs, dt, dev)
+    st = lib.lossk_ce_shard_fwd(n, d, Vs, v0, vocab_total, dt, _ptr(hidden), _len(hidden), _ptr(weight_shard),
+                                _len(weight_shard), _ptr(targets), _len(targets), _ptr(partials), _len(partials),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "lossk_ce_shard_fwd")
+    return partials
+
+
+def lossk_ce_shard_combine(partials_all, loss_mask=None, z_weight=0.0, lse_out=None, ce_out=None,
+                           scalars_out=None, ws=None, stream=None):
+    """lse, ce and the scalars from every shard's partials [P][3][n], in shard order."""
+    _contig(partials_all, "partials_all")
+    _contig(loss_mask, "loss_mask")
+    P, three, n = partials_all.shape
+    assert three == 3
+    dev = partials_all.device
+    lse_out = lse_out if lse_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    ce_out = ce_out if ce_out is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    scalars_out = scalars_out if scalars_out is not None else torch.empty(3, dtype=torch.float64, device=dev)
+    ws = _ws(ws, KIND_SHARD_COMBINE, n, 1, 1, F32, dev)
+    st = lib.lossk_ce_shard_combine(n, P, _ptr(partials_all), _len(partials_all), _ptr(loss_mask), z_weight,
+                                    _ptr(lse_out), _ptr(ce_out), _ptr(scalars_out), _ptr(ws), ws.numel(),
+                                    _stream(stream))
+    _check(st, "lossk_ce_shard_combine")
+    return {"lse": lse_out, "ce": ce_out, "scalars": scalars_out}
+
+
+def lossk_ce_shard_bwd(hidden, weight_shard, targets, v0, vocab_total, lse, loss_mask=None, z_weight=0.0,
+                       grad_scale=1.0, d_hidden=None, d_weight=None, want_d_hidden=True, want_d_weight=True,
+                       ws=None, stream=None):
+    """The shard's share of d_hidden and its d_weight rows, given the whole row's lse."""
+    for t, nm in ((hidden, "hidden"), (weight_shard, "weight_shard"), (targets, "targets"), (lse, "lse"),
+                  (loss_mask, "loss_mask")):
+        _contig(t, nm)
+    n, d = hidden.shape
+    Vs = weight_shard.shape[0]
+    dt = _dtype_code(hidden)
+    dev = hidden.device
+    if want_d_hidden and d_hidden is None:
+        d_hidden = torch.empty(n, d, dtype=torch.float32, device=dev)
+    if want_d_weight and d_weight is None:
+        d_weight = torch.empty(Vs, d, dtype=torch.float32, device=dev)
+    ws = _ws(ws, KIND_SHARD_BWD, n, d, Vs, dt, dev)
+    st = lib.lossk_ce_shard_bwd(n, d, Vs, v0, vocab_total, dt, _ptr(hidden), _len(hidden), _ptr(weight_shard),
+                                _len(weight_shard), _ptr(targets), _len(targets), _ptr(loss_mask), z_weight,
+                                grad_scale, _ptr(lse), _len(lse), _ptr(d_hidden), _ptr(d_weight), _ptr(ws),
+                                ws.numel(), _stream(stream))
+    _check(st, "lossk_ce_shard_bwd")
+    return {"d_hidden": d_hidden, "d_weight": d_weight}
+
+
+def lossk_selftest_wait(n_stages: int, n_arrive: int, limit_ns: int, ws, stream=None):
+    """Run the bounded-wait self-test; returns (status, stages the consumer saw)."""
+    seen = _i32(0)
+    st = lib.lossk_selftest_wait(n_stages, n_arrive, limit_ns, ctypes.byref(seen), _ptr(ws), ws.numel(),
+                                 _stream(stream))
+    return st, seen.value
 
 
 # ---- tracing ------------------------------------------------------------------
