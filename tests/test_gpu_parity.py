@@ -274,6 +274,16 @@ def test_config_512x1024x32000_full(L):
     assert rel_l2(_np(out["d_weight"]), dW) <= BF16_GRAD
 
 
+_QWEN3_ORACLE = {}
+
+
+def _qwen3_oracle(x, w):
+    """The oracle's full forward at the Qwen3 head shape (bf16 inputs), computed once."""
+    if not _QWEN3_ORACLE:
+        _QWEN3_ORACLE.update(oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], chunk=w.chunk))
+    return _QWEN3_ORACLE
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_qwen3_head_full_size_sampled(L, dtype):
     """n=2048, d=1024, V=151936, Zipf targets: the launch configuration the bench
@@ -291,7 +301,8 @@ def test_qwen3_head_full_size_sampled(L, dtype):
     close_loss(_np(out["ce"])[rows], s["lse"] - s["tgt"], BF16_LOSS)
     assert rel_l2(_np(out["d_hidden"])[rows], s["dH"]) <= BF16_GRAD
     # d_weight rows: the oracle needs every token's lse
-    full = oracle.ce_fwd(x["hidden"], x["weight"], x["targets"], chunk=w.chunk)
+    full = _qwen3_oracle(x, w) if dtype == "bf16" else oracle.ce_fwd(x["hidden"], x["weight"], x["targets"],
+                                                                      chunk=w.chunk)
     close_loss(_np(out["lse"]), full["lse"], BF16_LOSS)
     close_loss(_np(out["scalars"])[:1], [full["total"]], BF16_LOSS)
     vrows = np.concatenate([np.unique(x["targets"])[:24],
@@ -1009,3 +1020,109 @@ def test_distill_from_logits(L, dtype, direction, V):
     else:
         ideal = 2 * r["grad"]
     assert rel_l2(_np(gl), ideal) <= _tol(dtype)[1]
+
+
+# ---------------------------------------------------------------------------
+# Vocabulary-parallel cross-entropy.  The shards run one after another on one
+# GPU; their partials are stacked in shard order, as the all-gather between
+# ranks stacks them, then combined; d_hidden is the sum of the shards' shares
+# (what the all-reduce between ranks computes) and d_weight their concatenation.
+def _shard_step(L, H, W, y, cuts, mask, wz, gs):
+    V = W.shape[0]
+    edges = [0] + list(cuts) + [V]
+    parts, shards = [], []
+    for v0, v1 in zip(edges[:-1], edges[1:]):
+        Ws = W[v0:v1].contiguous()
+        parts.append(L.lossk_ce_shard_fwd(H, Ws, y, v0, V))
+        shards.append((v0, Ws))
+    pa = torch.stack(parts)
+    c = L.lossk_ce_shard_combine(pa, loss_mask=mask, z_weight=wz)
+    dh, dws = None, []
+    for v0, Ws in shards:
+        g = L.lossk_ce_shard_bwd(H, Ws, y, v0, V, c["lse"], loss_mask=mask, z_weight=wz, grad_scale=gs)
+        dh = g["d_hidden"] if dh is None else dh + g["d_hidden"]
+        dws.append(g["d_weight"])
+    torch.cuda.synchronize()
+    return pa, c, dh, torch.cat(dws)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "f16"])
+@pytest.mark.parametrize("shape,cuts", [((300, 200, 1000), (8, 504)),       # a one-tile shard
+                                        ((130, 1024, 5000), (2500,)),      # two halves
+                                        ((257, 520, 2000), (1000, 1001, 1999))])   # one-row shards
+def test_vocab_shards_small(L, dtype, shape, cuts):
+    n, d, V = shape
+    x = _redraw(_inputs("ce_512x1024x32000", seed=41, n_tok=n, d_model=d, vocab=V), dtype, 4, n, d, V)
+    yn = x["targets"].copy()
+    yn[:3] = [0, V - 1, cuts[0]]                # the vocabulary's ends and a shard's first row
+    mask = li.mask(8, n, 0.1)
+    wz, gs = 1e-3, 1.5
+    H, W, y, m = _dev(x["hidden"], dtype), _dev(x["weight"], dtype), _dev(yn, ""), _dev(mask, "")
+    pa, c, dh, dw = _shard_step(L, H, W, y, cuts, m, wz, gs)
+    lt, gt = _tol(dtype)
+    # each shard's partials against the oracle's
+    edges = [0] + list(cuts) + [V]
+    for p, (v0, v1) in enumerate(zip(edges[:-1], edges[1:])):
+        r = oracle.ce_shard_fwd(x["hidden"], x["weight"][v0:v1], yn, v0, V)
+        close_loss(_np(pa[p, 0]), r[0], lt)
+        close_loss(_np(pa[p, 1]), r[1], lt)
+        assert np.array_equal(_np(pa[p, 2]), r[2])
+    ref = oracle.ce_fwd(x["hidden"], x["weight"], yn, mask=mask, z_weight=wz)
+    dH, dW = oracle.ce_bwd(x["hidden"], x["weight"], yn, mask=mask, z_weight=wz, grad_scale=gs)
+    close_loss(_np(c["lse"]), ref["lse"], lt)
+    close_loss(_np(c["ce"]), ref["ce"], lt)
+    close_loss(_np(c["scalars"]), [ref["total"], ref["ce_mean"], ref["z_mean"]], lt)
+    assert rel_l2(_np(dh), dH) <= gt
+    assert rel_l2(_np(dw), dW) <= gt
+
+
+def test_vocab_shards_qwen3_head_split_in_two(L):
+    """The Qwen3 head shape (n 2048, d 1024, V 151936, bf16) split into two
+    shards of 75968 rows: every token's lse and the scalars against the
+    oracle's full forward, sampled tokens' loss and d_hidden rows, and
+    sampled d_weight rows from both shards."""
+    w = li.WORKLOADS["qwen3_0p6b_head"]
+    x = _inputs(w)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    half = w.vocab // 2
+    pa, c, dh, dw = _shard_step(L, H, W, y, (half,), None, 0.0, 1.0)
+    assert np.array_equal(_np(pa[:, 2]).sum(0), np.ones(w.n_tok))
+    full = _qwen3_oracle(x, w)
+    close_loss(_np(c["lse"]), full["lse"], BF16_LOSS)
+    close_loss(_np(c["ce"]), full["ce"], BF16_LOSS)
+    close_loss(_np(c["scalars"]), [full["total"], full["ce_mean"], full["z_mean"]], BF16_LOSS)
+    rows = np.sort(np.random.default_rng(17).choice(w.n_tok, 24, replace=False))
+    s = oracle.ce_token_rows(x["hidden"], x["weight"], x["targets"], rows)
+    assert rel_l2(_np(dh)[rows], s["dH"]) <= BF16_GRAD
+    vrows = np.concatenate([np.unique(x["targets"])[:12], [half - 1, half],
+                            np.random.default_rng(18).choice(w.vocab, 12, replace=False)])
+    dwr = oracle.ce_dweight_rows(x["hidden"], x["weight"], x["targets"], full["lse"], vrows)
+    assert rel_l2(_np(dw)[vrows], dwr) <= BF16_GRAD
+
+
+def test_vocab_shard_combine_refuses_shards_that_do_not_tile(L):
+    """A target held by no shard (a shard left out) or by two (a shard given
+    twice): 586, and no output written."""
+    n, d, V = 64, 64, 512
+    x = _inputs("ce_512x1024x32000", seed=43, n_tok=n, d_model=d, vocab=V)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    y[0], y[1] = 0, V - 1
+    p0 = L.lossk_ce_shard_fwd(H, W[:256].contiguous(), y, 0, V)
+    p1 = L.lossk_ce_shard_fwd(H, W[256:].contiguous(), y, 256, V)
+    lse = torch.full((n,), -7.0, device="cuda")
+    for bad in (torch.stack([p0]), torch.stack([p0, p1, p1])):
+        with pytest.raises(L.LosskError) as e:
+            L.lossk_ce_shard_combine(bad, lse_out=lse)
+        assert e.value.status == 586
+    assert bool((lse == -7.0).all())
+    c = L.lossk_ce_shard_combine(torch.stack([p0, p1]), lse_out=lse)
+    torch.cuda.synchronize()
+    close_loss(_np(c["lse"]), oracle.ce_fwd(x["hidden"], x["weight"], _np(y).astype(np.int64))["lse"], BF16_LOSS)
+    # a shard outside the vocabulary, and a target outside it
+    with pytest.raises(L.LosskError) as e:
+        L.lossk_ce_shard_fwd(H, W[:256].contiguous(), y, 300, V)
+    assert e.value.status == 582
+    y[5] = V
+    with pytest.raises(L.LosskError) as e:
+        L.lossk_ce_shard_fwd(H, W[:256].contiguous(), y, 0, V)
+    assert e.value.status == 586
