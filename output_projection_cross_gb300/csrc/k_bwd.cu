@@ -1,22 +1,24 @@
 // k_bwd.cu -- the backward passes of the fused LM-head loss on tcgen05 (and
 // the training step's fused forward + d_hidden pass), with each recomputed
-// grad_logits tile handed between the CTAs of a thread-block cluster through a
-// small L2-resident ring.
+// grad_logits tile handed between the CTAs of a group through a small
+// L2-resident ring.
 //
 // d_hidden = G W and d_weight = G^T H need a [128 x d_model] fp32 accumulator
 // per fixed tile, wider than tensor memory (512 columns).  So the accumulator
-// is split into 256-column d-slices, one per CTA of a cluster of c CTAs.  A
+// is split into 256-column d-slices, one per CTA of a group of c CTAs (c
+// consecutive blocks of the grid; not a thread-block group, see below).  A
 // unit of work is one fixed tile (128 tokens for d_hidden, 128 vocabulary rows
 // for d_weight), one d-group and a range of loop supertiles of 256 columns
-// (vocabulary for d_hidden, tokens for d_weight).  Every CTA of the cluster
+// (vocabulary for d_hidden, tokens for d_weight).  Every CTA of the group
 // walks the same supertiles; supertile y's logits -- the whole d_model
-// contraction, one 128 x 256 MMA tile -- are computed once, by CTA y % c.
+// contraction, one 128 x 256 MMA tile -- are computed once, by CTA y % c of the
+// group.
 // Its epilogue turns them into grad_logits G in registers ("Fuse distillation
 // + z-loss ...", "What it does": prob_coeff * softmax - label_coeff * onehot,
 // with the z term folded into prob_coeff, or the distribution-family form),
 // stores the bf16 tile into one of that CTA's slots of a global ring that
 // stays in L2 (each warp stages 32 x 32 chunks in shared memory and stores them
-// with TMA), and signals every CTA of the cluster.  Every CTA then loads the
+// with TMA), and signals the group.  Every CTA then loads the
 // tile with TMA like any other operand and adds G times its d-slice of the
 // loop tensor into its accumulator:
 //   d_hidden: D[tok][slice] += G[tok][voc] . W[voc][slice]
@@ -34,16 +36,21 @@
 // The accumulate stage's B part (the d-slice's four 64-column blocks) comes in
 // one 3-D box when d_model % 64 == 0.
 //
-// Ring hand-over (per CTA, G_SLOTS slots of one supertile each): the writer
-// waits on its gfree[g] until every CTA of the cluster has loaded the slot's
-// previous tile (c remote arrivals, one per loader's MMA issuer once the TMA
-// completed), writes, waits for its TMA stores to complete, fences and arrives
-// on gready[writer][g] in every CTA (4 warp arrivals, cluster-scope releases:
-// they publish the tile); a loader's TMA
-// producer waits on gready before loading.  The MMA issuer's gfree arrival is
-// a CTA-scope release (it announces completed reads, and a cluster-scope
-// release would hold the issuer, and the tensor pipe, for about a thousand
-// clocks).
+// Ring hand-over (per CTA, G_SLOTS slots of one supertile each), through two
+// monotonic counters per slot in global memory (the workspace; zeroed before
+// each launch): the writer waits until the slot's free count shows that every
+// CTA of the group has loaded the slot's previous tile (one relaxed add per
+// loader's MMA issuer once the TMA load has landed: it announces completed
+// reads and never holds the issuer), writes, waits for its TMA stores to
+// complete, fences and adds to the slot's ready count (one release add per
+// epilogue warp: they publish the tile); a loader's TMA producer waits for the
+// ready count (acquire) before loading.
+//
+// Why groups and not clusters: a cluster of c CTAs must sit in one GPC, and
+// on a 152-SM GB300 only 36 clusters of 4 (144 SMs), 15 of 8 (120) or 7 of 16
+// (112) fit at once.  A group only needs its CTAs resident at the same time,
+// which the cooperative launch guarantees for the whole grid: groups of 4 or
+// 8 use all 152 SMs, groups of 16 use 144.
 //
 // BWD_FUSED is the d_hidden schedule run before any log-sum-exp is known: its
 // grad tile is the unnormalised G'[t][v] = 2^(s[t][v] log2e - r_t) with the
@@ -56,7 +63,7 @@
 // and d_hidden_t = a_t (1 + 2 w_z lse_t) D_t / Z_t - a_t W[y_t], which a later
 // kernel applies and checks.
 //
-// The clusters are persistent: each walks units u, u + #clusters, ... with
+// The groups are persistent: each walks units u, u + #groups, ... with
 // the TMA ring, the TMEM logit buffer and the ring slots' phases carried
 // across units.  Step i of the schedule issues round i's own logit tile and
 // the accumulates of round i-1 (possibly of the previous unit).
@@ -77,8 +84,8 @@ namespace {
 constexpr int B_NST = 4;                          // operand ring stages
 constexpr int B_STAGE = 49152;                    // 48 KB: an A part and a B part
 constexpr int B_APART = 16384;                    // 128 rows x 64 K (bf16, 128-byte swizzle)
-constexpr int B_MAXC = BWD_MAX_CL;                // CTAs per cluster at most
-constexpr int B_NBARS = 2 * B_NST + 4 + B_MAXC * G_SLOTS + G_SLOTS + 1 + 8;
+constexpr int B_MAXC = BWD_MAX_CL;                // CTAs per group at most
+constexpr int B_NBARS = 2 * B_NST + 4 + 1 + 8;
 // The distillation d_weight pass reads its teacher block through TMA: per
 // epilogue warp two 32-token x 32-vocabulary bf16 buffers (2 KB each).
 // The plain d_weight pass uses the same 16 KB (four 1024-byte-aligned 4 KB
@@ -122,7 +129,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs &a, int u)
     return w;
 }
 
-// Position in this cluster's schedule: unit u (the k-th of the cluster), round r
+// Position in this group's schedule: unit u (the k-th of the group), round r
 // of its nr rounds of c supertiles.
 struct BwdCursor {
     int u, k, r, nr;
@@ -178,18 +185,19 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint64_t *tempty = tfull + 1;          // epilogue done with the TMEM logit buffer (128 threads)
     uint64_t *accfull = tempty + 1;        // accumulator of a unit final
     uint64_t *accempty = accfull + 1;      // accumulator of a unit stored (128 threads)
-    uint64_t *gready = accempty + 1;       // [B_MAXC][G_SLOTS] a writer's tile is in its slot (4 warps)
-    uint64_t *gfree = gready + B_MAXC * G_SLOTS;   // [G_SLOTS] own slot loaded by every CTA (c)
-    uint64_t *drain = gfree + G_SLOTS;
+    uint64_t *drain = accempty + 1;
     uint64_t *tbar = drain + 1;            // [4 warps][2] teacher block landed (TTMA)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(tbar + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int *err = a.err;
     const int c = a.n_cl;
-    const int crank = static_cast<int>(cluster_ctarank());
-    const int cluster = blockIdx.x / c, n_clusters = gridDim.x / c;
-    const int cbase = blockIdx.x - crank;                  // first CTA of this cluster
+    const int crank = static_cast<int>(blockIdx.x) % c;    // this CTA's place in its group
+    const int group = blockIdx.x / c, n_groups = gridDim.x / c;   // the group and the group count
+    const int cbase = blockIdx.x - crank;                  // first CTA of this group
+    // per (CTA, slot): tiles published (4 per tile) and loads completed (c per tile)
+    unsigned *const gready = a.gsig;
+    unsigned *const gfree = a.gsig + G_MAX_CTAS * G_SLOTS;
     const int n_units = a.n_fixed * a.n_split * a.n_dg;
     auto cursor_set = [&](BwdCursor &cu, int u, int k) {
         cu.u = u;
@@ -202,9 +210,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
     };
     auto cursor_next = [&](BwdCursor &cu) {
-        if (++cu.r >= cu.nr) cursor_set(cu, cu.u + n_clusters, cu.k + 1);
+        if (++cu.r >= cu.nr) cursor_set(cu, cu.u + n_groups, cu.k + 1);
     };
-    // First row of slot g of cluster CTA `wr` in the global grad-tile array
+    // First row of slot g of group CTA `wr` in the global grad-tile array
     // (a slot holds two 128 x 128 sub-tiles).
     auto slot_row = [&](int wr, int g) { return ((cbase + wr) * G_SLOTS + g) * 2 * 128; };
 
@@ -217,8 +225,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         mbar_init(tempty, 128);
         mbar_init(accfull, 1);
         mbar_init(accempty, 128);
-        for (int i = 0; i < B_MAXC * G_SLOTS; ++i) mbar_init(&gready[i], 4);
-        for (int g = 0; g < G_SLOTS; ++g) mbar_init(&gfree[g], c);
         mbar_init(drain, 1);
         for (int i = 0; i < 8; ++i) mbar_init(&tbar[i], 1);
         fence_mbarrier_init();
@@ -226,7 +232,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     if (warp == 1) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
-    cluster_sync();            // every CTA's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tslot;
     constexpr uint32_t ACC_COL = 256;
@@ -253,14 +258,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             if (++st == B_NST) { st = 0; ph ^= 1; }
         };
         BwdCursor cur, prev;
-        cursor_set(cur, cluster, 0);
+        cursor_set(cur, group, 0);
         bool have_prev = false;
         while (ok && (cur.u < n_units || have_prev)) {
-            if (!ROWS && cur.u < n_units && cur.r == 0 && cur.u + n_clusters < n_units) {
-                // d_weight: the cluster's next unit has a new fixed tile (128 weight rows
+            if (!ROWS && cur.u < n_units && cur.r == 0 && cur.u + n_groups < n_units) {
+                // d_weight: the group's next unit has a new fixed tile (128 weight rows
                 // over the whole d_model, read from HBM for the first time); bring it into
                 // L2 now, the CTAs splitting its K steps
-                const int fixn = bwd_unit(a, cur.u + n_clusters).fixed * 128;
+                const int fixn = bwd_unit(a, cur.u + n_groups).fixed * 128;
                 for (int kb = crank; kb < nk; kb += c) tma_prefetch_2d(&a.map_fix, kb * TC_BK, fixn);
             }
             if (cur.u < n_units) {
@@ -284,7 +289,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                     const int wr = yy - y0;
                     const int cw = cnt_get(cnt, wr);
                     const int g = cw % G_SLOTS;
-                    if (!mbar_wait_cluster(&gready[wr * G_SLOTS + g], (cw / G_SLOTS) & 1, err)) { ok = false; break; }
+                    // the writer's (cw / G_SLOTS)-th tile in slot g is published: 4 warp adds per tile
+                    if (!gsig_wait(&gready[(cbase + wr) * G_SLOTS + g], 4u * static_cast<unsigned>(cw / G_SLOTS + 1),
+                                   err)) {
+                        ok = false;
+                        break;
+                    }
                     fence_proxy_async_global();
                     const int loop0 = (prev.w.yt_begin + yy) * BWD_BN;
                     const int grow = slot_row(wr, g);
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const uint64_t dBa = sdesc_sw128(ring0 + B_APART, 8192, 1024);    // accumulate B: MN-major
         constexpr uint64_t STEP = B_STAGE >> 4;
         BwdCursor cur, prev;
-        cursor_set(cur, cluster, 0);
+        cursor_set(cur, group, 0);
         bool have_prev = false;
         while (ok && (cur.u < n_units || have_prev)) {
             if (cur.u < n_units) {
@@ -370,9 +380,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
                         if (!mbar_wait(&full[st], ph, err)) { ok = false; break; }
                         tc_fence_after();
                         // all four quarters of the writer's tile have landed: its slot may be
-                        // refilled (a release of completed reads: CTA scope is enough, and the
-                        // issuer must not stall)
-                        if (sidx == 3) mbar_arrive_remote_cta(mapa_shared(smem_u32(&gfree[g]), wr));
+                        // refilled (completed reads, nothing to publish: a relaxed add, which
+                        // never holds the issuer)
+                        if (sidx == 3) gsig_add_relaxed(&gfree[(cbase + wr) * G_SLOTS + g], 1u);
                         const uint64_t off = st * STEP;
                         const uint64_t a = dA + off, b = dBa + off;
                         tc_mma_bf16(tmem + ACC_COL, a, b, ID_ACC, first_acc ? 0u : 1u);
@@ -463,8 +473,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int y = m * c + crank;
             const int loop0 = (w.yt_begin + y) * BWD_BN;
             const int g = m_all % G_SLOTS;
-            // the slot's previous tile has been loaded by every CTA of the cluster
-            bool ok = mbar_wait_cluster(&gfree[g], ((m_all / G_SLOTS) & 1) ^ 1, err);
+            // the slot's previous tile has been loaded by every CTA of the group (one
+            // lane polls; the warp's writes below follow its acquire)
+            bool ok = true;
+            if (lane == 0)
+                ok = gsig_wait(&gfree[blockIdx.x * G_SLOTS + g], static_cast<unsigned>(c * (m_all / G_SLOTS)), err);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ROWS && !pcache) {
                 // per-token parameters of this supertile's 256 token columns (each warp
                 // keeps its own copy, so no barrier spans warps that may unwind apart)
@@ -631,8 +645,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             fence_proxy_async_global();
             __threadfence();
             __syncwarp();
-            // one lane per CTA of the cluster: the cluster-scope releases run side by side
-            if (lane < c) mbar_arrive_remote(mapa_shared(smem_u32(&gready[crank * G_SLOTS + g]), lane));
+            // publish: one release add per warp (4 per tile)
+            if (lane == 0) gsig_add_release(&gready[blockIdx.x * G_SLOTS + g], 1u);
             ++m_all;
             return true;
         };
@@ -640,7 +654,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         // unit's accumulator is stored: its logits are ready earlier (the MMA
         // issues them before this unit's last accumulates), and the MMA can
         // then start the next logit tile while the store runs.
-        int u = cluster;
+        int u = group;
         BwdUnit w;
         float4 P = P0;
         double zsum = 0.0;
@@ -654,7 +668,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             const int n_own = n_own_of(w);
             for (int m = m0; m < n_own && ok; ++m) ok = tile(w, m, P, zsum);
             if (!ok) break;
-            const int u2 = u + n_clusters;
+            const int u2 = u + n_groups;
             BwdUnit w2;
             float4 P2 = P0;
             double zsum2 = 0.0;
@@ -770,8 +784,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         tc_fence_before();
     }
     __syncthreads();
-    // No CTA leaves while another may still arrive on its barriers.
-    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -784,52 +796,49 @@ static cudaError_t launch_bwd_one(const BwdArgs &a, int n_units, cudaStream_t st
 {
     auto k = bwd_kernel<MODE, DISTILL, F16>;
     constexpr int SMEM = bwd_smem<MODE, DISTILL>();
-    // The function attributes and the resident-cluster count are set up once
-    // per device and cluster size: the launch of the training step's first
-    // pass waits on the host after the validation read-back, so host work here
-    // is GPU idle time.
+    // The function attribute and the resident-block count are set up once per
+    // device: the launch of the training step's first pass waits on the host
+    // after the validation read-back, so host work here is GPU idle time.
     constexpr int MAX_DEV = 64;
-    static std::atomic<int> attr_done[MAX_DEV];
-    static std::atomic<int> resident[MAX_DEV][BWD_MAX_CL + 1];
+    static std::atomic<int> resident[MAX_DEV];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool cache = dev >= 0 && dev < MAX_DEV;
-    if (!cache || !attr_done[dev].load(std::memory_order_acquire)) {
+    int active = cache ? resident[dev].load(std::memory_order_acquire) : 0;
+    if (active < 1) {
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        // clusters of 9-16 CTAs are beyond the portable size
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        if (cache) attr_done[dev].store(1, std::memory_order_release);
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 192, SMEM) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaGetLastError();
+        active = per_sm * sms;
+        if (active < 1) return cudaErrorInvalidConfiguration;
+        if (cache) resident[dev].store(active, std::memory_order_release);
     }
+    // As many groups as are resident at once (and as the grad-tile ring has
+    // slots for), each walking several units; the results do not depend on
+    // the count, only the schedule does.  Every CTA of the grid must be
+    // resident at the same time (the groups' CTAs wait on each other): the
+    // launch is cooperative.
+    int groups = active / a.n_cl;
+    if (groups > n_units) groups = n_units;
+    if (groups * a.n_cl > G_MAX_CTAS) groups = G_MAX_CTAS / a.n_cl;
+    if (groups < 1) return cudaErrorInvalidConfiguration;
+    // the ring's hand-off counters start from zero
+    e = cudaMemsetAsync(a.gsig, 0, sizeof(unsigned) * 2 * G_MAX_CTAS * G_SLOTS, st);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = st;
+    cfg.gridDim = dim3(groups * a.n_cl, 1, 1);
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.n_cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // As many clusters as fit at once (and as the grad-tile ring has slots
-    // for), each walking several units; the results do not depend on the
-    // count, only the schedule does.
-    cfg.gridDim = dim3(n_units * a.n_cl, 1, 1);
-    int active = cache ? resident[dev][a.n_cl].load(std::memory_order_relaxed) : 0;
-    if (active < 1) {
-        if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess || active < 1) {
-            (void)cudaGetLastError();
-            active = 0;
-        }
-        if (cache && active > 0) resident[dev][a.n_cl].store(active, std::memory_order_relaxed);
-        if (active < 1) active = n_units;
-    }
-    int clusters = active < n_units ? active : n_units;
-    if (clusters * a.n_cl > G_MAX_CTAS) clusters = G_MAX_CTAS / a.n_cl;
-    cfg.gridDim = dim3(clusters * a.n_cl, 1, 1);
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 

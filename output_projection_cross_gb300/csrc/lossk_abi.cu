@@ -279,6 +279,7 @@ struct Ws {
     float *zpart() const { return reinterpret_cast<float *>(base + L.off_zpart); }
     float2 *dhc() const { return reinterpret_cast<float2 *>(base + L.off_dhc); }
     uint16_t *gring() const { return reinterpret_cast<uint16_t *>(base + L.off_gring); }
+    unsigned *gsig() const { return reinterpret_cast<unsigned *>(base + L.off_gsig); }
     float *dhacc() const { return reinterpret_cast<float *>(base + L.off_dhacc); }
 };
 
@@ -298,6 +299,7 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
     a->g_tma = make_map_ring_store(&a->map_gst, w.gring(), G_RING_ROWS) ? 1 : 0;
     const BwdGeom g = bwd_geometry(d, false);
     a->gscr = w.gring();
+    a->gsig = w.gsig();
     a->n_tok = static_cast<int>(n);
     a->vocab = static_cast<int>(V);
     a->d = static_cast<int>(d);
@@ -611,25 +613,28 @@ int32_t run_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits,
     return status_of(launch_reduce(tokacc, n, n_pad, hdr, wz, scalars_out, st));
 }
 
+// Groups of c CTAs a 152-SM GB300 holds at once (one CTA per SM, at most
+// G_MAX_CTAS CTAs for the grad-tile ring).  A fixed table, so the geometry --
+// and with it every rounding order -- is a function of the shape alone.
+static int64_t resident_groups(int64_t c)
+{
+    const int64_t by_sm = 152 / c, by_ring = G_MAX_CTAS / c;
+    return by_sm < by_ring ? by_sm : by_ring;
+}
+
 BwdGeom bwd_geometry(int64_t d, bool distill)
 {
-    // Per loop supertile and d-group a cluster of c CTAs spends nk + 4c stages
+    // Per loop supertile and d-group a group of c CTAs spends nk + 4c stages
     // per CTA (the logit tile over the whole d_model, then c grad tiles in four
     // quarters), so the pass costs about n_dg (nk + 4c) / (CTAs resident).
-    // Clusters must sit in one GPC: a 152-SM GB300 holds this many clusters of
-    // c CTAs at once (one CTA per SM; measured with the occupancy query).  A
-    // fixed table, so the geometry -- and with it every rounding order -- is a
-    // function of the shape alone.
-    static const int resident[BWD_MAX_CL + 1] = {0, 152, 76, 46, 36, 28, 23, 15, 15,
-                                                 15, 13, 8, 8, 7, 7, 7, 7};
     const int64_t ns = cdiv(d, TC_SLICE);               // 256-column slices
     const int64_t nk = cdiv(d, TC_BK);
     BwdGeom g{0, 0};
     double best = 0.0;
     for (int64_t dg = cdiv(ns, BWD_MAX_CL); dg <= ns; ++dg) {
         const int64_t c = cdiv(ns, dg);
-        if (cdiv(ns, c) != dg) continue;                // the same clusters with idle d-groups
-        const double cost = static_cast<double>(dg * (nk + 4 * c)) / static_cast<double>(c * resident[c]);
+        if (cdiv(ns, c) != dg) continue;                // the same groups with idle d-groups
+        const double cost = static_cast<double>(dg * (nk + 4 * c)) / static_cast<double>(c * resident_groups(c));
         if (g.n_cl == 0 || cost < best) {
             best = cost;
             g.n_cl = static_cast<int>(c);
@@ -642,23 +647,38 @@ BwdGeom bwd_geometry(int64_t d, bool distill)
 
 int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
 {
-    // The d_hidden pass has one cluster per (token tile, d-group, vocabulary
-    // split).  A 152-SM GB300 holds 36 four-CTA clusters at a time, so aim for
-    // 144 clusters (four full waves) on the tensor-core path, and for about
-    // two CTAs per SM on the FFMA path.  Shape-only, so results never depend
-    // on the device.
+    // The d_hidden pass has one unit per (token tile, d-group, vocabulary
+    // split), walked by the resident groups.  On the tensor-core path the
+    // split count minimises the pass's estimated time: the rounds the busiest
+    // group walks (its units times each unit's rounds of c supertiles, one
+    // round = nk + 4c ring stages at about 512 clocks each) plus reading back
+    // the splits' partial slabs (4 n d bytes each; writing them hides under
+    // the pass's arithmetic).  At most 256 splits.  On the FFMA
+    // path, about two CTAs per SM.  Shape-only, so results never depend on
+    // the device.
     const bool tc = is16(dtype);
-    const int64_t bm = tc ? TC_BM : FP_BM, bn = tc ? TC_BN_ACC : FP_BN, sl = tc ? TC_SLICE : FP_SLICE;
-    const int64_t n_yt = cdiv(V, bn);
-    const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
-    int64_t s;
     if (tc) {
-        const int64_t clusters = cdiv(n, bm) * bwd_geometry(d, false).n_dg;   // token tiles x d-groups
-        s = clusters >= 144 ? 1 : 144 / clusters;
-    } else {
-        const int64_t base = cdiv(n, bm) * cdiv(d, sl);
-        s = base >= 296 ? 1 : cdiv(296, base);
+        const BwdGeom g = bwd_geometry(d, false);
+        const int64_t c = g.n_cl, groups = resident_groups(c);
+        const int64_t tiles = cdiv(n, TC_BM) * g.n_dg, n_loop = cdiv(V, BWD_BN), nk = cdiv(d, TC_BK);
+        const double round_s = static_cast<double>(nk + 4 * c) * 512.0 / 1.9e9;
+        const double slab_s = 4.0 * static_cast<double>(n) * static_cast<double>(d) / 6.8e12;
+        int64_t best_s = 1;
+        double best = 0.0;
+        for (int64_t s = 1; s <= n_loop && s <= 256; ++s) {
+            const int64_t per_group = cdiv(tiles * s, groups), rounds = cdiv(cdiv(n_loop, s), c);
+            const double cost = static_cast<double>(per_group * rounds) * round_s + (s > 1 ? s * slab_s : 0.0);
+            if (s == 1 || cost < best) {
+                best = cost;
+                best_s = s;
+            }
+        }
+        return best_s;
     }
+    const int64_t n_yt = cdiv(V, FP_BN);
+    const int64_t cap = n_yt / 8 > 1 ? n_yt / 8 : 1;
+    const int64_t base = cdiv(n, FP_BM) * cdiv(d, FP_SLICE);
+    int64_t s = base >= 296 ? 1 : cdiv(296, base);
     if (s < 1) s = 1;
     return s < cap ? s : cap;
 }
@@ -701,6 +721,8 @@ bool ws_layout(int kind, int64_t n, int64_t d, int64_t V, int dtype, WsLayout *L
     if (fused) off = align256(off + sizeof(float2) * L->n_pad);
     L->off_gring = off;
     if (bwd && tc) off = align256(off + sizeof(uint16_t) * 128 * static_cast<size_t>(G_RING_ROWS));
+    L->off_gsig = off;
+    if (bwd && tc) off = align256(off + sizeof(unsigned) * 2 * G_MAX_CTAS * G_SLOTS);
     L->off_tstat = off;
     if (distill) off = align256(off + sizeof(double2) * L->n_pad);
     L->off_dhacc = off;

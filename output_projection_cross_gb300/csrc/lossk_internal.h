@@ -50,7 +50,8 @@ struct WsLayout {
     size_t off_dhpart = 0;   // float  [nsplit][n_tok][d_model] (nsplit > 1)
     size_t off_zpart = 0;    // float  [nsplit * BWD_MAX_CL][n_pad] fused pass: sums of G' per (split, CTA)
     size_t off_dhc = 0;      // float2 [n_pad] fused pass: d_hidden coefficients per token
-    size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the cluster passes
+    size_t off_gring = 0;    // bf16 [G_RING_ROWS][128] grad-tile ring of the group passes
+    size_t off_gsig = 0;     // unsigned [2][G_MAX_CTAS][G_SLOTS] the ring's hand-off counters
     size_t off_tstat = 0;    // double2 [n_pad] distillation: teacher (lse_t2, Eb) per token
     size_t off_dhacc = 0;    // float [n_tok][d_model] training step with accumulation: d_hidden before it is added
     size_t off_chk = 0;      // chunk self-check: two runs' lse and ce, float [4][n_pad], + double [8]
@@ -106,7 +107,7 @@ constexpr float FUSED_SHIFT = 64.f;
 // BWD_BN loop columns.  Grad-tile ring: G_SLOTS slots of one supertile
 // (2 x 128 x 128 bf16) per CTA, for at most G_MAX_CTAS CTAs.
 constexpr int BWD_BN = 256;
-constexpr int BWD_MAX_CL = 16;     // CTAs per cluster at most (above 8: a non-portable size)
+constexpr int BWD_MAX_CL = 16;     // CTAs per group at most
 constexpr int G_SLOTS = 2;
 constexpr int G_MAX_CTAS = 160;
 constexpr int64_t G_RING_ROWS = int64_t(G_MAX_CTAS) * G_SLOTS * 2 * 128;   // rows of 128 bf16
@@ -129,7 +130,7 @@ struct BwdArgs {
     int n_fixed;           // fixed tiles: token tiles (d_hidden) or vocabulary tiles (d_weight)
     int n_loop;            // loop supertiles (BWD_BN columns): vocabulary (d_hidden) or tokens (d_weight)
     int n_split;           // splits of the loop range (d_hidden)
-    int n_cl;              // CTAs per cluster = 256-column d-slices per group
+    int n_cl;              // CTAs per group (consecutive blocks sharing grad tiles) = 256-column d-slices
     int n_dg;              // d-groups (clusters per fixed tile and split)
     int direction;
     float inv_t_l2e;
@@ -141,11 +142,12 @@ struct BwdArgs {
     int accumulate;        // add the accumulator into `out` instead of overwriting it
     float out_scale;       // fp16 operands: the factor the stored accumulator is multiplied by
     const int *refused;    // nonzero: the validation before found a bad target; return at once
+    unsigned *gsig;        // grad-tile ring hand-off counters [2][G_MAX_CTAS][G_SLOTS] (ready, free)
     int *err;
 };
 
-// Cluster geometry of the backward for a d_model: slices of 256 columns, one
-// per CTA of a cluster of at most BWD_MAX_CL CTAs, d-groups beyond that (each
+// Group geometry of the backward for a d_model: slices of 256 columns, one
+// per CTA of a group of at most BWD_MAX_CL CTAs, d-groups beyond that (each
 // d-group recomputes the logits); chosen from the shape alone.
 struct BwdGeom {
     int n_cl, n_dg;

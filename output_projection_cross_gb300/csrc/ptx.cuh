@@ -116,6 +116,55 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+// ---- hand-offs through global memory -----------------------------------------
+// Monotonic counters in global memory by which CTAs of one grid (not of one
+// cluster) hand buffers to each other.  The grid is launched cooperatively, so
+// every CTA is resident and a waiter's partner always makes progress.
+
+// Add with release at GPU scope: this thread's earlier writes (and the bulk
+// async-proxy writes it has waited for and fenced) are visible to whoever
+// observes the new count with an acquire load.
+__device__ __forceinline__ void gsig_add_release(unsigned *ctr, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+// Relaxed add: announces reads that have completed (it publishes no data) and
+// never holds the issuing thread.
+__device__ __forceinline__ void gsig_add_relaxed(unsigned *ctr, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *ctr >= target, bounded like mbar_wait: after limit_ns (or as
+// soon as another thread has raised the error word) it records a timeout and
+// returns false.
+__device__ __forceinline__ bool gsig_wait(const unsigned *ctr, unsigned target, int *err,
+                                          uint64_t limit_ns = 2000000000ull)
+{
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            if (ld_acquire_gpu(ctr) >= target) return true;
+            __nanosleep(32);
+        }
+        if (*reinterpret_cast<volatile int *>(err) != ERR_NONE) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(err, ERR_NONE, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ---- TMA --------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)

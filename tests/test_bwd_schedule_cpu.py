@@ -1,19 +1,28 @@
-"""The synchronisation protocol of the backward cluster passes, checked on the host.
+"""The synchronisation protocol of the backward group passes, checked on the host.
 
-A cluster of c CTAs walks a list of units (ny loop supertiles each).  Per CTA
-three agents run: the TMA producer, the MMA issuer and the epilogue.  They meet
-on mbarriers: the operand ring (full / empty per stage), the TMEM logit buffer
-(tfull / tempty), the accumulator (accfull / accempty) and the grad-tile ring
-(gready[writer][slot] in every CTA, gfree[slot] in the writer, G_SLOTS slots per
-writer).  This model replays the kernel's program order for every agent of
+A group of c CTAs walks a list of units (ny loop supertiles each).  Per CTA
+three agents run: the TMA producer, the MMA issuer and the epilogue.  Inside a
+CTA they meet on mbarriers: the operand ring (full / empty per stage), the
+TMEM logit buffer (tfull / tempty) and the accumulator (accfull / accempty).
+Between the CTAs of the group, the grad-tile ring (G_SLOTS slots per writer)
+is handed over through two monotonic counters per slot in global memory: the
+writer adds to `ready` once per tile (the kernel: one add per epilogue warp,
+four per tile) and a loader waits until it reaches the fill it needs; every
+loader's MMA issuer adds to `free` once its loads of the tile have landed,
+and the writer waits for c adds per earlier fill before writing the slot
+again.  This model replays the kernel's program order for every agent of
 every CTA under many random interleavings and checks that
 
   * every run finishes (no deadlock: the kernel's bounded waits would turn one
-    into status 590), and
-  * no barrier ever runs two phases ahead of a waiter.  A wait on mbarrier
+    into status 590);
+  * no mbarrier ever runs two phases ahead of a waiter.  A wait on mbarrier
     phase i is a parity test: it passes when phase i has completed and phase
     i+1 has not.  If phase i+1 could complete first, the waiter would block on
-    the wrong parity (or later pass on a stale one).
+    the wrong parity (or later pass on a stale one);
+  * every load of a grad slot reads the tile it expects: the writer has
+    written that fill and not yet a later one (no read before the write, no
+    read of an overwritten slot), and a writer never writes a slot that a
+    loader has still to read.
 
 Operation order mirrors k_bwd.cu; TMA and MMA completions are modelled as
 immediate, which only removes delays.
@@ -59,9 +68,13 @@ def _schedule(nys, c):
     return steps
 
 
-def _cta_agents(j, c, nys, nk, B):
+def _cta_agents(j, c, nys, nk, B, S, free_short=0, ready_short=0):
     steps = _schedule(nys, c)
     nrounds = {k: (ny + c - 1) // c for k, ny in enumerate(nys)}
+
+    def _until(cond):
+        while not cond():
+            yield
 
     def producer():
         k_acq = 0
@@ -85,9 +98,15 @@ def _cta_agents(j, c, nys, nk, B):
                 for yy in range(r * c, min(r * c + c, ny)):
                     wr = yy - r * c
                     g, u = cnt[wr] % G_SLOTS, cnt[wr] // G_SLOTS
-                    yield from _wait(B[j]["gready"][wr][g], u)
+                    # the writer's u-th tile in slot g is published
+                    yield from _until(lambda: S["ready"][wr][g] >= u + 1 - ready_short)
                     for _ in range(4):
                         yield from acquire()
+                        # the quarter is read now (the model's TMA completes at once)
+                        if S["fills"][wr][g] != u + 1:
+                            raise Violation(f"CTA {j} read slot {g} of writer {wr} holding fill "
+                                            f"{S['fills'][wr][g] - 1}, expected {u}")
+                    S["loaded"][j][wr][g] += 1
                     cnt[wr] += 1
 
     def mma():
@@ -122,7 +141,7 @@ def _cta_agents(j, c, nys, nk, B):
                     for q in range(4):
                         s = yield from consume()
                         if q == 3:
-                            B[wr]["gfree"][g].arrive()
+                            S["free"][wr][g] += 1     # this CTA's loads of the tile have landed
                         B[j]["empty"][s].arrive()
                     cnt[wr] += 1
                 if r == nrounds[k] - 1:
@@ -136,11 +155,16 @@ def _cta_agents(j, c, nys, nk, B):
         def tile():
             nonlocal m_all
             g, u = m_all % G_SLOTS, m_all // G_SLOTS
-            yield from _wait(B[j]["gfree"][g], u - 1)
+            # every CTA of the group has loaded this slot's earlier fills
+            yield from _until(lambda: S["free"][j][g] >= c * u - free_short)
             yield from _wait(B[j]["tfull"], m_all)
-            B[j]["tempty"].arrive()
             for q in range(c):
-                B[q]["gready"][j][g].arrive()
+                if S["loaded"][q][j][g] < u:
+                    raise Violation(f"CTA {j} wrote fill {u} of slot {g} before CTA {q} read fill "
+                                    f"{S['loaded'][q][j][g]}")
+            S["fills"][j][g] += 1
+            B[j]["tempty"].arrive()
+            S["ready"][j][g] += 1
             m_all += 1
 
         def n_own(ny):
@@ -160,22 +184,25 @@ def _cta_agents(j, c, nys, nk, B):
     return [producer(), mma(), epilogue()]
 
 
-def _run(c, nys, nk, seed, gfree_arrivals=None):
+def _run(c, nys, nk, seed, free_short=0, ready_short=0):
     B = [{"full": [Bar(1) for _ in range(NST)], "empty": [Bar(1) for _ in range(NST)],
-          "tfull": Bar(1), "tempty": Bar(1), "accfull": Bar(1), "accempty": Bar(1),
-          "gready": [[Bar(1) for _ in range(G_SLOTS)] for _ in range(c)],
-          "gfree": [Bar(gfree_arrivals or c) for _ in range(G_SLOTS)]} for _ in range(c)]
-    agents = [a for j in range(c) for a in _cta_agents(j, c, nys, nk, B)]
+          "tfull": Bar(1), "tempty": Bar(1), "accfull": Bar(1), "accempty": Bar(1)} for _ in range(c)]
+    S = {"ready": [[0] * G_SLOTS for _ in range(c)], "free": [[0] * G_SLOTS for _ in range(c)],
+         "fills": [[0] * G_SLOTS for _ in range(c)],
+         "loaded": [[[0] * G_SLOTS for _ in range(c)] for _ in range(c)]}
+    agents = [a for j in range(c) for a in _cta_agents(j, c, nys, nk, B, S, free_short, ready_short)]
     rng = random.Random(seed)
     live = list(range(len(agents)))
     stalled = 0
+
+    def state():
+        return ([(b.phases, b.count) for cta in B for b in _all_bars(cta)], str(S))
     while live:
         i = rng.choice(live)
         try:
-            before = [(b.phases, b.count) for cta in B for b in _all_bars(cta)]
+            before = state()
             next(agents[i])
-            after = [(b.phases, b.count) for cta in B for b in _all_bars(cta)]
-            stalled = 0 if after != before else stalled + 1
+            stalled = 0 if state() != before else stalled + 1
         except StopIteration:
             live.remove(i)
             stalled = 0
@@ -190,9 +217,6 @@ def _all_bars(cta):
     yield cta["tempty"]
     yield cta["accfull"]
     yield cta["accempty"]
-    for row in cta["gready"]:
-        yield from row
-    yield from cta["gfree"]
 
 
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 8])
@@ -203,7 +227,7 @@ def test_protocol_finishes_without_phase_overrun(c, nys):
 
 
 @pytest.mark.parametrize("nys", [[20, 17, 3], [16], [40]])
-def test_protocol_clusters_of_16(nys):
+def test_protocol_groups_of_16(nys):
     for seed in range(2):
         _run(16, nys, nk=2, seed=seed)
 
@@ -216,31 +240,28 @@ def test_protocol_long_units(seed):
     _run(4, [8] * 7, nk=16, seed=seed)
 
 
-def test_model_detects_a_missing_release():
-    """A planted mistake -- every slot release one arrival short -- must
-    deadlock in the model, or the checks above prove nothing."""
-    with pytest.raises(AssertionError, match="deadlock"):
-        _run(2, [6], nk=3, seed=0, gfree_arrivals=3)
+def test_model_detects_a_short_free_count():
+    """A planted mistake -- the writer waiting for one release fewer than the
+    group's loads -- lets it overwrite a slot a loader has still to read; the
+    model must catch it, or the checks above prove nothing."""
+    found = False
+    for seed in range(40):
+        try:
+            _run(3, [9], nk=1, seed=seed, free_short=1)
+        except Violation:
+            found = True
+            break
+    assert found
 
 
-def test_model_detects_a_phase_overrun():
-    """A planted mistake -- a single grad slot per writer, filled again before
-    every CTA has loaded it when the loaders' gready waits lag -- is caught by
-    the parity check: with one ready barrier per writer and two tiles in
-    flight, a lagging loader can see the barrier two phases ahead."""
-    global G_SLOTS
-    saved = G_SLOTS
-    try:
-        G_SLOTS = 1
-        found = False
-        for seed in range(40):
-            try:
-                _run(2, [8], nk=1, seed=seed, gfree_arrivals=1)   # release after one loader only
-            except Violation:
-                found = True
-                break
-            except AssertionError:
-                pass
-        assert found
-    finally:
-        G_SLOTS = saved
+def test_model_detects_a_short_ready_count():
+    """A planted mistake -- a loader waiting for one publication fewer than
+    the fill it needs -- lets it read a slot before the tile is written."""
+    found = False
+    for seed in range(40):
+        try:
+            _run(2, [8], nk=1, seed=seed, ready_short=1)
+        except Violation:
+            found = True
+            break
+    assert found
