@@ -162,6 +162,27 @@ static double lse_row(const double *x, int64_t V)
     return m + log(s);
 }
 
+/* A block of logit rows: buf[r][v] = H[t] . W[v] (dot_asc) for the R tokens
+ * t = rows[r] (or t = t0 + r when rows is NULL) and every v < V.  Each
+ * element is the one dot product above; the buffer is filled tile by tile
+ * (64 tokens x 64 vocabulary rows, tiles spread over the threads) so that a
+ * weight row is read from memory once per tile of tokens instead of once per
+ * token.  The fill order changes no element. */
+static void fill_logits(const float *H, const float *W, const int64_t *rows, int64_t t0, int64_t R,
+                        int64_t d, int64_t V, double *buf)
+{
+    const int64_t TB = 64;
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t rb = 0; rb < R; rb += TB)
+        for (int64_t vb = 0; vb < V; vb += TB) {
+            const int64_t r1 = rb + TB < R ? rb + TB : R, v1 = vb + TB < V ? vb + TB : V;
+            for (int64_t r = rb; r < r1; ++r) {
+                const float *h = H + (rows ? rows[r] : t0 + r) * d;
+                for (int64_t v = vb; v < v1; ++v) buf[r * V + v] = dot_asc(h, W + v * d, d);
+            }
+        }
+}
+
 static int64_t count_valid(const uint8_t *mask, int64_t n)
 {
     if (!mask) return n;
@@ -268,10 +289,7 @@ int oracle_ce_fwd(const float *H, const float *W, const int64_t *y, const uint8_
     for (int64_t t0 = 0; t0 < n; t0 += chunk) {
         int64_t rows = n - t0 < chunk ? n - t0 : chunk;
         /* project the chunk: buf[r][v] = H[t0+r] . W[v] */
-        #pragma omp parallel for collapse(2) schedule(static)
-        for (int64_t r = 0; r < rows; ++r)
-            for (int64_t v = 0; v < V; ++v)
-                buf[r * V + v] = dot_asc(H + (t0 + r) * d, W + v * d, d);
+        fill_logits(H, W, NULL, t0, rows, d, V, buf);
         /* reduce each row to (lse, target logit) and drop the chunk */
         #pragma omp parallel for schedule(static)
         for (int64_t r = 0; r < rows; ++r) {
@@ -369,13 +387,16 @@ int oracle_ce_token_rows(const float *H, const float *W, const int64_t *y, const
     int st = fused_checks(n, d, V, 0, y, wz, grad_scale);
     if (st != OR_OK) return st;
     int64_t nvalid = count_valid(mask, n);
-    #pragma omp parallel
-    {
-        double *s = (double *)malloc(sizeof(double) * (size_t)V);
-        #pragma omp for schedule(dynamic, 1)
-        for (int64_t i = 0; i < n_rows; ++i) {
-            int64_t t = rows[i];
-            for (int64_t v = 0; v < V; ++v) s[v] = dot_asc(H + t * d, W + v * d, d);
+    /* the listed tokens' logit rows, a block of at most 256 at a time */
+    const int64_t RB = 256;
+    double *blk = (double *)malloc(sizeof(double) * (size_t)((n_rows < RB ? n_rows : RB) * V));
+    for (int64_t i0 = 0; i0 < n_rows; i0 += RB) {
+        const int64_t nb = n_rows - i0 < RB ? n_rows - i0 : RB;
+        fill_logits(H, W, rows + i0, 0, nb, d, V, blk);
+        #pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t ib = 0; ib < nb; ++ib) {
+            const int64_t i = i0 + ib, t = rows[i];
+            const double *s = blk + ib * V;
             double lse = lse_row(s, V);
             lse_out[i] = lse;
             tgt_out[i] = s[y[t]];
@@ -393,8 +414,8 @@ int oracle_ce_token_rows(const float *H, const float *W, const int64_t *y, const
                 }
             }
         }
-        free(s);
     }
+    free(blk);
     return OR_OK;
 }
 
@@ -613,7 +634,9 @@ int oracle_distill_from_logits(const float *logits, const float *teacher, const 
     return OR_OK;
 }
 
-/* Sampled distillation rows: per listed token, L_t, lse(a) and the dH row. */
+/* Sampled distillation rows: per listed token, L_t, lse(a) and the dH row.
+ * The listed tokens' logit rows are computed a block of at most 256 tokens
+ * at a time (fill_logits), then each row is reduced on its own. */
 int oracle_distill_token_rows(const float *H, const float *W, const float *teacher,
                               const uint8_t *mask, int64_t n, int64_t d, int64_t V,
                               int direction, double T, double wz, double grad_scale,
@@ -625,35 +648,40 @@ int oracle_distill_token_rows(const float *H, const float *W, const float *teach
     if (!scalar_ok(T) || T <= 0.0) return OR_NON_FINITE_SCALAR;
     if (direction < 0 || direction > 2) return OR_UNKNOWN_OBJECTIVE;
     int64_t nvalid = count_valid(mask, n);
-    #pragma omp parallel
-    {
-        double *s = (double *)malloc(sizeof(double) * (size_t)V);
-        double *a = (double *)malloc(sizeof(double) * (size_t)V);
-        double *b = (double *)malloc(sizeof(double) * (size_t)V);
-        double *g = (double *)malloc(sizeof(double) * (size_t)V);
-        #pragma omp for schedule(dynamic, 1)
-        for (int64_t i = 0; i < n_rows; ++i) {
-            int64_t t = rows[i];
-            for (int64_t v = 0; v < V; ++v) s[v] = dot_asc(H + t * d, W + v * d, d);
-            double la;
-            double L = distill_row(s, teacher + t * V, V, direction, T, a, b, &la, g);
-            int on = mask ? (mask[t] != 0) : 1;
-            loss_out[i] = L;
-            lse_out[i] = la;
-            if (dH_rows) {
-                double alpha = (on && nvalid > 0) ? grad_scale / (double)nvalid : 0.0;
-                double *dh = dH_rows + i * d;
-                for (int64_t k = 0; k < d; ++k) dh[k] = 0.0;
-                for (int64_t v = 0; v < V; ++v) {
-                    double q = exp(a[v] - la);
-                    double gv = alpha * (g[v] + 2.0 * wz * la * q / T);
-                    const float *w = W + v * d;
-                    for (int64_t k = 0; k < d; ++k) dh[k] += gv * (double)w[k];
+    const int64_t RB = 256;
+    double *blk = (double *)malloc(sizeof(double) * (size_t)((n_rows < RB ? n_rows : RB) * V));
+    for (int64_t i0 = 0; i0 < n_rows; i0 += RB) {
+        const int64_t nb = n_rows - i0 < RB ? n_rows - i0 : RB;
+        fill_logits(H, W, rows + i0, 0, nb, d, V, blk);
+        #pragma omp parallel
+        {
+            double *a = (double *)malloc(sizeof(double) * (size_t)V);
+            double *b = (double *)malloc(sizeof(double) * (size_t)V);
+            double *g = (double *)malloc(sizeof(double) * (size_t)V);
+            #pragma omp for schedule(dynamic, 1)
+            for (int64_t ib = 0; ib < nb; ++ib) {
+                const int64_t i = i0 + ib, t = rows[i];
+                double la;
+                double L = distill_row(blk + ib * V, teacher + t * V, V, direction, T, a, b, &la, g);
+                int on = mask ? (mask[t] != 0) : 1;
+                loss_out[i] = L;
+                lse_out[i] = la;
+                if (dH_rows) {
+                    double alpha = (on && nvalid > 0) ? grad_scale / (double)nvalid : 0.0;
+                    double *dh = dH_rows + i * d;
+                    for (int64_t k = 0; k < d; ++k) dh[k] = 0.0;
+                    for (int64_t v = 0; v < V; ++v) {
+                        double q = exp(a[v] - la);
+                        double gv = alpha * (g[v] + 2.0 * wz * la * q / T);
+                        const float *w = W + v * d;
+                        for (int64_t k = 0; k < d; ++k) dh[k] += gv * (double)w[k];
+                    }
                 }
             }
+            free(a); free(b); free(g);
         }
-        free(s); free(a); free(b); free(g);
     }
+    free(blk);
     return OR_OK;
 }
 
