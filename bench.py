@@ -215,7 +215,7 @@ def _code_only(text):
 # What builds the cluster passes and launches them: the kernel, the headers it
 # includes, and the host side that encodes its tensor maps and launch shapes.
 # The streaming and CTA-pair kernels are other translation units.
-BWD_KERNEL_SRCS = ("output_projection_cross_gb300/csrc/k_bwd.cu",
+BWD_KERNEL_SRCS = ("output_projection_cross_gb300/csrc/k_bwp.cu",
                    "output_projection_cross_gb300/csrc/ptx.cuh",
                    "output_projection_cross_gb300/csrc/lossk_internal.h",
                    "output_projection_cross_gb300/csrc/lossk_abi.cu",

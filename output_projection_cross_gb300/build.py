@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liblossk.so")
-SOURCES = ["lossk_abi.cu", "k_fwd2.cu", "k_bwd.cu", "k_bwp.cu", "k_simt.cu", "lossk_static.cu"]
+SOURCES = ["lossk_abi.cu", "k_fwd2.cu", "k_bwp.cu", "k_simt.cu", "lossk_static.cu"]
 HEADERS = ["ptx.cuh", "lossk_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

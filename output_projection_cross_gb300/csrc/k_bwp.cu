@@ -40,8 +40,9 @@
 // tile); a loader's TMA producer waits for the ready count (acquire) before
 // loading.  Groups are not clusters: only the two CTAs of a pair form a
 // cluster (cta_group::2 needs one), and a group's pairs wait on each other
-// through global memory, which the cooperative launch makes safe (every CTA
-// of the grid is resident).  Groups of 4 pairs fill all 152 SMs of a GB300.
+// through global memory, which is safe as the grid never holds more pairs
+// than fit at once (every CTA of the grid is resident).  Groups of 4 pairs
+// fill all 152 SMs of a GB300.
 //
 // BWD_FUSED is the d_hidden schedule run before any log-sum-exp is known: its
 // grad tile is the unnormalised G'[t][v] = 2^(s[t][v] log2e - r_t) with the
@@ -830,13 +831,11 @@ static cudaError_t launch_bwp_one(const BwdArgs &a, int n_units, cudaStream_t st
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     int pairs = cache ? resident[dev].load(std::memory_order_acquire) : 0;
     if (pairs < 1) {
@@ -854,7 +853,11 @@ static cudaError_t launch_bwp_one(const BwdArgs &a, int n_units, cudaStream_t st
     // ring has slots for), each walking several units; the results do not
     // depend on the count, only the schedule does.  Every CTA of the grid
     // must be resident at the same time (the groups' pairs wait on each
-    // other): the launch is cooperative.
+    // other): the grid never holds more pairs than the occupancy query says
+    // fit at once, one CTA per SM, so once no other kernel holds an SM every
+    // pair is resident; a pair kept out longer than the waits' limit turns
+    // into status 590, not a hang.  (A cooperative launch would state the same
+    // guarantee, but the profiler cannot launch one.)
     int groups = pairs / a.n_cl;
     if (groups > n_units) groups = n_units;
     if (groups * 2 * a.n_cl > G_MAX_CTAS) groups = G_MAX_CTAS / (2 * a.n_cl);
@@ -863,7 +866,7 @@ static cudaError_t launch_bwp_one(const BwdArgs &a, int n_units, cudaStream_t st
     e = cudaMemsetAsync(a.gsig, 0, sizeof(unsigned) * 2 * G_MAX_CTAS * G_SLOTS, st);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(groups * 2 * a.n_cl, 1, 1);
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 

@@ -550,7 +550,7 @@ cudaError_t launch_sum_splits(const float *part, int64_t nsplit, int64_t count, 
 }
 
 // ---------------------------------------------------------------------------
-// The fused forward + d_hidden path.  See k_bwd.cu (BWD_FUSED) for the pass
+// The fused forward + d_hidden path.  See k_bwp.cu (BWD_FUSED) for the pass
 // itself: it exponentiates every logit against r_t = s[t][y_t] log2e + 64 and
 // reports, per (split, CTA, token), the sum of those terms.
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }

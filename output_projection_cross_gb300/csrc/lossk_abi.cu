@@ -293,19 +293,19 @@ bool bwd_args(const Ws &w, bool rows, int64_t n, int64_t d, int64_t V, const voi
     const void *Fx = rows ? H : W, *Lp = rows ? W : H;
     const int64_t nf = rows ? n : V, nl = rows ? V : n;
     const BwdGeom g = bwd_geometry(d, false);
-    // a CTA of a pair loads half of the loop supertile and half of the d-slice
-    const uint32_t loop_box = g.pairs ? BWD_BN / 2 : BWD_BN, nblk = g.pairs ? 2 : 4;
-    if (!make_map(&a->map_fix, Fx, d, nf, 64, 128) || !make_map(&a->map_loop, Lp, d, nl, 64, loop_box) ||
+    // a CTA of a pair loads its 128 fixed rows, half of the loop supertile and
+    // half of the d-slice
+    if (!make_map(&a->map_fix, Fx, d, nf, 64, 128) || !make_map(&a->map_loop, Lp, d, nl, 64, BWD_BN / 2) ||
         !make_map(&a->map_ys, Lp, d, nl, 64, 64) || !make_map(&a->map_g, w.gring(), 128, G_RING_ROWS, 64, 128))
         return false;
-    a->ys3 = make_map_blocks(&a->map_ys3, Lp, d, nl, 64, nblk) ? 1 : 0;
+    a->ys3 = make_map_blocks(&a->map_ys3, Lp, d, nl, 64, 2) ? 1 : 0;
     a->g_tma = make_map_ring_store(&a->map_gst, w.gring(), G_RING_ROWS) ? 1 : 0;
     a->gscr = w.gring();
     a->gsig = w.gsig();
     a->n_tok = static_cast<int>(n);
     a->vocab = static_cast<int>(V);
     a->d = static_cast<int>(d);
-    a->n_fixed = static_cast<int>(cdiv(nf, g.pairs ? 256 : 128));
+    a->n_fixed = static_cast<int>(cdiv(nf, 256));
     a->n_loop = static_cast<int>(cdiv(nl, BWD_BN));
     a->n_split = 1;
     a->n_cl = g.n_cl;
@@ -405,9 +405,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
-                e = bwd_geometry(d, distill).pairs
-                        ? launch_bwp(rows ? BWD_ROWS : BWD_COLS, distill, dtype == LOSSK_F16, a, n_units, st)
-                        : launch_bwd(rows ? BWD_ROWS : BWD_COLS, distill, dtype == LOSSK_F16, a, n_units, st);
+                e = launch_bwp(rows ? BWD_ROWS : BWD_COLS, distill, dtype == LOSSK_F16, a, n_units, st);
             }
             if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
             if (rows && L.nsplit > 1) {
@@ -448,7 +446,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
 // The d_hidden schedule of the backward run before any lse exists: every logit
 // is exponentiated against the per-token shift r_t = s[t][y_t] log2e + 64
 // (computed with the validation), the pass accumulates D = G' W and reports the sums of G'
-// (BWD_FUSED in k_bwd.cu), merge_fused turns the sums into lse, ce, z and the
+// (BWD_FUSED in k_bwp.cu), merge_fused turns the sums into lse, ce, z and the
 // d_weight parameters, and combine_dh scales D into d_hidden.  One logit pass
 // less than the separate forward and d_hidden passes.  A row whose shifted
 // terms left the trusted range raises the workspace's redo word; the caller
@@ -506,8 +504,7 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     a.err = &w.hdr()->err;
     {
         Launch k(KK_TC_FUSED, st);
-        e = g.pairs ? launch_bwp(BWD_FUSED, false, false, a, a.n_fixed * a.n_split * a.n_dg, st)
-                    : launch_bwd(BWD_FUSED, false, false, a, a.n_fixed * a.n_split * a.n_dg, st);
+        e = launch_bwp(BWD_FUSED, false, false, a, a.n_fixed * a.n_split * a.n_dg, st);
     }
     if (e != cudaSuccess) return LOSSK_DEVICE_ERROR;
     {
@@ -618,22 +615,13 @@ int32_t run_from_logits(int64_t n, int64_t V, int32_t dtype, const void *logits,
     return status_of(launch_reduce(tokacc, n, n_pad, hdr, wz, scalars_out, st));
 }
 
-// Whether the cluster passes run on CTA pairs: a shape-only choice (so every
-// rounding order is a function of the shape alone).
-static bool bwd_pairs(int64_t d)
+// Groups of c CTA pairs a 152-SM GB300 holds at once (one CTA per SM, at
+// most G_MAX_CTAS CTAs for the grad-tile ring).  A fixed table, so the
+// geometry -- and with it every rounding order -- is a function of the shape
+// alone.
+static int64_t resident_groups(int64_t c)
 {
-    (void)d;
-    return true;
-}
-
-// Groups of c CTAs (or of c CTA pairs) a 152-SM GB300 holds at once (one CTA
-// per SM, at most G_MAX_CTAS CTAs for the grad-tile ring).  A fixed table, so
-// the geometry -- and with it every rounding order -- is a function of the
-// shape alone.
-static int64_t resident_groups(int64_t c, bool pairs)
-{
-    const int64_t ctas = pairs ? 2 * c : c;
-    const int64_t by_sm = 152 / ctas, by_ring = G_MAX_CTAS / ctas;
+    const int64_t by_sm = 152 / (2 * c), by_ring = G_MAX_CTAS / (2 * c);
     return by_sm < by_ring ? by_sm : by_ring;
 }
 
@@ -644,13 +632,12 @@ BwdGeom bwd_geometry(int64_t d, bool distill)
     // quarters), so the pass costs about n_dg (nk + 4c) / (CTAs resident).
     const int64_t ns = cdiv(d, TC_SLICE);               // 256-column slices
     const int64_t nk = cdiv(d, TC_BK);
-    const bool pairs = bwd_pairs(d);
-    BwdGeom g{0, 0, pairs};
+    BwdGeom g{0, 0};
     double best = 0.0;
     for (int64_t dg = cdiv(ns, BWD_MAX_CL); dg <= ns; ++dg) {
         const int64_t c = cdiv(ns, dg);
         if (cdiv(ns, c) != dg) continue;                // the same groups with idle d-groups
-        const int64_t ctas = (pairs ? 2 * c : c) * resident_groups(c, pairs);
+        const int64_t ctas = 2 * c * resident_groups(c);
         if (ctas < 1) continue;
         const double cost = static_cast<double>(dg * (nk + 4 * c)) / static_cast<double>(ctas);
         if (g.n_cl == 0 || cost < best) {
@@ -677,8 +664,8 @@ int64_t dh_splits(int64_t n, int64_t d, int64_t V, int dtype)
     const bool tc = is16(dtype);
     if (tc) {
         const BwdGeom g = bwd_geometry(d, false);
-        const int64_t c = g.n_cl, groups = resident_groups(c, g.pairs);
-        const int64_t tiles = cdiv(n, g.pairs ? 2 * TC_BM : TC_BM) * g.n_dg, n_loop = cdiv(V, BWD_BN),
+        const int64_t c = g.n_cl, groups = resident_groups(c);
+        const int64_t tiles = cdiv(n, 2 * TC_BM) * g.n_dg, n_loop = cdiv(V, BWD_BN),
                       nk = cdiv(d, TC_BK);
         const double round_s = static_cast<double>(nk + 4 * c) * 512.0 / 1.9e9;
         const double slab_s = 4.0 * static_cast<double>(n) * static_cast<double>(d) / 6.8e12;

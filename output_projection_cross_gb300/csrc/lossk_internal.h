@@ -97,7 +97,7 @@ struct TcArgs {
 
 // ---- backward (cluster-shared grad tiles) kernel arguments -------------------
 // BWD_FUSED: the d_hidden schedule run as the forward pass as well, with a
-// per-token reference shift in place of the log-sum-exp (k_bwd.cu).
+// per-token reference shift in place of the log-sum-exp (k_bwp.cu).
 enum BwdMode : int { BWD_ROWS = 1, BWD_COLS = 2, BWD_FUSED = 3 };
 
 // The fused pass's reference: r_t = s[t][y_t] log2e + FUSED_SHIFT (log2 units).
@@ -113,11 +113,11 @@ constexpr int G_MAX_CTAS = 160;
 constexpr int64_t G_RING_ROWS = int64_t(G_MAX_CTAS) * G_SLOTS * 2 * 128;   // rows of 128 bf16
 
 struct BwdArgs {
-    CUtensorMap map_fix;   // the fixed tensor (hidden for d_hidden, weight for d_weight), box {64, 128}
-    CUtensorMap map_loop;  // the loop tensor as the logit MMA's B operand, box {64, 256} (pairs: {64, 128})
+    CUtensorMap map_fix;   // the fixed tensor (hidden for d_hidden, weight for d_weight), box {64, 128} (a CTA's half)
+    CUtensorMap map_loop;  // the loop tensor as the logit MMA's B operand (a CTA's half), box {64, 128}
     CUtensorMap map_ys;    // the loop tensor rows x d-slice (MN-major B of the accumulate), box {64, 64}
     CUtensorMap map_g;     // the grad-tile ring [G_RING_ROWS][128] bf16, box {64, 128}
-    CUtensorMap map_ys3;   // map_ys as [64-column blocks][rows][64] (d_model % 64 == 0): one box {64, 64, 4} (pairs: 2)
+    CUtensorMap map_ys3;   // map_ys as [64-column blocks][rows][64] (d_model % 64 == 0): one box {64, 64, 2}
     int ys3;               // map_ys3 is valid
     CUtensorMap map_teach; // distillation d_weight: teacher [n_tok][vocab] bf16, box {32, 32}
     CUtensorMap map_gst;   // the grad-tile ring for stores, box {32, 32} bf16, 64-byte swizzle
@@ -149,12 +149,10 @@ struct BwdArgs {
 // Group geometry of the backward for a d_model: slices of 256 columns, one
 // per CTA of a group of at most BWD_MAX_CL CTAs, d-groups beyond that (each
 // d-group recomputes the logits); chosen from the shape alone.
-// pairs: the passes run on CTA pairs (k_bwp.cu; n_cl pairs per group, fixed
-// tiles of 256 rows), else on single CTAs (k_bwd.cu; n_cl CTAs per group,
-// fixed tiles of 128 rows).
+// The passes run on CTA pairs (k_bwp.cu): n_cl pairs per group, fixed tiles of
+// 256 rows.
 struct BwdGeom {
     int n_cl, n_dg;
-    bool pairs;
 };
 BwdGeom bwd_geometry(int64_t d, bool distill);
 
@@ -228,10 +226,9 @@ cudaError_t launch_validate(const int64_t *targets, const uint8_t *mask, int64_t
 // waits on each with the bounded wait (limit_ns); an expired wait sets *err.
 cudaError_t launch_wait_selftest(int n_stages, int n_arrive, uint64_t limit_ns, int *err, int *seen,
                                  cudaStream_t st);
-// Persistent clusters: at most as many as fit at once, walking `n_units` units.
-// f16: fp16 operands (BWD_ROWS / BWD_COLS only); otherwise bf16.
-cudaError_t launch_bwd(int mode, bool distill, bool f16, const BwdArgs &a, int n_units, cudaStream_t st);
-// The same passes on CTA pairs (BwdArgs built for pairs: fixed tiles of 256 rows).
+// The group passes on CTA pairs (k_bwp.cu): persistent groups, at most as many
+// as fit at once, walking `n_units` units.  f16: fp16 operands (BWD_ROWS /
+// BWD_COLS only); otherwise bf16.
 cudaError_t launch_bwp(int mode, bool distill, bool f16, const BwdArgs &a, int n_units, cudaStream_t st);
 cudaError_t launch_fwd2(const TcArgs &a, bool distill, bool f16, int grid, cudaStream_t st);
 cudaError_t launch_fp(int mode, bool distill, const void *X, const void *Y, const float *teach,

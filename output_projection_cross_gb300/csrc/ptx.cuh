@@ -118,8 +118,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
 
 // ---- hand-offs through global memory -----------------------------------------
 // Monotonic counters in global memory by which CTAs of one grid (not of one
-// cluster) hand buffers to each other.  The grid is launched cooperatively, so
-// every CTA is resident and a waiter's partner always makes progress.
+// cluster) hand buffers to each other.  Such a grid never holds more CTAs than
+// fit at once, so every CTA is resident and a waiter's partner makes progress.
 
 // Add with release at GPU scope: this thread's earlier writes (and the bulk
 // async-proxy writes it has waited for and fenced) are visible to whoever

@@ -1,10 +1,14 @@
 """The synchronisation protocol of the backward group passes, checked on the host.
 
-A group of c CTAs walks a list of units (ny loop supertiles each).  Per CTA
-three agents run: the TMA producer, the MMA issuer and the epilogue.  Inside a
-CTA they meet on mbarriers: the operand ring (full / empty per stage), the
-TMEM logit buffer (tfull / tempty) and the accumulator (accfull / accempty).
-Between the CTAs of the group, the grad-tile ring (G_SLOTS slots per writer)
+A group of c CTA pairs walks a list of units (ny loop supertiles each).  The
+two CTAs of a pair act as one MMA unit and meet on the same barriers at the
+same points of their program, so the model takes one agent set per pair
+(the pair's barriers complete when both CTAs have arrived, which only delays
+them).  Per pair three agents run: the TMA producer, the MMA issuer and the
+epilogue.  Inside a pair they meet on mbarriers: the operand ring (full /
+empty per stage), the TMEM logit buffer (tfull / tempty) and the accumulator
+(accfull / accempty).  Between the pairs of the group, the grad-tile ring
+(G_SLOTS slots per writer)
 is handed over through two monotonic counters per slot in global memory: the
 writer adds to `ready` once per tile (the kernel: one add per epilogue warp,
 four per tile) and a loader waits until it reaches the fill it needs; every
@@ -24,14 +28,14 @@ every CTA under many random interleavings and checks that
     read of an overwritten slot), and a writer never writes a slot that a
     loader has still to read.
 
-Operation order mirrors k_bwd.cu; TMA and MMA completions are modelled as
+Operation order mirrors k_bwp.cu; TMA and MMA completions are modelled as
 immediate, which only removes delays.
 """
 import random
 
 import pytest
 
-NST, G_SLOTS = 4, 2
+NST, G_SLOTS = 6, 2
 
 
 class Bar:
