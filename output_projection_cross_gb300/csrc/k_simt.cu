@@ -230,6 +230,29 @@ __device__ __forceinline__ float teach_exp2(float x)
     else return exp2f(x);
 }
 
+// The largest of a 16-byte vector's values (as fmaxf: a NaN loses to a
+// number), the 16-bit ones compared two at a time in their own format
+// (exact: the maximum is one of the values).
+template <typename T> __device__ __forceinline__ float raw_max(const uint4 &v)
+{
+    if constexpr (sizeof(T) == 4) {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    } else {
+        uint32_t a, b, m;
+        if constexpr (kIsF16<T>) {
+            asm("max.f16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+            asm("max.f16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+            asm("max.f16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+        } else {
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+        }
+        return fmaxf(h16_lo<kIsF16<T>>(m), h16_hi<kIsF16<T>>(m));
+    }
+}
+
 // One warp's scan of a teacher row into (M, Z, E), merged over the lanes:
 // b = x kT for raw logits x, M the running maximum of b, Z = sum 2^(b - M) and
 // E = sum 2^(b - M) x (scaled by kT at the end), so each element costs one FFMA
@@ -248,11 +271,8 @@ __device__ __forceinline__ void teacher_scan(const T *__restrict__ row, int64_t 
     M = -INFINITY;
     Z = 0;
     E = 0;
-    auto absorb = [&](const float (&x)[VEC], int nv) {
-        float cm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < VEC; ++i)
-            if (i < nv) cm = fmaxf(cm, x[i]);
+    // cm: the largest of the nv raw values x
+    auto absorb = [&](const float (&x)[VEC], int nv, float cm) {
         cm *= kT;                                   // kT > 0: the maximum commutes with the scale
         if (cm > M) {
             const A f = static_cast<A>(teach_exp2<T>(M - cm));
@@ -289,7 +309,7 @@ __device__ __forceinline__ void teacher_scan(const T *__restrict__ row, int64_t 
                     x[2 * i] = h16_lo<kIsF16<T>>(q[i]);
                     x[2 * i + 1] = h16_hi<kIsF16<T>>(q[i]);
                 }
-                absorb(x, VEC);
+                absorb(x, VEC, raw_max<T>(w[u]));
             }
         }
     } else {
@@ -298,7 +318,11 @@ __device__ __forceinline__ void teacher_scan(const T *__restrict__ row, int64_t 
             const int nv = V - v0 < VEC ? static_cast<int>(V - v0) : VEC;
 #pragma unroll
             for (int i = 0; i < VEC; ++i) x[i] = i < nv ? static_cast<float>(row[v0 + i]) : 0.f;
-            absorb(x, nv);
+            float cm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i)
+                if (i < nv) cm = fmaxf(cm, x[i]);
+            absorb(x, nv, cm);
         }
     }
     E *= static_cast<A>(kT);
@@ -520,16 +544,42 @@ cudaError_t launch_tokp_ce(const float *lse, const int64_t *targets, const uint8
 }
 
 // ---------------------------------------------------------------------------
+// Element i of the nsplit partial planes (count4 float4 apart), added in split
+// order.  The planes are read once, so the loads stream past L2, eight (then
+// four, then one) at a time so that each thread keeps several in flight.
+__device__ __forceinline__ float4 split_sum(const float4 *__restrict__ part, int64_t nsplit, int64_t count4,
+                                            int64_t i)
+{
+    auto add = [](float4 &a, const float4 &v) {
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    };
+    float4 acc = __ldcs(part + i);
+    int64_t s = 1;
+    for (; s + 8 <= nsplit; s += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __ldcs(part + (s + q) * count4 + i);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) add(acc, v[q]);
+    }
+    if (s + 4 <= nsplit) {
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = __ldcs(part + (s + q) * count4 + i);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) add(acc, v[q]);
+        s += 4;
+    }
+    for (; s < nsplit; ++s) add(acc, __ldcs(part + s * count4 + i));
+    return acc;
+}
+
 __global__ void sum_splits_kernel(const float4 *__restrict__ part, int64_t nsplit, int64_t count4,
                                   float4 *__restrict__ out, int accumulate)
 {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float4 acc = part[i];
-        for (int64_t s = 1; s < nsplit; ++s) {
-            const float4 v = part[s * count4 + i];
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
+        float4 acc = split_sum(part, nsplit, count4, i);
         if (accumulate) {
             const float4 o = out[i];
             acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
@@ -758,11 +808,7 @@ __global__ void combine_dh_kernel(const float4 *part, int64_t nsplit, int64_t n,
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t t = i / d4, k4 = i - t * d4;
-        float4 acc = part[i];
-        for (int64_t s = 1; s < nsplit; ++s) {
-            const float4 v = part[s * count4 + i];
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
+        const float4 acc = split_sum(part, nsplit, count4, i);
         const float2 c = dhc[t];
         const uint2 wv = *reinterpret_cast<const uint2 *>(W + targets[t] * (d4 * 4) + k4 * 4);
         float4 o;
@@ -1032,18 +1078,16 @@ template <typename T> __device__ __forceinline__ void cvt16(const uint4 &v, floa
     }
 }
 
-// One 16-byte vector into a running (max m, sum z) in log2 units: the
-// vector's maximum first, one rescale if it rose, then its exponentials,
-// which do not depend on one another.
-template <int NV> __device__ __forceinline__ void online_vec(float &m, float &z, float (&f)[NV], float scale)
+// One 16-byte vector of raw values f into a running (max m, sum z) of
+// f * scale in log2 units (scale > 0): the vector's maximum lm (raw_max of
+// the same vector; scaling commutes with it) first, one rescale if it rose,
+// then its exponentials, which do not depend on one another, each argument
+// one FFMA.
+template <int NV>
+__device__ __forceinline__ void online_vec(float &m, float &z, const float (&f)[NV], float scale, float lm)
 {
-    float lm = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-        f[u] *= scale;
-        lm = fmaxf(lm, f[u]);
-    }
     if (lm == -INFINITY) return;                   // every term is zero
+    lm *= scale;
     if (lm > m) {
         z *= ex2_approx(m - lm);
         m = lm;
@@ -1051,8 +1095,8 @@ template <int NV> __device__ __forceinline__ void online_vec(float &m, float &z,
     float z0 = 0.f, z1 = 0.f;
 #pragma unroll
     for (int u = 0; u < NV; u += 2) {
-        z0 += ex2_approx(f[u] - m);
-        z1 += ex2_approx(f[u + 1] - m);
+        z0 += ex2_approx(fmaf(f[u], scale, -m));
+        z1 += ex2_approx(fmaf(f[u + 1], scale, -m));
     }
     z += z0 + z1;
 }
@@ -1103,7 +1147,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) from_logits_kernel(const T *__r
                 if (base + u * NT + tid >= nvec) continue;
                 float f[NV];
                 cvt16<T>(v[u], f);
-                online_vec<NV>(m, z, f, L2E);
+                online_vec<NV>(m, z, f, L2E, raw_max<T>(v[u]));
             }
         }
     } else {
@@ -1176,9 +1220,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) from_logits_kernel(const T *__r
                 float f[NV], gv[NV];
                 cvt16<T>(v[u], f);
 #pragma unroll
-                for (int q = 0; q < NV; ++q) {
-                    gv[q] = c * ex2_approx(fmaf(f[q], L2E, -lse2));
-                    if (i * NV + q == y) gv[q] -= at;
+                for (int q = 0; q < NV; ++q) gv[q] = c * ex2_approx(fmaf(f[q], L2E, -lse2));
+                const int64_t dy = y - i * NV;     // the one-hot term, in one vector of the row
+                if (dy >= 0 && dy < NV) {
+#pragma unroll
+                    for (int q = 0; q < NV; ++q)
+                        if (q == dy) gv[q] -= at;
                 }
                 store_vec(g + i * NV, gv);
             }
@@ -1291,20 +1338,19 @@ __device__ __forceinline__ void dl_merge(DlState<A> &S, const DlState<A> &O)
     S.mt = Mt;
 }
 
-// One 16-byte vector of student and teacher logits into the running maxima,
-// sums and the direction's cross sums (as dl_add, vector-wise: the maxima
-// first, one rescale each if they rose, then the independent exponentials).
+// One 16-byte vector of raw student and teacher logits (fa, fb; a = fa kT,
+// b = fb kT) into the running maxima, sums and the direction's cross sums, as
+// dl_add does element-wise: the maxima first (lms, lmt: raw_max of the two
+// vectors; kT > 0 commutes with them), one rescale each if they rose, then the
+// independent exponentials, each argument one FFMA.  The cross sums take the
+// raw logits: a state built by dl_vec holds xa, xb and xq divided by kT (the
+// row kernel scales them back once).
 template <typename T, typename A, int NV>
-__device__ __forceinline__ void dl_vec(DlState<A> &S, float (&fa)[NV], float (&fb)[NV], float kT, int direction)
+__device__ __forceinline__ void dl_vec(DlState<A> &S, const float (&fa)[NV], const float (&fb)[NV], float kT,
+                                       int direction, float lms, float lmt)
 {
-    float lms = -INFINITY, lmt = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-        fa[u] *= kT;
-        fb[u] *= kT;
-        lms = fmaxf(lms, fa[u]);
-        lmt = fmaxf(lmt, fb[u]);
-    }
+    lms *= kT;
+    lmt *= kT;
     if (lms > S.ms) {
         const A f = static_cast<A>(teach_exp2<T>(S.ms - lms));
         S.zs *= f;
@@ -1324,8 +1370,8 @@ __device__ __forceinline__ void dl_vec(DlState<A> &S, float (&fa)[NV], float (&f
     A zs = 0, zt = 0, x1 = 0, x2 = 0;
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const A es = static_cast<A>(teach_exp2<T>(fa[u] - S.ms));
-        const A et = static_cast<A>(teach_exp2<T>(fb[u] - S.mt));
+        const A es = static_cast<A>(teach_exp2<T>(fmaf(fa[u], kT, -S.ms)));
+        const A et = static_cast<A>(teach_exp2<T>(fmaf(fb[u], kT, -S.mt)));
         zs += es;
         zt += et;
         if (direction == DIR_RKL) {
@@ -1394,7 +1440,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
                 float fa[NV], fb[NV];
                 cvt16<T>(vs[u], fa);
                 cvt16<T>(vt[u], fb);
-                dl_vec<T, A, NV>(S, fa, fb, kT, direction);
+                dl_vec<T, A, NV>(S, fa, fb, kT, direction, raw_max<T>(vs[u]), raw_max<T>(vt[u]));
             }
         }
     } else {
@@ -1441,6 +1487,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     }
     if (w == 0) {
         if (l == 0) {
+            if (!masked) {
+                // dl_vec's cross sums are in raw logits
+                R.xa *= static_cast<A>(kT);
+                R.xb *= static_cast<A>(kT);
+                R.xq *= static_cast<A>(kT);
+            }
             // fp32 row statistics for 16-bit logits (far inside their 2e-3
             // tolerance, and one lane's serial work per row here), fp64 for fp32
             using M = typename std::conditional<sizeof(T) == 2, float, double>::type;
@@ -1482,11 +1534,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     if (!grad) return;
     __syncthreads();
     const float ls2 = sP[0], lt2 = sP[1], pz = sP[2], pw = sP[3];
-    const float ln2f = static_cast<float>(LN2);
-    auto gval = [&](float a, float b) {
-        const float qv = teach_exp2<T>(a - ls2);
-        if (direction == DIR_RKL) return pz * qv * fmaf(a - b, ln2f, pw);
-        return pz * qv - pw * teach_exp2<T>(b - lt2);
+    const float ln2f = static_cast<float>(LN2), kTln2 = kT * ln2f;
+    // the gradient of one element from its raw logits (a = fa kT, b = fb kT)
+    auto gval = [&](float fa, float fb) {
+        const float qv = teach_exp2<T>(fmaf(fa, kT, -ls2));
+        if (direction == DIR_RKL) return pz * qv * fmaf(fa - fb, kTln2, pw);
+        return pz * qv - pw * teach_exp2<T>(fmaf(fb, kT, -lt2));
     };
     T *g = grad + t * V;
     // In reverse KL a -inf student logit has q = 0 and a gradient of 0, where
@@ -1518,7 +1571,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
                 if (accumulate) load_vec<T>(g + i * NV, gv, false);
 #pragma unroll
                 for (int q = 0; q < NV; ++q) {
-                    const float v = gval(fs[q] * kT, ft[q] * kT);
+                    const float v = gval(fs[q], ft[q]);
                     gv[q] = accumulate ? gv[q] + v : v;
                 }
                 store_vec(g + i * NV, gv);
@@ -1527,8 +1580,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
         return;
     }
     for (int64_t i = tid; i < V; i += NT) {
-        const float a = to_f(xs[i]) * kT;
-        float v = direction == DIR_RKL && teach_exp2<T>(a - ls2) == 0.f ? 0.f : gval(a, to_f(xt[i]) * kT);
+        const float fa = to_f(xs[i]);
+        float v = direction == DIR_RKL && teach_exp2<T>(fmaf(fa, kT, -ls2)) == 0.f ? 0.f : gval(fa, to_f(xt[i]));
         if (accumulate) v += to_f(g[i]);
         from_f(v, g[i]);
     }
