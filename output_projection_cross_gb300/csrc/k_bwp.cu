@@ -442,10 +442,27 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
         // before any wait a warp could unwind from.
         const int n_own_all = crank < a.n_loop ? (a.n_loop - crank + c - 1) / c : 0;
         const bool pcache = !ROWS && a.n_split == 1 && n_own_all <= 4;
+        // Label-CE d_weight keeps a supertile's 256 token parameters (4 KB) as
+        // {x_j, c_j, x_j+1, c_j+1} pairs in the first 2 KB (the exponent shift
+        // and coefficient of two adjacent columns: one shared-memory load per two
+        // elements), the targets (int) in the next 1 KB and the one-hot
+        // coefficients a_j in the last; the other passes keep the float4 records.
+        constexpr bool PAIRS = !ROWS && !DISTILL;
+        auto put_param = [&](float4 *blk, int j, const float4 &p) {
+            if (PAIRS) {
+                float *f = reinterpret_cast<float *>(blk);
+                f[(j >> 1) * 4 + (j & 1) * 2] = p.x;
+                f[(j >> 1) * 4 + (j & 1) * 2 + 1] = p.y;
+                reinterpret_cast<int *>(f + 512)[j] = __float_as_int(p.w);
+                f[768 + j] = p.z;
+            } else {
+                blk[j] = p;
+            }
+        };
         if (pcache) {
             for (int i = r; i < n_own_all * BWD_BN; i += 128) {
                 const int t = ((i / BWD_BN) * c + crank) * BWD_BN + i % BWD_BN;
-                sPall[i] = t < a.n_tok ? a.tokp[t] : P0;
+                put_param(sPall + (i / BWD_BN) * BWD_BN, i % BWD_BN, t < a.n_tok ? a.tokp[t] : P0);
             }
             named_bar_sync(1, 128);
         }
@@ -496,7 +513,7 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
 #pragma unroll
                 for (int i = 0; i < BWD_BN / 32; ++i) {
                     const int t = loop0 + lane + i * 32;
-                    sP[lane + i * 32] = t < a.n_tok ? a.tokp[t] : P0;
+                    put_param(sP, lane + i * 32, t < a.n_tok ? a.tokp[t] : P0);
                 }
                 __syncwarp();
             }
@@ -588,6 +605,44 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                 }
                 tmem_ld_wait();
                 uint32_t pk[16];
+                if (!FUSED && !DISTILL) {
+                    // label CE: G = c p - a [v = y].  The one-hot term is added only in
+                    // the chunks that hold one: this row's target column (d_hidden),
+                    // or a column whose target is one of this warp's 32 rows (d_weight,
+                    // found with one load and one vote per chunk).
+                    float gf[32];
+                    if (ROWS) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            gf[i] = P.y * ex2_approx(fmaf(__uint_as_float(v[i]), L2E, -P.x));
+                        const int jr = rel - q * 32;
+                        if (static_cast<unsigned>(jr) < 32u) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (i == jr) gf[i] -= P.z;
+                        }
+                    } else {
+                        const float4 *pp = sPt + q * 16;             // the chunk's 16 column pairs
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float4 PP = pp[i >> 1];
+                            gf[i] = PP.y * ex2_approx(fmaf(__uint_as_float(v[i]), L2E, -PP.x));
+                            gf[i + 1] = PP.w * ex2_approx(fmaf(__uint_as_float(v[i + 1]), L2E, -PP.z));
+                        }
+                        const int *tg = reinterpret_cast<const int *>(sPt) + 512 + q * 32;
+                        const float *sa = reinterpret_cast<const float *>(sPt) + 768 + q * 32;
+                        const int row0w = w.fixed * 256 + hh * 128 + quad * 32;
+                        const uint32_t hit =
+                            __ballot_sync(0xffffffffu, static_cast<unsigned>(tg[lane] - row0w) < 32u);
+                        if (hit) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (((hit >> i) & 1u) && tg[i] == fixrow) gf[i] -= sa[i];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) pk[i >> 1] = pack_16x2<F16>(gf[i], gf[i + 1]);
+                } else {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float gg[2];
@@ -600,10 +655,6 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                             const float gv = ex2_approx(fmaf(s, L2E, -Pq.x));
                             gg[uu] = gv;
                             zt += j < ncols ? gv : 0.f;
-                        } else if (!DISTILL) {
-                            float gv = Pq.y * ex2_approx(fmaf(s, L2E, -Pq.x));
-                            if (ROWS ? (rel == j) : (__float_as_int(Pq.w) == fixrow)) gv -= Pq.z;
-                            gg[uu] = gv;
                         } else {
                             const float tv = uu ? h16_hi<F16>(tcur[i >> 1]) : h16_lo<F16>(tcur[i >> 1]);
                             const float a2 = s * kT, b2 = tv * kT;
@@ -615,6 +666,7 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                         }
                     }
                     pk[i >> 1] = pack_16x2<F16>(gg[0], gg[1]);
+                }
                 }
                 // columns q*32 .. q*32+31: sub-tile q/4, 64 bytes at column (q%4)*32
                 if (GSTG && a.g_tma) {

@@ -1345,9 +1345,9 @@ __device__ __forceinline__ void dl_merge(DlState<A> &S, const DlState<A> &O)
 // independent exponentials, each argument one FFMA.  The cross sums take the
 // raw logits: a state built by dl_vec holds xa, xb and xq divided by kT (the
 // row kernel scales them back once).
-template <typename T, typename A, int NV>
+template <typename T, typename A, int NV, bool RKL>
 __device__ __forceinline__ void dl_vec(DlState<A> &S, const float (&fa)[NV], const float (&fb)[NV], float kT,
-                                       int direction, float lms, float lmt)
+                                       float lms, float lmt)
 {
     lms *= kT;
     lmt *= kT;
@@ -1374,7 +1374,7 @@ __device__ __forceinline__ void dl_vec(DlState<A> &S, const float (&fa)[NV], con
         const A et = static_cast<A>(teach_exp2<T>(fmaf(fb[u], kT, -S.mt)));
         zs += es;
         zt += et;
-        if (direction == DIR_RKL) {
+        if (RKL) {
             x1 += es * static_cast<A>(fa[u] - fb[u]);
         } else {
             x1 += et * static_cast<A>(fa[u]);
@@ -1383,7 +1383,7 @@ __device__ __forceinline__ void dl_vec(DlState<A> &S, const float (&fa)[NV], con
     }
     S.zs += zs;
     S.zt += zt;
-    if (direction == DIR_RKL) {
+    if (RKL) {
         S.xq += x1;
     } else {
         S.xa += x1;
@@ -1404,7 +1404,9 @@ template <typename T, typename A> __device__ __forceinline__ DlState<A> dl_shfl(
     return r;
 }
 
-template <typename T, int NT>
+// RKL: reverse KL (its own cross sum and gradient form); otherwise CE or
+// forward KL, which share them.
+template <typename T, int NT, bool RKL>
 __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     const T *__restrict__ student, const T *__restrict__ teacher, const uint8_t *__restrict__ mask,
     int64_t V, int direction, float kT, double wz, double at_on, double inv_t, float *__restrict__ lse_out,
@@ -1440,7 +1442,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
                 float fa[NV], fb[NV];
                 cvt16<T>(vs[u], fa);
                 cvt16<T>(vt[u], fb);
-                dl_vec<T, A, NV>(S, fa, fb, kT, direction, raw_max<T>(vs[u]), raw_max<T>(vt[u]));
+                dl_vec<T, A, NV, RKL>(S, fa, fb, kT, raw_max<T>(vs[u]), raw_max<T>(vt[u]));
             }
         }
     } else {
@@ -1538,18 +1540,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
     // the gradient of one element from its raw logits (a = fa kT, b = fb kT)
     auto gval = [&](float fa, float fb) {
         const float qv = teach_exp2<T>(fmaf(fa, kT, -ls2));
-        if (direction == DIR_RKL) return pz * qv * fmaf(fa - fb, kTln2, pw);
+        if (RKL) return pz * qv * fmaf(fa - fb, kTln2, pw);
         return pz * qv - pw * teach_exp2<T>(fmaf(fb, kT, -lt2));
     };
     T *g = grad + t * V;
     // In reverse KL a -inf student logit has q = 0 and a gradient of 0, where
     // gval's product q (a - b) would be 0 * -inf: rows that held a -inf take the
     // element-wise loop, which tests for it.
-    if (vec_ok && !(masked && direction == DIR_RKL)) {
+    if (vec_ok && !(masked && RKL)) {
         // the second read, last rounds first: the most recently read part of the
-        // rows is the most likely to be still in L2
+        // rows is the most likely to be still in L2 (one loop per accumulate mode)
         const int64_t nvec = V / NV;
         const int64_t nround = (nvec + NT * FL_U - 1) / (NT * FL_U);
+        auto pass2 = [&](auto acc_mode) {
+        constexpr bool ACC = decltype(acc_mode)::value;
         for (int64_t rr = nround - 1; rr >= 0; --rr) {
             const int64_t base = rr * NT * FL_U;
             uint4 vs[FL_U], vt[FL_U];
@@ -1568,20 +1572,23 @@ __global__ void __launch_bounds__(NT, 1024 / NT) distill_logits_kernel(
                 float fs[NV], ft[NV], gv[NV];
                 cvt16<T>(vs[u], fs);
                 cvt16<T>(vt[u], ft);
-                if (accumulate) load_vec<T>(g + i * NV, gv, false);
+                if (ACC) load_vec<T>(g + i * NV, gv, false);
 #pragma unroll
                 for (int q = 0; q < NV; ++q) {
                     const float v = gval(fs[q], ft[q]);
-                    gv[q] = accumulate ? gv[q] + v : v;
+                    gv[q] = ACC ? gv[q] + v : v;
                 }
                 store_vec(g + i * NV, gv);
             }
         }
+        };
+        if (accumulate) pass2(std::true_type{});
+        else pass2(std::false_type{});
         return;
     }
     for (int64_t i = tid; i < V; i += NT) {
         const float fa = to_f(xs[i]);
-        float v = direction == DIR_RKL && teach_exp2<T>(fmaf(fa, kT, -ls2)) == 0.f ? 0.f : gval(fa, to_f(xt[i]));
+        float v = RKL && teach_exp2<T>(fmaf(fa, kT, -ls2)) == 0.f ? 0.f : gval(fa, to_f(xt[i]));
         if (accumulate) v += to_f(g[i]);
         from_f(v, g[i]);
     }
@@ -1594,11 +1601,18 @@ static void launch_dl_t(const void *student, const void *teacher, const uint8_t 
 {
     const T *xs = static_cast<const T *>(student), *xt = static_cast<const T *>(teacher);
     T *g = static_cast<T *>(grad);
-    if (grad)
-        distill_logits_kernel<T, FL_THREADS_GRAD><<<static_cast<unsigned>(n), FL_THREADS_GRAD, 0, st>>>(
+    const unsigned grid = static_cast<unsigned>(n);
+    if (grad && direction == DIR_RKL)
+        distill_logits_kernel<T, FL_THREADS_GRAD, true><<<grid, FL_THREADS_GRAD, 0, st>>>(
+            xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
+    else if (grad)
+        distill_logits_kernel<T, FL_THREADS_GRAD, false><<<grid, FL_THREADS_GRAD, 0, st>>>(
+            xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
+    else if (direction == DIR_RKL)
+        distill_logits_kernel<T, FL_THREADS_STAT, true><<<grid, FL_THREADS_STAT, 0, st>>>(
             xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
     else
-        distill_logits_kernel<T, FL_THREADS_STAT><<<static_cast<unsigned>(n), FL_THREADS_STAT, 0, st>>>(
+        distill_logits_kernel<T, FL_THREADS_STAT, false><<<grid, FL_THREADS_STAT, 0, st>>>(
             xs, xt, mask, V, direction, kT, wz, at_on, inv_t, lse_out, per_token, tokacc, n_pad, g, accumulate);
 }
 
