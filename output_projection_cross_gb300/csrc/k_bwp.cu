@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
         int tiss_all = 0, tuse_all = 0;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float L2E = static_cast<float>(LOG2E);
-        const float kT = a.inv_t_l2e;
+        const float kT = a.inv_t_l2e, kTln2 = kT * static_cast<float>(LN2);
         const float4 P0 = DISTILL ? make_float4(0.f, 0.f, 0.f, 0.f)
                                   : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
         int m_all = 0;                                // own logit tiles consumed so far
@@ -605,7 +605,30 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                 }
                 tmem_ld_wait();
                 uint32_t pk[16];
-                if (!FUSED && !DISTILL) {
+                if (FUSED) {
+                    // G' = 2^(s log2e - r_t); the chunk's sum of G' over the valid vocabulary
+                    // columns in two partial sums (a chunk past the vocabulary's end tests
+                    // each column)
+                    float gf[32], z0 = 0.f, z1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) gf[i] = ex2_approx(fmaf(__uint_as_float(v[i]), L2E, -P.x));
+                    if (q * 32 + 32 <= ncols) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            z0 += gf[i];
+                            z1 += gf[i + 1];
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            z0 += q * 32 + i < ncols ? gf[i] : 0.f;
+                            z1 += q * 32 + i + 1 < ncols ? gf[i + 1] : 0.f;
+                        }
+                    }
+                    zt += z0 + z1;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) pk[i >> 1] = pack_16x2<F16>(gf[i], gf[i + 1]);
+                } else if (!DISTILL) {
                     // label CE: G = c p - a [v = y].  The one-hot term is added only in
                     // the chunks that hold one: this row's target column (d_hidden),
                     // or a column whose target is one of this warp's 32 rows (d_weight,
@@ -651,19 +674,14 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                         const int j = q * 32 + i + uu;           // loop column within the supertile
                         const float s = __uint_as_float(v[i + uu]);
                         const float4 Pq = ROWS ? P : sPt[j];
-                        if (FUSED) {
-                            const float gv = ex2_approx(fmaf(s, L2E, -Pq.x));
-                            gg[uu] = gv;
-                            zt += j < ncols ? gv : 0.f;
-                        } else {
-                            const float tv = uu ? h16_hi<F16>(tcur[i >> 1]) : h16_lo<F16>(tcur[i >> 1]);
-                            const float a2 = s * kT, b2 = tv * kT;
-                            const float qv = ex2_approx(a2 - Pq.x);
-                            if (a.direction == DIR_RKL)
-                                gg[uu] = Pq.z * qv * fmaf(a2 - b2, static_cast<float>(LN2), Pq.w);
-                            else
-                                gg[uu] = Pq.z * qv - Pq.w * ex2_approx(b2 - Pq.y);
-                        }
+                        // distillation: the student's and teacher's logits scaled by log2e / T
+                        // inside one FFMA each
+                        const float tv = uu ? h16_hi<F16>(tcur[i >> 1]) : h16_lo<F16>(tcur[i >> 1]);
+                        const float qv = ex2_approx(fmaf(s, kT, -Pq.x));
+                        if (a.direction == DIR_RKL)
+                            gg[uu] = Pq.z * qv * fmaf(s - tv, kTln2, Pq.w);
+                        else
+                            gg[uu] = Pq.z * qv - Pq.w * ex2_approx(fmaf(tv, kT, -Pq.y));
                     }
                     pk[i >> 1] = pack_16x2<F16>(gg[0], gg[1]);
                 }
