@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
                 if (q * 32 >= ncols) break;
                 uint32_t v[32];
                 tmem_ld32(tbuf + q * 32, v);
-                float bt[32];
+                float bt[32];                                  // raw teacher logits of the chunk
                 if (DISTILL) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(trow_g + q * 32);
 #pragma unroll
@@ -207,19 +207,22 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
                         const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            bt[c4 * 8 + 2 * e] = h16_lo<F16>(ww[e]) * kS;
-                            bt[c4 * 8 + 2 * e + 1] = h16_hi<F16>(ww[e]) * kS;
+                            bt[c4 * 8 + 2 * e] = h16_lo<F16>(ww[e]);
+                            bt[c4 * 8 + 2 * e + 1] = h16_hi<F16>(ww[e]);
                         }
                     }
                 }
                 tmem_ld_wait();
-                float f[32];
-                float cm = -INFINITY;
+                // The chunk's terms from the raw logits: its maximum first (kS > 0
+                // commutes with it), each exponent argument one FFMA, the cross sum in
+                // raw logits scaled once.  Only the vocabulary's last chunk tests its
+                // columns.
+                const bool full = q * 32 + 32 <= ncols;
+                float cr = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    f[i] = (q * 32 + i < ncols) ? __uint_as_float(v[i]) * kS : -INFINITY;
-                    cm = fmaxf(cm, f[i]);
-                }
+                for (int i = 0; i < 32; ++i)
+                    if (full || q * 32 + i < ncols) cr = fmaxf(cr, __uint_as_float(v[i]));
+                const float cm = cr * kS;
                 if (cm > m2) {
                     const float sc = ex2_approx(m2 - cm);
                     z *= sc;
@@ -229,16 +232,17 @@ __global__ void __launch_bounds__(192, 1) fwd2_kernel(const __grid_constant__ Tc
                 float acc = 0.f, xa = 0.f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float e = ex2_approx(f[i] - m2);
+                    const bool in = full || q * 32 + i < ncols;
+                    const float sv = __uint_as_float(v[i]);
+                    const float e = in ? ex2_approx(fmaf(sv, kS, -m2)) : 0.f;
                     acc += e;
                     if (DISTILL) {
-                        const bool in = q * 32 + i < ncols;
-                        if (a.direction == DIR_RKL) xa = fmaf(e, in ? f[i] - bt[i] : 0.f, xa);
-                        else xa = fmaf(in ? ex2_approx(bt[i] - lt2) : 0.f, in ? f[i] : 0.f, xa);
+                        if (a.direction == DIR_RKL) xa = fmaf(e, sv - bt[i], xa);
+                        else xa = fmaf(in ? ex2_approx(fmaf(bt[i], kS, -lt2)) : 0.f, sv, xa);
                     }
                 }
                 z += acc;
-                x += xa;
+                x += xa * kS;
             }
             if (row_ok) {
                 const int64_t o = static_cast<int64_t>(vt) * a.part_stride + t;
