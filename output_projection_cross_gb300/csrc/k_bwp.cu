@@ -819,6 +819,37 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                         bulk_commit_group();
                     }
                 }
+            } else if (ROWS && a.out3_tma) {
+                // d_hidden (or its split partial): the same staging, stored (or added)
+                // as boxes of this split's plane, which clip at n_tok
+                uint8_t *stg = gblk;
+                const int row0 = w.fixed * 256 + hh * 128 + quad * 32;
+                const uint32_t sb = smem_u32(stg) + static_cast<uint32_t>(lane) * 128;
+#pragma unroll 1
+                for (int q = 0; q < TC_SLICE / 32; ++q) {
+                    const int col = slice0 + q * 32;
+                    if (col >= a.d || row0 >= a.n_tok) break;
+                    uint32_t v[32];
+                    tmem_ld32(trow + ACC_COL + q * 32, v);
+                    tmem_ld_wait();
+                    if (F16) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a.out_scale);
+                    }
+                    if (lane == 0) bulk_wait_read_all();            // the block's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq)
+                        st_shared_v4(sb + ((static_cast<uint32_t>(kq) ^ (lane & 7)) << 4), v[4 * kq], v[4 * kq + 1],
+                                     v[4 * kq + 2], v[4 * kq + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (a.accumulate) tma_reduce_add_3d(&a.map_out3, stg, col, row0, split);
+                        else tma_store_3d(&a.map_out3, stg, col, row0, split);
+                        bulk_commit_group();
+                    }
+                }
             } else {
                 // Two 32-column chunks per TMEM wait; full chunks leave as 32-byte
                 // stores (rows are d_model floats apart, d_model % 8 == 0, so every

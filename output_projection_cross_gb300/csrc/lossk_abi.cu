@@ -129,6 +129,23 @@ bool make_map_out_f32(CUtensorMap *m, void *base, int64_t inner, int64_t outer)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [planes][rows][inner] (a d_hidden pass's partial slabs, or d_hidden itself),
+// 32 x 32 boxes of one plane: a box's rows past `rows` are clipped, never
+// written into the next plane.
+bool make_map_out3_f32(CUtensorMap *m, void *base, int64_t inner, int64_t rows, int64_t planes)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || inner % 4 != 0) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(planes)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 4, static_cast<cuuint64_t>(inner * rows) * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_blocks(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, uint32_t box_outer,
                      uint32_t nblk)
 {
@@ -402,6 +419,8 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             // d_weight leaves TMEM through shared memory and TMA stores (row-per-
             // thread global stores would touch 32 lines per warp instruction)
             a.out_tma = (!rows && !distill && make_map_out_f32(&a.map_out, dst, d, V)) ? 1 : 0;
+            // d_hidden: the accumulators leave through TMA stores too (per split plane)
+            a.out3_tma = (rows && make_map_out3_f32(&a.map_out3, a.out, d, n, a.out == dst ? 1 : L.nsplit)) ? 1 : 0;
             const int n_units = a.n_fixed * a.n_split * a.n_dg;
             {
                 Launch k(rows ? KK_TC_ROWS : KK_TC_COLS, st);
@@ -498,6 +517,7 @@ int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, c
     a.inv_t_l2e = static_cast<float>(LOG2E);
     float *part = L.nsplit > 1 ? w.dhpart() : d_hidden;
     a.out = part;
+    a.out3_tma = make_map_out3_f32(&a.map_out3, part, d, n, L.nsplit > 1 ? L.nsplit : 1) ? 1 : 0;
     a.out_split_stride = n * d;
     a.zpart = w.zpart();
     a.zpart_stride = L.n_pad;
