@@ -60,10 +60,14 @@
 // units.  Step i of the schedule issues round i's own logit tile and the
 // accumulates of round i-1 (possibly of the previous unit).
 //
-// Roles per CTA (192 threads): warp 0 loads this CTA's operand halves with TMA
+// Roles per CTA (224 threads): warp 0 loads this CTA's operand halves with TMA
 // (counted on the even CTA's stage barrier), warp 1 owns the pair's tensor
 // memory and, in the even CTA, issues the pair's MMAs; warps 2-5 are the
-// epilogue (one logit-tile row per thread).  TMEM per CTA: one 256-column
+// epilogue (one logit-tile row per thread); warp 6 watches the group's publish
+// counts in global memory ahead of the loader and hands each writer's count to
+// it in shared memory, so the L2 round trip of that check is off the loader's
+// path (it otherwise held the MMAs up at the first stage of every grad tile
+// but a round's first).  TMEM per CTA: one 256-column
 // logit buffer and the 256-column accumulator.  Every wait is bounded.
 #include "lossk_internal.h"
 #include "ptx.cuh"
@@ -90,7 +94,8 @@ constexpr int B_STG = 32 * 32 * 4;
 static_assert(4 * B_STG == B_TEACH, "the staging blocks fill the teacher-block region");
 template <int MODE, bool DISTILL> constexpr int bwd_smem()
 {
-    return 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + (MODE == BWD_COLS ? B_TEACH : 0) + B_NBARS * 8 + 16;
+    return 1024 + B_NST * B_STAGE + 4 * BWD_BN * 16 + (MODE == BWD_COLS ? B_TEACH : 0) + B_NBARS * 8 + 16 +
+           4 * B_MAXC;
 }
 static_assert(bwd_smem<BWD_COLS, true>() <= 232448, "fits the 227 KB per-CTA shared memory limit");
 static_assert(B_NST <= 8, "stage masks fit a byte");
@@ -152,8 +157,9 @@ __device__ __forceinline__ void cnt_inc(int (&cnt)[B_MAXC], int i)
 // G / out_scale (every per-token coefficient without the common factor
 // grad_scale / N_valid, so it stays inside fp16's range) and the accumulator
 // is multiplied by out_scale when it is stored.
+constexpr int B_THREADS = 224;
 template <int MODE, bool DISTILL, bool F16>
-__global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ BwdArgs a)
+__global__ void __launch_bounds__(B_THREADS, 1) bwp_kernel(const __grid_constant__ BwdArgs a)
 {
     constexpr bool FUSED = MODE == BWD_FUSED;
     constexpr bool ROWS = MODE != BWD_COLS;     // token rows x vocabulary columns
@@ -182,6 +188,7 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
     uint64_t *drain = accempty + 1;
     uint64_t *tbar = drain + 1;            // [4 warps][2] teacher block landed (TTMA)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(tbar + 8);
+    uint32_t *gseen = tslot + 4;           // [B_MAXC] tiles of each writer seen published (the poller's)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int *err = a.err;
@@ -226,6 +233,7 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
         mbar_init(accempty, 8);
         mbar_init(drain, 1);
         for (int i = 0; i < 8; ++i) mbar_init(&tbar[i], 1);
+        for (int i = 0; i < B_MAXC; ++i) gseen[i] = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc_pair(tslot, 512);
@@ -295,9 +303,9 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
                     const int wr = yy - y0;
                     const int cw = cnt_get(cnt, wr);
                     const int g = cw % G_SLOTS;
-                    // the writer's (cw / G_SLOTS)-th tile in slot g is published: 4 warp adds per tile
-                    if (!gsig_wait(&gready[wcta(wr) * G_SLOTS + g], 4u * static_cast<unsigned>(cw / G_SLOTS + 1),
-                                   err)) {
+                    // the writer's cw-th tile is published (the poller has seen it; its
+                    // acquire and this one order the tile's stores before the loads)
+                    if (!scnt_wait(smem_u32(&gseen[wr]), static_cast<unsigned>(cw + 1), err)) {
                         ok = false;
                         break;
                     }
@@ -414,7 +422,35 @@ __global__ void __launch_bounds__(192, 1) bwp_kernel(const __grid_constant__ Bwd
         }
         tc_commit_pair_multicast(drain, 1);
         bw_wait_drain(drain, 0);
-    } else if (warp >= 2) {
+    } else if (warp == 6 && lane == 0) {
+        // ================= grad-tile poller =================
+        // The loader's sequence of grad tiles (every round of every unit, the
+        // round's writers in order): wait until the writer's tile is published
+        // (its (cw / G_SLOTS)-th fill of slot cw % G_SLOTS: 4 warp adds per tile)
+        // and pass the count on.  It runs ahead of the loader as far as the
+        // writers allow, and a writer refills a slot only once this CTA has
+        // loaded it, so the counts stay in step with what the loader reads.
+        int cnt[B_MAXC] = {};
+        bool ok = true;
+        for (int u = group; u < n_units && ok; u += n_groups) {
+            const BwdUnit w = bwd_unit(a, u);
+            const int nr = (w.ny + c - 1) / c;
+            for (int rr = 0; rr < nr && ok; ++rr) {
+                const int y0 = rr * c, y_end = min(y0 + c, w.ny);
+                for (int yy = y0; yy < y_end; ++yy) {
+                    const int wr = yy - y0;
+                    const int cw = cnt_get(cnt, wr);
+                    if (!gsig_wait(&gready[wcta(wr) * G_SLOTS + cw % G_SLOTS],
+                                   4u * static_cast<unsigned>(cw / G_SLOTS + 1), err)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_cta_shared(smem_u32(&gseen[wr]), static_cast<unsigned>(cw + 1));
+                    cnt_inc(cnt, wr);
+                }
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
         // ================= epilogue =================
         const int quad = warp & 3;
         const int r = quad * 32 + lane;               // logit-tile row of this thread
@@ -929,7 +965,7 @@ static cudaError_t launch_bwp_one(const BwdArgs &a, int n_units, cudaStream_t st
     if (e != cudaSuccess) return e;
     const bool cache = dev >= 0 && dev < MAX_DEV;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(B_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

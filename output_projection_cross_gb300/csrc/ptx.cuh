@@ -165,6 +165,35 @@ __device__ __forceinline__ bool gsig_wait(const unsigned *ctr, unsigned target, 
     }
 }
 
+// A count handed from one thread of the CTA to another through shared memory
+// (release / acquire at CTA scope), and a bounded wait for it to reach a target.
+__device__ __forceinline__ void st_release_cta_shared(uint32_t saddr, unsigned v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_cta_shared(uint32_t saddr)
+{
+    unsigned v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool scnt_wait(uint32_t saddr, unsigned target, int *err,
+                                          uint64_t limit_ns = 2000000000ull)
+{
+    if (ld_acquire_cta_shared(saddr) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (ld_acquire_cta_shared(saddr) >= target) return true;
+        if (*reinterpret_cast<volatile int *>(err) != ERR_NONE) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(err, ERR_NONE, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ---- TMA --------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)

@@ -5,13 +5,15 @@ two CTAs of a pair act as one MMA unit and meet on the same barriers at the
 same points of their program, so the model takes one agent set per pair
 (the pair's barriers complete when both CTAs have arrived, which only delays
 them).  Per pair three agents run: the TMA producer, the MMA issuer and the
-epilogue.  Inside a pair they meet on mbarriers: the operand ring (full /
+epilogue, plus a poller that watches the group's publish counts and hands
+them to the producer through shared memory.  Inside a pair they meet on mbarriers: the operand ring (full /
 empty per stage), the TMEM logit buffer (tfull / tempty) and the accumulator
 (accfull / accempty).  Between the pairs of the group, the grad-tile ring
 (G_SLOTS slots per writer)
 is handed over through two monotonic counters per slot in global memory: the
 writer adds to `ready` once per tile (the kernel: one add per epilogue warp,
-four per tile) and a loader waits until it reaches the fill it needs; every
+four per tile) and a loader's poller waits until it reaches the fill it needs,
+then raises the loader's shared count of that writer's published tiles; every
 loader's MMA issuer adds to `free` once its loads of the tile have landed,
 and the writer waits for c adds per earlier fill before writing the slot
 again.  This model replays the kernel's program order for every agent of
@@ -102,8 +104,8 @@ def _cta_agents(j, c, nys, nk, B, S, free_short=0, ready_short=0):
                 for yy in range(r * c, min(r * c + c, ny)):
                     wr = yy - r * c
                     g, u = cnt[wr] % G_SLOTS, cnt[wr] // G_SLOTS
-                    # the writer's u-th tile in slot g is published
-                    yield from _until(lambda: S["ready"][wr][g] >= u + 1 - ready_short)
+                    # the poller has seen the writer's tile published
+                    yield from _until(lambda: S["seen"][j][wr] >= cnt[wr] + 1)
                     for _ in range(4):
                         yield from acquire()
                         # the quarter is read now (the model's TMA completes at once)
@@ -112,6 +114,17 @@ def _cta_agents(j, c, nys, nk, B, S, free_short=0, ready_short=0):
                                             f"{S['fills'][wr][g] - 1}, expected {u}")
                     S["loaded"][j][wr][g] += 1
                     cnt[wr] += 1
+
+    def poller():
+        cnt = [0] * c
+        for k, r, ny in (p for _, p in steps if p is not None):
+            for yy in range(r * c, min(r * c + c, ny)):
+                wr = yy - r * c
+                g, u = cnt[wr] % G_SLOTS, cnt[wr] // G_SLOTS
+                # the writer's u-th tile in slot g is published
+                yield from _until(lambda: S["ready"][wr][g] >= u + 1 - ready_short)
+                S["seen"][j][wr] = cnt[wr] + 1
+                cnt[wr] += 1
 
     def mma():
         k_con = 0
@@ -185,14 +198,14 @@ def _cta_agents(j, c, nys, nk, B, S, free_short=0, ready_short=0):
             yield from _wait(B[j]["accfull"], k)
             B[j]["accempty"].arrive()
 
-    return [producer(), mma(), epilogue()]
+    return [producer(), poller(), mma(), epilogue()]
 
 
 def _run(c, nys, nk, seed, free_short=0, ready_short=0):
     B = [{"full": [Bar(1) for _ in range(NST)], "empty": [Bar(1) for _ in range(NST)],
           "tfull": Bar(1), "tempty": Bar(1), "accfull": Bar(1), "accempty": Bar(1)} for _ in range(c)]
     S = {"ready": [[0] * G_SLOTS for _ in range(c)], "free": [[0] * G_SLOTS for _ in range(c)],
-         "fills": [[0] * G_SLOTS for _ in range(c)],
+         "fills": [[0] * G_SLOTS for _ in range(c)], "seen": [[0] * c for _ in range(c)],
          "loaded": [[[0] * G_SLOTS for _ in range(c)] for _ in range(c)]}
     agents = [a for j in range(c) for a in _cta_agents(j, c, nys, nk, B, S, free_short, ready_short)]
     rng = random.Random(seed)
