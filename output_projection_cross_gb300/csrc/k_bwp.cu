@@ -819,15 +819,19 @@ __global__ void __launch_bounds__(B_THREADS, 1) bwp_kernel(const __grid_constant
             float *dst = a.out + static_cast<int64_t>(split) * a.out_split_stride +
                          static_cast<int64_t>(fixrow) * a.d;
             if (STG && a.out_tma) {
-                // d_weight: per 32-column chunk, each warp writes its 32 rows
-                // into its own 4 KB block (128-byte swizzle: the 16-byte piece k of
-                // row r sits at piece k ^ (r % 8), so a warp's stores hit every
-                // bank) and lane 0 stores the block with TMA, which also clips
-                // the vocabulary tail and d_model.  Only this warp waits on its
-                // block, so no barrier spans warps that may unwind apart.
+                // d_weight: per 16-column half chunk, each warp writes its 32 rows
+                // into one of the two 2 KB halves of its block, alternately (64-byte
+                // swizzle: the 16-byte piece k of row r sits at piece k ^ ((r / 2) % 4),
+                // so a warp's stores hit every bank), and lane 0 stores the half with
+                // TMA, which also clips the vocabulary tail and d_model.  A half is
+                // refilled once the store issued from it two half chunks before has
+                // read it: the TMA unit, busy with the operand loads, takes a while to
+                // get to a store, and with one buffer the warp waited for each.  Only
+                // this warp waits on its block, so no barrier spans warps that may
+                // unwind apart.
                 uint8_t *stg = gblk;
                 const int row0 = w.fixed * 256 + hh * 128 + quad * 32;
-                const uint32_t sb = smem_u32(stg) + static_cast<uint32_t>(lane) * 128;
+                const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3;
 #pragma unroll 1
                 for (int q = 0; q < TC_SLICE / 32; ++q) {
                     const int col = slice0 + q * 32;
@@ -839,20 +843,29 @@ __global__ void __launch_bounds__(B_THREADS, 1) bwp_kernel(const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a.out_scale);
                     }
-                    // the block's previous store has read it
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
 #pragma unroll
-                    for (int kq = 0; kq < 8; ++kq)
-                        st_shared_v4(sb + ((static_cast<uint32_t>(kq) ^ (lane & 7)) << 4), v[4 * kq], v[4 * kq + 1],
-                                     v[4 * kq + 2], v[4 * kq + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        // gradient accumulation: out += the accumulator, one add per element
-                        if (a.accumulate) tma_reduce_add_2d(&a.map_out, stg, col, row0);
-                        else tma_store_2d(&a.map_out, stg, col, row0);
-                        bulk_commit_group();
+                    for (int hq = 0; hq < 2; ++hq) {
+                        if (col + hq * 16 >= a.d) break;
+                        const int hc = 2 * q + hq;
+                        uint8_t *h = stg + (hc & 1) * (B_STG / 2);
+                        if (lane == 0) {
+                            if (hc == 0) bulk_wait_read_all();
+                            else if (hc >= 2) bulk_wait_read_but1();
+                        }
+                        __syncwarp();
+                        const uint32_t hb = smem_u32(h) + static_cast<uint32_t>(lane) * 64;
+#pragma unroll
+                        for (int kq = 0; kq < 4; ++kq)
+                            st_shared_v4(hb + ((static_cast<uint32_t>(kq) ^ sw) << 4), v[hq * 16 + 4 * kq],
+                                         v[hq * 16 + 4 * kq + 1], v[hq * 16 + 4 * kq + 2], v[hq * 16 + 4 * kq + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // gradient accumulation: out += the accumulator, one add per element
+                            if (a.accumulate) tma_reduce_add_2d(&a.map_out, h, col + hq * 16, row0);
+                            else tma_store_2d(&a.map_out, h, col + hq * 16, row0);
+                            bulk_commit_group();
+                        }
                     }
                 }
             } else if (ROWS && a.out3_tma) {
