@@ -174,7 +174,9 @@ __global__ void __launch_bounds__(B_THREADS, 1) bwp_kernel(const __grid_constant
     // d_weight: per-token parameters of a supertile's columns, one copy per epilogue warp
     float4 *sPall = reinterpret_cast<float4 *>(ring + B_NST * B_STAGE);
     constexpr bool TTMA = MODE == BWD_COLS && DISTILL;     // teacher blocks through TMA
-    constexpr bool STG = MODE == BWD_COLS && !DISTILL;     // accumulator staged for TMA stores
+    // the accumulator staged for TMA stores (in the distillation pass through the
+    // warp's teacher buffers, which hold nothing between tiles)
+    constexpr bool STG = MODE == BWD_COLS;
     constexpr bool GSTG = !TTMA;                           // grad tiles staged for TMA stores
     static_assert(4 * BWD_BN * 16 == 4 * B_STG, "the parameter region holds four staging blocks");
     uint8_t *tblk = reinterpret_cast<uint8_t *>(sPall + 4 * BWD_BN);   // [4 warps][2][32][32] bf16
@@ -867,6 +869,12 @@ __global__ void __launch_bounds__(B_THREADS, 1) bwp_kernel(const __grid_constant
                             bulk_commit_group();
                         }
                     }
+                }
+                // the teacher blocks of the next tile land in the same buffers: the
+                // stores have read them first
+                if (TTMA) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
                 }
             } else if (ROWS && a.out3_tma) {
                 // d_hidden (or its split partial): the same staging, stored (or added)

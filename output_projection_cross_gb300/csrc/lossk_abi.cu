@@ -418,7 +418,7 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
             a.out_scale = static_cast<float>(out_scale);
             // d_weight leaves TMEM through shared memory and TMA stores (row-per-
             // thread global stores would touch 32 lines per warp instruction)
-            a.out_tma = (!rows && !distill && make_map_out_f32(&a.map_out, dst, d, V)) ? 1 : 0;
+            a.out_tma = (!rows && make_map_out_f32(&a.map_out, dst, d, V)) ? 1 : 0;
             // d_hidden: the accumulators leave through TMA stores too (per split plane)
             a.out3_tma = (rows && make_map_out3_f32(&a.map_out3, a.out, d, n, a.out == dst ? 1 : L.nsplit)) ? 1 : 0;
             const int n_units = a.n_fixed * a.n_split * a.n_dg;

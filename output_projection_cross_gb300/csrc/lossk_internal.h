@@ -123,7 +123,7 @@ struct BwdArgs {
     CUtensorMap map_gst;   // the grad-tile ring for stores, box {32, 32} bf16, 64-byte swizzle
     int g_tma;             // map_gst is valid: grad tiles leave through shared memory and TMA
     CUtensorMap map_out;   // d_weight output [vocab][d_model] fp32, box {16, 32}, 64-byte swizzle
-    int out_tma;           // d_weight (no distillation): store (or, accumulating, add) through map_out
+    int out_tma;           // d_weight: store (or, accumulating, add) through map_out
     CUtensorMap map_out3;  // d_hidden passes: `out` as fp32 [planes][n_tok][d_model], box {32, 32, 1}, 128-byte swizzle
     int out3_tma;          // the d_hidden passes store (or add) their accumulators through map_out3
     uint16_t *gscr;        // the grad-tile ring itself
