@@ -431,13 +431,13 @@ int32_t lossk_selftest_wait(int32_t n_stages, int32_t n_arrive, int64_t limit_ns
  *    code are those of lossk_ce_from_logits (the two share them), 590
  *    included.
  *  - The first call on each device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress) and caches it; make that
- *    first call before any stream capture on that device.  The cached
+ *    that device current (cudaGetSymbolAddress) and caches it.  The cached
  *    address is that of the device's primary context: after a
  *    cudaDeviceReset of a device, do not call this entry point on it again
  *    in the same process.
  *  - Like lossk_ce_from_logits, each call synchronises `stream` once, after
- *    its validation kernel, to read back the target-range flag.
+ *    its validation kernel, to read back the target-range flag, so a call
+ *    cannot be recorded into a CUDA graph.
  *  - All calls share the one array, which keeps the previous call's
  *    contents; each call clears the header before use.  Calls that overlap
  *    on the GPU (two streams, or two host threads on one device) race on it
