@@ -37,8 +37,9 @@
 // stage have landed: it announces completed reads and never holds the
 // issuer), writes, waits for its TMA stores to complete, fences and adds to
 // the slot's ready count (one release add per epilogue warp: they publish the
-// tile); a loader's TMA producer waits for the ready count (acquire) before
-// loading.  Groups are not clusters: only the two CTAs of a pair form a
+// tile); a loader CTA's poller warp waits for the ready count (acquire) and
+// passes it to the CTA's TMA producer in shared memory, which then loads the
+// tile.  Groups are not clusters: only the two CTAs of a pair form a
 // cluster (cta_group::2 needs one), and a group's pairs wait on each other
 // through global memory, which is safe as the grid never holds more pairs
 // than fit at once (every CTA of the grid is resident).  Groups of 4 pairs
