@@ -49,7 +49,12 @@
  *    kernel after it returns at once on the device when it found a target out
  *    of range (so a 586 still leaves every output untouched), and the end
  *    read-back carries the validation result with the range flag of the
- *    single-pass forward (see there).  The
+ *    single-pass forward (see there).  Those calls also run the token mean
+ *    and d_hidden's last kernel on a helper stream the library keeps for
+ *    each calling stream (up to 8 streams per device; a call on a further
+ *    stream runs them on `stream` itself) and join it back into `stream`
+ *    before returning, so calls on different streams never wait for each
+ *    other's helper work.  The
  *    read-backs go through a one-warp kernel writing into mapped pinned host
  *    memory, not through a copy engine, so large copies other streams have in
  *    flight do not delay them; the library allocates that memory (64 bytes

@@ -470,12 +470,18 @@ int32_t run_acc(const Ws &w, int64_t n, int64_t d, int64_t V, int32_t dtype, con
 // less than the separate forward and d_hidden passes.  A row whose shifted
 // terms left the trusted range raises the workspace's redo word; the caller
 // then recomputes everything on the separate passes.
-// A helper stream per device: the training step's small kernels that nothing
-// after them waits for (the token mean, d_hidden's combine) run on it beside
-// the d_weight pass, on the SMs its clusters leave free; the call joins it back
-// into the caller's stream before it returns.
+// A helper stream per (device, caller stream): the training step's small
+// kernels that nothing after them waits for (the token mean, d_hidden's
+// combine) run on it beside the d_weight pass, on the SMs its groups leave
+// free; the call joins it back into the caller's stream before it returns.
+// Calls on different caller streams get different helper streams, so neither
+// waits for the other's helper work.  Up to SIDE_PER_DEV caller streams per
+// device get one; a call on a further stream runs those kernels on its own
+// stream (the same results, without the overlap).
 struct SideStream {
     std::mutex mu;
+    cudaStream_t owner = nullptr;      // the caller stream this helper serves
+    bool used = false;
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
     bool ready()
@@ -492,12 +498,24 @@ struct SideStream {
     }
 };
 
-SideStream *side_stream()
+constexpr int SIDE_PER_DEV = 8;
+
+SideStream *side_stream(cudaStream_t caller)
 {
-    static SideStream sides[64];
+    static SideStream sides[64][SIDE_PER_DEV];
+    static std::mutex table_mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    return &sides[dev];
+    std::lock_guard<std::mutex> g(table_mu);
+    for (int i = 0; i < SIDE_PER_DEV; ++i)
+        if (sides[dev][i].used && sides[dev][i].owner == caller) return &sides[dev][i];
+    for (int i = 0; i < SIDE_PER_DEV; ++i)
+        if (!sides[dev][i].used) {
+            sides[dev][i].used = true;
+            sides[dev][i].owner = caller;
+            return &sides[dev][i];
+        }
+    return nullptr;
 }
 
 int32_t run_fused(const Ws &w, int64_t n, int64_t d, int64_t V, const void *H, const void *W,
@@ -889,7 +907,7 @@ static int32_t ce_common(bool do_fwd, bool do_bwd, int64_t n, int64_t d, int64_t
         if (!bwd_args(w, true, n, d, V, H, W, &fa) || (dW && !bwd_args(w, false, n, d, V, H, W, &ca)))
             return LOSSK_DEVICE_ERROR;
         float *dh_fused = acc ? w.dhacc() : dH;
-        SideStream *sd = acc ? nullptr : side_stream();
+        SideStream *sd = acc ? nullptr : side_stream(st);
         std::unique_lock<std::mutex> lk;
         cudaStream_t aux = st;
         if (sd) {

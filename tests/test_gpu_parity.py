@@ -632,6 +632,38 @@ def test_chunk_invariance_and_determinism(L, dtype):
             assert torch.equal(o[k], base[k]), (chunk, k)
 
 
+def test_calls_on_two_streams_match_one_stream(L):
+    """Training-step calls from two host threads, each on its own stream and
+    workspace (each caller stream gets its own helper stream for the token mean
+    and d_hidden's combine), give the bits of the same calls made one at a
+    time."""
+    import threading
+
+    n, d, V = 512, 256, 4000
+    x = _inputs("ce_512x1024x32000", seed=31, n_tok=n, d_model=d, vocab=V)
+    H, W, y = _dev(x["hidden"], "bf16"), _dev(x["weight"], "bf16"), _dev(x["targets"], "")
+    H2 = (H.float() * 0.5).to(torch.bfloat16)
+    ref = [L.lossk_ce_fwd_bwd(H, W, y, z_weight=0.01), L.lossk_ce_fwd_bwd(H2, W, y, z_weight=0.01)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        out = [None, None]
+
+        def run(i, Hx):
+            with torch.cuda.stream(streams[i]):
+                out[i] = L.lossk_ce_fwd_bwd(Hx, W, y, z_weight=0.01, stream=streams[i])
+
+        th = [threading.Thread(target=run, args=(0, H)), threading.Thread(target=run, args=(1, H2))]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+        torch.cuda.synchronize()
+        for i in range(2):
+            for k in ("lse", "ce", "scalars", "d_hidden", "d_weight"):
+                assert torch.equal(out[i][k], ref[i][k]), (i, k)
+
+
 def test_zero_weight_closed_form(L):
     n, d, V = 100, 64, 1000
     H = torch.randn(n, d, device="cuda").to(torch.bfloat16)
